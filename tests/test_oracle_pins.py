@@ -1,0 +1,366 @@
+"""Pins for the CPU oracle: each test ties an oracle function to something
+other than itself -- values the pages print, closed forms, an independent
+library routine (torch's float8 casts), invariants and brute force.
+
+Sources: "FP8 Training Infrastructure" (introl.com), section "O panorama da
+precisao numerica" (E4M3 up to +-448; E5M2 wider range); the MoE FP4 page
+("Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs"),
+section 2 "Metodologia" (32-element MXFP4 blocks, power-of-two scales,
+numerically equivalent FP4->FP8 conversion); OCP Microscaling v1.0 for the
+element encodings.
+"""
+import os
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import E4M3, E5M2, E2M1, UE4M3
+from block_scaled_precision_03_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ------------------------------------------------------------------ codecs
+def test_page_constants():
+    g = dict(_golden("format_constants.txt"))
+    assert oracle.max_finite(E4M3) == float(g["e4m3_max"])          # 448 (FP8 page)
+    assert oracle.BLOCK["mxfp4"] == int(g["mxfp4_block"])            # 32 (MoE FP4 page)
+    # NVFP4 4 + 8/16 = 4.5 bit/elem vs FP8 8 bit: ~1.8x (FP8 page)
+    nv_bits = 8.0 * (8192 * 4096 // 2 + oracle.scales_nbytes(8192, 4096 // 16)) / (8192 * 4096)
+    assert abs(8.0 / nv_bits - float(g["nvfp4_vs_fp8_memory"])) < 0.05
+    mx8_bits = 8.0 * (8192 * 4096 + oracle.scales_nbytes(8192, 4096 // 32)) / (8192 * 4096)
+    assert mx8_bits == 8.25 and nv_bits == 4.5
+
+
+def test_closed_form_extremes():
+    assert oracle.max_finite(E5M2) == 1.75 * 2 ** 15 == 57344.0
+    assert oracle.max_finite(E2M1) == 6.0
+    assert oracle.decode(E4M3, 0x01) == 2.0 ** -9
+    assert oracle.decode(E5M2, 0x01) == 2.0 ** -16
+    assert oracle.decode(E2M1, 0x1) == 0.5
+    assert oracle.decode_e8m0(127) == 1.0
+    assert oracle.decode_e8m0(0) == 2.0 ** -127
+    assert oracle.decode_e8m0(254) == 2.0 ** 127
+    assert math.isnan(oracle.decode_e8m0(255))
+
+
+def test_e2m1_value_set():
+    t = oracle.decode_table(E2M1)
+    assert list(t[:8]) == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    assert list(t[8:]) == [-0.0, -0.5, -1, -1.5, -2, -3, -4, -6]
+    assert math.copysign(1, t[8]) == -1
+
+
+@pytest.mark.parametrize("fmt,dt", [(E4M3, torch.float8_e4m3fn), (E5M2, torch.float8_e5m2)])
+def test_decode_matches_torch_float8(fmt, dt):
+    """All 256 codes decode exactly as torch's independent float8 types do."""
+    ours = oracle.decode_table(fmt)
+    ref = torch.arange(256, dtype=torch.uint8).view(dt).to(torch.float64).numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(ours[ok], ref[ok])
+    np.testing.assert_array_equal(np.signbit(ours[ok]), np.signbit(ref[ok]))
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2, E2M1])
+def test_roundtrip_and_monotonic(fmt):
+    t = oracle.decode_table(fmt)
+    half = len(t) // 2
+    for c, v in enumerate(t):
+        if math.isnan(v):
+            assert oracle.encode(fmt, v) == 0x7F
+        elif math.isinf(v):
+            # saturating encode: Inf maps to the largest finite magnitude
+            assert oracle.decode(fmt, oracle.encode(fmt, v)) == math.copysign(oracle.max_finite(fmt), v)
+        else:
+            assert oracle.encode(fmt, v) == c, (fmt, c, v)
+    pos = t[:half]
+    pos = pos[np.isfinite(pos)]
+    assert np.all(np.diff(pos) > 0)
+
+
+@pytest.mark.parametrize("fmt", [E4M3, E5M2, E2M1])
+def test_midpoints_round_to_even(fmt):
+    t = oracle.decode_table(fmt)
+    n = {E4M3: 127, E5M2: 124, E2M1: 8}[fmt]
+    for i in range(n - 1):
+        lo, hi = t[i], t[i + 1]
+        mid = (lo + hi) / 2
+        even = i if i % 2 == 0 else i + 1
+        assert oracle.encode(fmt, mid) == even
+        assert oracle.encode(fmt, -mid) == even | (0x8 if fmt == E2M1 else 0x80)
+        assert oracle.encode(fmt, np.nextafter(mid, 0)) == i
+        assert oracle.encode(fmt, np.nextafter(mid, np.inf)) == i + 1
+    # saturation above the largest finite value
+    mx = oracle.max_finite(fmt)
+    assert oracle.decode(fmt, oracle.encode(fmt, mx * 1.5)) == mx
+    assert oracle.decode(fmt, oracle.encode(fmt, -mx * 100)) == -mx
+
+
+def test_e2m1_golden_rounding():
+    for v, code in _golden("e2m1_rounding.txt"):
+        assert oracle.encode(E2M1, float(v)) == int(code, 16), v
+
+
+@pytest.mark.parametrize("fmt,dt", [(E4M3, torch.float8_e4m3fn), (E5M2, torch.float8_e5m2)])
+def test_encode_matches_torch_cast(fmt, dt):
+    """In range, RNE encode equals torch's float32 -> float8 cast."""
+    rng = np.random.default_rng(7)
+    mx = oracle.max_finite(fmt)
+    v = (rng.uniform(-1, 1, 4000) * np.exp2(rng.uniform(-24, math.log2(mx), 4000))).astype(np.float32)
+    v = np.clip(v, -mx, mx)
+    ref = torch.from_numpy(v).to(dt).view(torch.uint8).numpy()
+    ours = np.array([oracle.encode(fmt, float(x)) for x in v], dtype=np.uint8)
+    np.testing.assert_array_equal(ours, ref)
+
+
+# ------------------------------------------------------------- block scale
+def _blk(fmt, vals, n=32):
+    v = np.zeros(n)
+    v[:len(vals)] = vals
+    return oracle.mx_block(fmt, v)
+
+
+def test_block_scale_hand_cases():
+    # amax exactly a power of two: e = k - emax
+    c, s = _blk(E4M3, [2.0 ** 5, 1.0])
+    assert s == 127 + 5 - 8 and c[0] == oracle.encode(E4M3, 2.0 ** 8)
+    # amax = 448 * 2^k: top code, no saturation
+    c, s = _blk(E4M3, [448.0 * 2 ** -3])
+    assert s == 127 - 3 and c[0] == 0x7E
+    # amax just below 2^(k+1): scaled value 510 > 448 saturates to 448
+    c, s = _blk(E4M3, [1.9921875 * 2 ** 4])
+    assert s == 127 + 4 - 8 and c[0] == 0x7E
+    c, s = _blk(E2M1, [7.5, -1.0])
+    assert s == 127 + 2 - 2 and c[0] == 0x7 and c[1] == 0xA
+    c, s = _blk(E5M2, [3.0 * 2 ** -20])
+    assert s == 127 - 19 - 15 and oracle.decode(E5M2, c[0]) == 1.5 * 2 ** 15  # 3*2^-20 = 1.5*2^-19
+    # all-zero block
+    c, s = _blk(E4M3, [])
+    assert s == 0 and not c.any()
+    # NaN / Inf blocks
+    c, s = _blk(E4M3, [1.0, float("nan")])
+    assert s == 0xFF and (c == 0x7F).all()
+    c, s = _blk(E2M1, [float("inf")])
+    assert s == 0xFF and not c.any()
+    # single large outlier (the x50 activations): scale follows the outlier
+    v = np.full(32, 0.01)
+    v[3] = -50.0 * 1.3
+    c, s = oracle.mx_block(E4M3, v)
+    assert s == 127 + 6 - 8 and oracle.decode(E4M3, c[3]) * 2.0 ** (s - 127) == pytest.approx(-65.0, rel=2 ** -4)
+
+
+def test_block_scale_exponent_range_clamps():
+    c, s = _blk(E4M3, [2.0 ** -130])
+    assert s == 0
+    c, s = _blk(E2M1, [2.0 ** 127])
+    assert s == 127 + 127 - 2
+
+
+@pytest.mark.parametrize("fmt,top", [(E4M3, range(0x78, 0x7F)), (E5M2, range(0x78, 0x7C)), (E2M1, (6, 7))])
+def test_quantize_dequant_identity(fmt, top):
+    """Blocks whose values are code * 2^e with e the rule's exponent come back unchanged."""
+    rng = np.random.default_rng(fmt)
+    t = oracle.decode_table(fmt)
+    finite = [c for c in range(len(t)) if np.isfinite(t[c])]
+    for trial in range(200):
+        codes = rng.choice(finite, 32).astype(np.uint8)
+        codes[rng.integers(32)] = rng.choice(list(top)) | (0x80 if fmt != E2M1 and rng.random() < .5 else 0)
+        e = int(rng.integers(-100, 100))
+        vals = np.array([t[c] * 2.0 ** e for c in codes])
+        c2, s2 = oracle.mx_block(fmt, vals)
+        assert s2 == e + 127
+        np.testing.assert_array_equal(c2, codes)
+
+
+def test_mx_rows_matches_torch_pipeline():
+    """Whole-tensor E4M3 MX quantize equals: rule exponent, then torch's RNE cast
+    of the clamped scaled values (saturation is clamp-then-round)."""
+    x = inputs.outlier_activations_bf16((64, 256), seed=3)
+    codes, scales = oracle.mx_quantize_rows(x, "mxfp8_e4m3")
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64).reshape(64, 8, 32)
+    amax = np.abs(xf).max(axis=2)
+    e = np.floor(np.log2(amax)).astype(np.int64) - 8
+    np.testing.assert_array_equal(scales, e + 127)
+    scaled = np.clip(xf * np.exp2(-e)[:, :, None], -448, 448).astype(np.float32)
+    ref = torch.from_numpy(scaled.reshape(64, 256)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(codes, ref)
+
+
+# ------------------------------------------------------------------- NVFP4
+def test_nvfp4_tensor_amax_block():
+    x = inputs.normal_bf16((32, 64), seed=5)
+    xf = inputs.bf16_bits_to_f32(x)
+    r, c = np.unravel_index(np.argmax(np.abs(xf)), xf.shape)
+    codes, scales, s_t = oracle.nvfp4_quantize_rows(x)
+    amax = float(np.abs(xf).max())
+    assert s_t == float(np.float32(amax) / np.float32(2688.0))
+    assert scales[r, c // 16] == 0x7E                  # 448 = 2688 / 6
+    assert codes[r, c] & 0x7 == 0x7                    # magnitude 6
+    # dequantized values stay within half an E2M1 step of the block scale grid
+    deq = oracle.dequant_rows(codes, scales, "nvfp4", s_t)
+    assert np.all(np.abs(deq - xf) <= np.abs(xf) * 0.25 + 1e-30 + np.repeat(
+        oracle.decode_table(E4M3)[scales].reshape(32, 4, 1), 16, axis=2).reshape(32, 64) * s_t * 0.25)
+
+
+def test_nvfp4_zero_and_tiny_blocks():
+    x = np.zeros((1, 32), dtype=np.uint16)
+    x[0, 0] = inputs.f32_to_bf16_bits(np.array([1000.0], np.float32))[0]
+    x[0, 16] = inputs.f32_to_bf16_bits(np.array([1e-6], np.float32))[0]
+    codes, scales, s_t = oracle.nvfp4_quantize_rows(x)
+    assert scales[0, 0] == 0x7E and scales[0, 1] == 0 and not codes[0, 16:].any()
+    z = np.zeros((2, 16), dtype=np.uint16)
+    codes, scales, s_t = oracle.nvfp4_quantize_rows(z)
+    assert s_t == 1.0 and not scales.any() and not codes.any()
+
+
+def test_nvfp4_division_is_fp32():
+    """The E2M1 code is the RNE code of the FP32-rounded quotient x / d."""
+    x = inputs.normal_bf16((16, 256), seed=11)
+    codes, scales, s_t = oracle.nvfp4_quantize_rows(x)
+    xf = inputs.bf16_bits_to_f32(x).reshape(16, 16, 16)
+    sb = oracle.decode_table(E4M3)[scales].astype(np.float32)
+    d = (sb * np.float32(s_t)).astype(np.float32)
+    q = (xf / d[:, :, None]).astype(np.float32)
+    ref = np.array([oracle.encode(E2M1, float(v)) for v in q.ravel()]).reshape(16, 256)
+    ref[np.repeat(scales == 0, 16, axis=1)] = 0
+    np.testing.assert_array_equal(codes, ref)
+
+
+# ------------------------------------------------------------------- repack
+REPACK_SCALES = [0, 1, 2, 5, 6, 7, 8, 9, 10, 60, 117, 118, 119, 120, 127, 128, 200, 254, 255]
+
+
+def test_repack_preserves_values_exhaustive():
+    """dequant(repack(x)) == dequant(x) exactly, for every E2M1 code next to
+    every other code, over scales including the clamp edge near 2^-127."""
+    rows = []
+    for a in range(16):
+        for b in range(16):
+            blk = np.zeros(32, dtype=np.uint8)
+            blk[0], blk[1] = a, b
+            blk[2:] = (np.arange(30) * 7 + a) % 16
+            rows.append(blk)
+    codes = np.array(rows, dtype=np.uint8)
+    for s in REPACK_SCALES:
+        scales = np.full((codes.shape[0], 1), s, dtype=np.uint8)
+        c8, s8 = oracle.mxfp4_to_mxfp8_rows(codes, scales)
+        d4 = oracle.dequant_rows(codes, scales, "mxfp4")
+        d8 = oracle.dequant_rows(c8, s8, "mxfp8_e4m3")
+        if s == 255:
+            assert np.isnan(d8).all() and (s8 == 255).all()
+            continue
+        np.testing.assert_array_equal(d8, d4)
+        np.testing.assert_array_equal(np.signbit(d8), np.signbit(d4))
+
+
+def test_repack_integer_rule():
+    """For scales away from the E8M0 floor, the new scale is e + e_c - 8 where
+    e_c = floor(log2(max |code value|)), and each code is shifted exactly."""
+    rng = np.random.default_rng(1)
+    codes = rng.integers(0, 16, (500, 32)).astype(np.uint8)
+    scales = rng.integers(12, 250, (500, 1)).astype(np.uint8)
+    c8, s8 = oracle.mxfp4_to_mxfp8_rows(codes, scales)
+    t4 = oracle.decode_table(E2M1)
+    for r in range(500):
+        m = np.abs(t4[codes[r]]).max()
+        if m == 0:
+            assert s8[r, 0] == 0 and all(c in (0, 0x80) for c in c8[r])
+            continue
+        e_c = int(math.floor(math.log2(m)))
+        assert s8[r, 0] == scales[r, 0] + e_c - 8
+        for k in range(32):
+            assert oracle.decode(E4M3, c8[r, k]) == t4[codes[r, k]] * 2.0 ** (8 - e_c)
+
+
+# --------------------------------------------------------------------- GEMM
+def test_gemm_brute_force_integers():
+    """Hand-chosen codes whose values are small integers: the result must be
+    the exact integer dot product times 2^(eA + eB)."""
+    rng = np.random.default_rng(0)
+    int_codes = {v: oracle.encode(E4M3, v) for v in range(-16, 17)}
+    for M, N, K in [(1, 1, 32), (3, 5, 64), (8, 8, 32), (7, 2, 96)]:
+        Ai = rng.integers(-16, 17, (M, K))
+        Bi = rng.integers(-16, 17, (N, K))
+        Ac = np.vectorize(int_codes.get)(Ai).astype(np.uint8)
+        Bc = np.vectorize(int_codes.get)(Bi).astype(np.uint8)
+        eA = rng.integers(120, 135, (M, K // 32)).astype(np.uint8)
+        eB = rng.integers(120, 135, (N, K // 32)).astype(np.uint8)
+        A = oracle.dequant_rows(Ac, eA, "mxfp8_e4m3")
+        B = oracle.dequant_rows(Bc, eB, "mxfp8_e4m3")
+        ref, mag = oracle.gemm_full(A, B)
+        for m in range(M):
+            for n in range(N):
+                exact = sum(int(Ai[m, k]) * int(Bi[n, k]) * 2.0 ** (int(eA[m, k // 32]) + int(eB[n, k // 32]) - 254)
+                            for k in range(K))
+                absum = sum(abs(int(Ai[m, k]) * int(Bi[n, k])) * 2.0 ** (int(eA[m, k // 32]) + int(eB[n, k // 32]) - 254)
+                            for k in range(K))
+                assert ref[m, n] == exact and mag[m, n] == absum
+        ms, ns = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+        r2, g2 = oracle.gemm_pairs(A, B, ms.ravel(), ns.ravel())
+        np.testing.assert_array_equal(r2, ref.ravel())
+        np.testing.assert_array_equal(g2, mag.ravel())
+
+
+def test_gemm_single_block_is_integer_dot():
+    a = np.zeros((1, 32), np.uint8)
+    b = np.zeros((1, 32), np.uint8)
+    a[0, :4] = [oracle.encode(E4M3, v) for v in (1, 2, -3, 0.5)]
+    b[0, :4] = [oracle.encode(E4M3, v) for v in (4, -1, 2, 8)]
+    A = oracle.dequant_rows(a, np.array([[130]], np.uint8), "mxfp8_e4m3")
+    B = oracle.dequant_rows(b, np.array([[120]], np.uint8), "mxfp8_e4m3")
+    ref, mag = oracle.gemm_full(A, B)
+    assert ref[0, 0] == (4 - 2 - 6 + 4) * 2.0 ** (3 - 7)
+    assert mag[0, 0] == (4 + 2 + 6 + 4) * 2.0 ** (3 - 7)
+
+
+# ------------------------------------------------------------- scale layout
+def test_scale_layout_positions():
+    # hand-computed offsets: (r, c) in a [200, 9] scale matrix (S padded to 12)
+    assert oracle.scale_tile_offset(0, 0, 9) == 0
+    assert oracle.scale_tile_offset(1, 0, 9) == 16
+    assert oracle.scale_tile_offset(32, 0, 9) == 4
+    assert oracle.scale_tile_offset(33, 5, 9) == 512 + 16 + 4 + 1
+    assert oracle.scale_tile_offset(127, 3, 9) == 31 * 16 + 3 * 4 + 3
+    assert oracle.scale_tile_offset(128, 0, 9) == 3 * 512
+    assert oracle.scale_tile_offset(199, 8, 9) == (3 + 2) * 512 + (199 % 32) * 16 + (71 // 32) * 4
+
+
+def test_scale_layout_bijection_and_padding():
+    rng = np.random.default_rng(2)
+    for R, S in [(1, 1), (130, 9), (256, 128), (77, 4)]:
+        s = rng.integers(1, 255, (R, S)).astype(np.uint8)
+        buf = oracle.swizzle_scales(s)
+        assert buf.size == oracle.scales_nbytes(R, S) == ((R + 127) // 128 * 128) * ((S + 3) // 4 * 4)
+        np.testing.assert_array_equal(oracle.unswizzle_scales(buf, R, S), s)
+        pad = oracle.scale_pad_mask(R, S)
+        assert pad.sum() == buf.size - R * S and not buf[pad].any()
+
+
+def test_fp4_packing():
+    c = np.array([[1, 2, 3, 4, 0xF, 0x8]], np.uint8)
+    p = oracle.pack_fp4(c)
+    np.testing.assert_array_equal(p, [[0x21, 0x43, 0x8F]])
+    np.testing.assert_array_equal(oracle.unpack_fp4(p), c)
+
+
+def test_column_wise_is_transpose():
+    x = inputs.normal_bf16((64, 96), seed=4)
+    c1, s1, _ = oracle.quantize_cols(x, "mxfp8_e5m2")
+    c2, s2 = oracle.mx_quantize_rows(np.ascontiguousarray(x.T), "mxfp8_e5m2")
+    np.testing.assert_array_equal(c1, c2)
+    np.testing.assert_array_equal(s1, s2)
+    assert c1.shape == (96, 64)
