@@ -1,0 +1,211 @@
+// MXFP4 -> MXFP8 (E4M3) direct re-encode and exact dequantization.
+//
+// Re-encode ("Practical FP4 Training for Large-Scale MoE Models on Hopper
+// GPUs", section 2, "Algoritmo de Conversao Direta" and kernel
+// FP4RowToFP8Row): the conversion stays in the integer domain.  For a
+// 32-block with scale byte s and largest code magnitude exponent e_c the
+// new scale byte is s + e_c - 8 (floored at 0, the E8M0 minimum); each E2M1
+// nibble keeps its sign and mantissa bit and its exponent moves by the
+// shift between the two scales, so every value is carried over exactly.
+// There is no BF16 or FP32 intermediate.
+#include "common.cuh"
+#include "internal.h"
+
+namespace bsq {
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// 4 nibbles (low 16 bits of x) -> one byte each, nibble k in byte k.
+__device__ __forceinline__ uint32_t spread_nibbles(uint32_t x) {
+    x &= 0xFFFFu;
+    x = (x | (x << 8)) & 0x00FF00FFu;
+    x = (x | (x << 4)) & 0x0F0F0F0Fu;
+    return x;
+}
+
+// 8 E2M1 nibbles of w -> 8 E4M3 bytes given the magnitude table (lut_lo =
+// bytes for magnitudes 0..3, lut_hi = 4..7).
+__device__ __forceinline__ uint2 remap8(uint32_t w, uint32_t lut_lo, uint32_t lut_hi) {
+    const uint32_t m = w & 0x77777777u;
+    uint32_t lo = prmt(lut_lo, lut_hi, m & 0xFFFFu);
+    uint32_t hi = prmt(lut_lo, lut_hi, m >> 16);
+    lo |= (spread_nibbles(w) & 0x08080808u) << 4;
+    hi |= (spread_nibbles(w >> 16) & 0x08080808u) << 4;
+    return make_uint2(lo, hi);
+}
+
+__global__ void __launch_bounds__(256)
+repack_kernel(const uint4* __restrict__ in, const uint8_t* __restrict__ sin, uint4* __restrict__ out,
+              uint8_t* __restrict__ sout, int64_t nblocks, uint32_t bpr, int64_t s_tiles) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
+        const uint4 w = in[b];
+        const uint32_t r = (uint32_t)(b / bpr), j = (uint32_t)(b - (int64_t)r * bpr);
+        const int64_t off = sf_offset(r, j, s_tiles);
+        const uint32_t s = sin[off];
+        uint4 o0, o1;
+        uint32_t ns;
+        if (s == 0xFF) {
+            ns = 0xFF;
+            o0 = o1 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else {
+            // largest magnitude index over the 32 nibbles (value order = code order)
+            uint32_t mx = __vmaxu4(__vmaxu4(w.x & 0x07070707u, (w.x >> 4) & 0x07070707u),
+                                   __vmaxu4(w.y & 0x07070707u, (w.y >> 4) & 0x07070707u));
+            mx = __vmaxu4(mx, __vmaxu4(__vmaxu4(w.z & 0x07070707u, (w.z >> 4) & 0x07070707u),
+                                       __vmaxu4(w.w & 0x07070707u, (w.w >> 4) & 0x07070707u)));
+            mx = max(max(mx & 0xFF, (mx >> 8) & 0xFF), max((mx >> 16) & 0xFF, mx >> 24));
+            uint32_t lut_lo = 0, lut_hi = 0;
+            if (mx == 0) {
+                ns = 0;                                  // all-zero block: e = -127
+            } else {
+                // exponent of the largest magnitude: 0.5 -> -1, 1|1.5 -> 0, 2|3 -> 1, 4|6 -> 2
+                const int e_c = mx == 1 ? -1 : (int)(mx >> 1) - 1;
+                int nb = (int)s + e_c - 8;
+                if (nb < 0) nb = 0;
+                ns = (uint32_t)nb;
+                const uint32_t E = (uint32_t)((int)s - nb + 7);   // biased E4M3 exponent of magnitude 1.0
+                // E4M3 bytes of magnitudes 0, 0.5, 1, 1.5 | 2, 3, 4, 6 scaled by 2^(s - nb)
+                lut_lo = ((E - 1) << 11) | ((E << 3) << 16) | (((E << 3) | 4u) << 24);
+                lut_hi = ((E + 1) << 3) | ((((E + 1) << 3) | 4u) << 8) | (((E + 2) << 3) << 16) |
+                         ((((E + 2) << 3) | 4u) << 24);
+            }
+            const uint2 a = remap8(w.x, lut_lo, lut_hi), bb = remap8(w.y, lut_lo, lut_hi);
+            const uint2 c = remap8(w.z, lut_lo, lut_hi), d = remap8(w.w, lut_lo, lut_hi);
+            o0 = make_uint4(a.x, a.y, bb.x, bb.y);
+            o1 = make_uint4(c.x, c.y, d.x, d.y);
+        }
+        out[2 * b] = o0;
+        out[2 * b + 1] = o1;
+        sout[off] = (uint8_t)ns;
+    }
+}
+
+cudaError_t run_repack(const RepackArgs& a, cudaStream_t st) {
+    cudaError_t e;
+    if (a.scales_pad && (e = cudaMemsetAsync(a.out_scales, 0, a.scales_bytes, st)) != cudaSuccess) return e;
+    const int64_t nblocks = a.rows * (a.cols / 32);
+    int64_t grid = (nblocks + 255) / 256;
+    if (grid > (int64_t)a.num_sms * 16) grid = (int64_t)a.num_sms * 16;
+    if (grid < 1) grid = 1;
+    const uint32_t bpr = (uint32_t)(a.cols / 32);
+    repack_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(a.in_codes), a.in_scales,
+                                                 reinterpret_cast<uint4*>(a.out_codes), a.out_scales, nblocks,
+                                                 bpr, (bpr + 3) / 4);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Dequantize: value = code * scale (* tensor scale), rounded once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float e5m2_to_float(uint32_t b) {
+    // an E5M2 byte is the high byte of the binary16 with the same value
+    return __half2float(__ushort_as_half((uint16_t)((b & 0xFF) << 8)));
+}
+__device__ __forceinline__ float e2m1_to_float(uint32_t n) {
+    const float mag[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+    const float v = mag[n & 7];
+    return (n & 8) ? -v : v;
+}
+__device__ __forceinline__ float e8m0_to_float(uint32_t s) {
+    if (s == 0xFF) return __uint_as_float(0x7FC00000u);
+    if (s == 0) return __uint_as_float(0x00400000u);    // 2^-127 (subnormal)
+    return __uint_as_float(s << 23);
+}
+
+// Round the exact product p*q (FP32 inputs) once to BF16, nearest-even:
+// hi = RN(p*q), lo = p*q - hi exactly (FMA two-product, Ogita-Rump-Oishi
+// 2005); when hi sits exactly on a BF16 midpoint the residual decides.
+__device__ __forceinline__ uint16_t mul_round_bf16(float p, float q) {
+    const float hi = __fmul_rn(p, q);
+    const float lo = __fmaf_rn(p, q, -hi);
+    uint32_t u = __float_as_uint(hi);
+    if ((u & 0x7F800000u) == 0x7F800000u) return __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    if ((u & 0xFFFFu) == 0x8000u && lo != 0.0f) {
+        // exact value is above or below the midpoint in magnitude
+        const bool away = (lo > 0.0f) == (hi > 0.0f);
+        return (uint16_t)((u >> 16) + (away ? 1u : 0u));
+    }
+    return __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(256)
+dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, const float* __restrict__ ts,
+               int64_t nchunks, uint32_t cols, int64_t s_tiles, void* __restrict__ dst, int out_bf16) {
+    constexpr int BLK = block_of(FMT);
+    const float s_t = FMT == kNVFP4 ? *ts : 1.0f;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < nchunks; c += stride) {
+        const int64_t e0 = c * 8;
+        const uint32_t r = (uint32_t)(e0 / cols), k = (uint32_t)(e0 - (int64_t)r * cols);
+        const uint32_t sb = scales[sf_offset(r, k / BLK, s_tiles)];
+        float v[8];
+        if (is_fp4(FMT)) {
+            const uint32_t w = reinterpret_cast<const uint32_t*>(codes)[c];
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] = e2m1_to_float(w >> (4 * i));
+        } else {
+            const uint2 w = reinterpret_cast<const uint2*>(codes)[c];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const uint32_t b = ((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFF;
+                v[i] = FMT == kE4M3 ? e4m3_to_float(b) : e5m2_to_float(b);
+            }
+        }
+        if (FMT == kNVFP4) {
+            const float sv = sb == 0x7F ? __uint_as_float(0x7FC00000u) : e4m3_to_float(sb);
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] = __fmul_rn(v[i], sv);     // exact: <= 6 significant bits
+            if (out_bf16) {
+                uint32_t o[4];
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    o[i] = (uint32_t)mul_round_bf16(v[2 * i], s_t) | ((uint32_t)mul_round_bf16(v[2 * i + 1], s_t) << 16);
+                reinterpret_cast<uint4*>(dst)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+                continue;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] = __fmul_rn(v[i], s_t);
+        } else {
+            const float f = e8m0_to_float(sb);
+#pragma unroll
+            for (int i = 0; i < 8; i++) v[i] = __fmul_rn(v[i], f);     // exact (power of two)
+        }
+        if (out_bf16) {
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++)
+                o[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i])) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * i + 1])) << 16);
+            reinterpret_cast<uint4*>(dst)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            float4* d = reinterpret_cast<float4*>(dst) + 2 * c;
+            d[0] = make_float4(v[0], v[1], v[2], v[3]);
+            d[1] = make_float4(v[4], v[5], v[6], v[7]);
+        }
+    }
+}
+
+cudaError_t run_dequant(const DequantArgs& a, cudaStream_t st) {
+    const int64_t nchunks = a.rows * a.cols / 8;
+    int64_t grid = (nchunks + 255) / 256;
+    if (grid > (int64_t)a.num_sms * 16) grid = (int64_t)a.num_sms * 16;
+    if (grid < 1) grid = 1;
+    const int64_t S = a.cols / block_of(a.fmt);
+    const int64_t st_ = (S + 3) / 4;
+    const uint32_t cols = (uint32_t)a.cols;
+    switch (a.fmt) {
+    case kE4M3: dequant_kernel<kE4M3><<<(unsigned)grid, 256, 0, st>>>(a.codes, a.scales, a.ts, nchunks, cols, st_, a.dst, a.out_bf16); break;
+    case kE5M2: dequant_kernel<kE5M2><<<(unsigned)grid, 256, 0, st>>>(a.codes, a.scales, a.ts, nchunks, cols, st_, a.dst, a.out_bf16); break;
+    case kMXFP4: dequant_kernel<kMXFP4><<<(unsigned)grid, 256, 0, st>>>(a.codes, a.scales, a.ts, nchunks, cols, st_, a.dst, a.out_bf16); break;
+    default: dequant_kernel<kNVFP4><<<(unsigned)grid, 256, 0, st>>>(a.codes, a.scales, a.ts, nchunks, cols, st_, a.dst, a.out_bf16); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace bsq

@@ -1,0 +1,69 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace bsq {
+
+struct QuantizeArgs {
+    const void* src;
+    int64_t rows, cols;
+    int fmt, axis;
+    uint8_t *row_codes, *row_scales, *col_codes, *col_scales;
+    float *row_ts, *col_ts;
+    size_t row_scales_bytes, col_scales_bytes;
+    bool row_scales_pad, col_scales_pad;     // buffer has padding to zero
+    int num_sms;
+};
+cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st);
+
+struct RepackArgs {
+    const uint8_t* in_codes;
+    const uint8_t* in_scales;
+    uint8_t* out_codes;
+    uint8_t* out_scales;
+    int64_t rows, cols;
+    size_t scales_bytes;
+    bool scales_pad;
+    int num_sms;
+};
+cudaError_t run_repack(const RepackArgs& a, cudaStream_t st);
+
+struct DequantArgs {
+    int fmt;
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const float* ts;
+    int64_t rows, cols;
+    void* dst;
+    int out_bf16;
+    int num_sms;
+};
+cudaError_t run_dequant(const DequantArgs& a, cudaStream_t st);
+
+constexpr int kMaxGroups = 256;
+
+struct GemmArgs {
+    int fmt_a, fmt_b;              // bsq_format of A and B
+    const uint8_t* a_codes;
+    const uint8_t* a_scales;
+    const uint8_t* b_codes;        // grouped: group 0, groups consecutive
+    const uint8_t* b_scales;       // dense only
+    const float* ts_a;             // NVFP4 tensor scales
+    const float* ts_b;
+    int64_t M, N, K;               // grouped: M = total rows, N = per-group rows of B
+    void* C;
+    int out_bf16;
+    // grouped
+    int num_groups;                // 0 = dense
+    const int64_t* offsets;        // device
+    const uint8_t* const* b_group_scales;   // host array [num_groups]
+    int num_sms;
+    unsigned* status;
+    uint64_t timeout_ns;
+};
+cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st);
+
+cudaError_t run_timeout_probe(unsigned* status, uint64_t limit_ns, cudaStream_t st);
+
+}  // namespace bsq

@@ -1,0 +1,433 @@
+// Quantize kernels: BF16 -> MXFP8 (E4M3 / E5M2), MXFP4, NVFP4.
+//
+// Row-wise MX ("FP8 Training Infrastructure", section "Estrategias de
+// escalonamento": per-block scale factors; "Practical FP4 Training for
+// Large-Scale MoE Models on Hopper GPUs", section 2, kernel BF16ToFP4Row:
+// quantize and pack).  The row kernel streams the input once with 16-byte
+// loads; four lanes own one 32-element block and find its amax with two
+// shuffles.
+//
+// Column-wise / both (MoE FP4 page, section 2: the transposed operand of
+// FP4RowToFP8Col; the backward needs column blocks of activations, weights
+// and gradients).  The tile kernel stages a 128 x 128 BF16 tile in shared
+// memory and emits the transposed column-wise tensor and, in BOTH mode, the
+// row-wise tensor from the same read.
+//
+// NVFP4 (FP8 page, section "MXFP8 e NVFP4 do Blackwell"): a tensor amax
+// pass, then per 16-block UE4M3 scales against the FP32 tensor scale
+// amax / (448 * 6), each step an IEEE FP32 operation.
+#include "common.cuh"
+#include "internal.h"
+
+namespace bsq {
+
+// ---------------------------------------------------------------------------
+// Block encoders working on registers.
+// ---------------------------------------------------------------------------
+
+// MX: encode n values (n multiple of 8) given the block's scale byte.
+// FP8 output: n bytes; FP4 output: n/2 bytes.  Writes to `out` words.
+template <int FMT, int N>
+__device__ __forceinline__ void mx_encode(const float* x, uint32_t sbyte, uint32_t* out) {
+    if (sbyte == 0xFF) {
+        // NaN/Inf in the block: NaN scale, NaN codes (E2M1 has no NaN: 0)
+#pragma unroll
+        for (int i = 0; i < (is_fp4(FMT) ? N / 8 : N / 4); i++) out[i] = is_fp4(FMT) ? 0u : 0x7F7F7F7Fu;
+        return;
+    }
+    const float inv = mx_inv_scale(sbyte);
+    float v[N];
+#pragma unroll
+    for (int i = 0; i < N; i++) v[i] = x[i] * inv;
+    if (is_fp4(FMT)) {
+#pragma unroll
+        for (int i = 0; i < N / 8; i++) out[i] = pack8_fp4(v + 8 * i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N / 8; i++) {
+            uint2 p = pack8_fp8<FMT>(v + 8 * i);
+            out[2 * i] = p.x;
+            out[2 * i + 1] = p.y;
+        }
+    }
+}
+
+// NVFP4 per-block scale byte from the block amax and the tensor scale.
+__device__ __forceinline__ uint32_t nv_scale_byte(uint32_t amax_bits, float s_t) {
+    if (amax_bits >= 0x7F80u) return 0x7Fu;      // NaN/Inf in the block
+    float amax_b = __uint_as_float(amax_bits << 16);
+    float q = __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_t);
+    return cvt_e4m3x2(q, 0.0f) & 0xFFu;
+}
+
+// NVFP4: encode n values (multiple of 8) of one block with scale byte sb.
+template <int N>
+__device__ __forceinline__ void nv_encode(const float* x, uint32_t sb, float s_t, uint32_t* out) {
+    if (sb == 0 || sb == 0x7F) {
+#pragma unroll
+        for (int i = 0; i < N / 8; i++) out[i] = 0u;
+        return;
+    }
+    const float d = __fmul_rn(e4m3_to_float(sb), s_t);
+    float v[N];
+#pragma unroll
+    for (int i = 0; i < N; i++) v[i] = __fdiv_rn(x[i], d);
+#pragma unroll
+    for (int i = 0; i < N / 8; i++) out[i] = pack8_fp4(v + 8 * i);
+}
+
+__device__ __forceinline__ float nv_tensor_scale(const unsigned* amax_bits) {
+    float amax = __uint_as_float(*amax_bits);
+    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& w, float* f) {
+    f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+    f[4] = bf16lo(w.z); f[5] = bf16hi(w.z); f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+}
+
+__device__ __forceinline__ uint32_t absmax8(const uint4& w) {
+    return absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, w.x), w.y), w.z), w.w);
+}
+
+// ---------------------------------------------------------------------------
+// Row-wise kernel: one thread = 8 elements; BLK/8 lanes = one block.
+// ---------------------------------------------------------------------------
+constexpr int kRowThreads = 256;
+constexpr int kRowUnroll = 4;
+
+template <int FMT>
+__global__ void __launch_bounds__(kRowThreads)
+quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t blocks_per_row,
+                     int64_t s_tiles, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                     const unsigned* __restrict__ nv_amax) {
+    constexpr int BLK = block_of(FMT);
+    constexpr int LPB = BLK / 8;            // lanes per block: 4 (MX) or 2 (NV)
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
+    const bool vec_sf = (blocks_per_row & 3u) == 0;
+    float s_t = 1.0f;
+    if (FMT == kNVFP4) s_t = nv_tensor_scale(nv_amax);
+
+    for (int64_t base = warp * 32 * kRowUnroll; base < nchunks; base += nwarps * 32 * kRowUnroll) {
+        uint4 w[kRowUnroll];
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; u++) {
+            int64_t c = base + u * 32 + lane;
+            w[u] = c < nchunks ? ld_stream(src + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; u++) {
+            const int64_t c = base + u * 32 + lane;
+            uint32_t am = absmax8(w[u]);
+            am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+            if (LPB == 4) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t) : mx_scale_byte<FMT>(am);
+            float f[8];
+            unpack8(w[u], f);
+            uint32_t out[2];
+            if (FMT == kNVFP4) nv_encode<8>(f, sb, s_t, out);
+            else mx_encode<FMT, 8>(f, sb, out);
+            if (c < nchunks) {
+                if (is_fp4(FMT)) reinterpret_cast<uint32_t*>(codes)[c] = out[0];
+                else reinterpret_cast<uint2*>(codes)[c] = make_uint2(out[0], out[1]);
+            }
+            // scale bytes: gather 4 consecutive blocks into one 32-bit store
+            // when a row holds a multiple of 4 blocks, else one byte each.
+            const uint32_t blk = (uint32_t)(c / LPB);
+            if (vec_sf) {
+                uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, LPB);
+                uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2 * LPB);
+                uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3 * LPB);
+                if ((lane % (4 * LPB)) == 0 && c < nchunks) {
+                    uint32_t r = blk / blocks_per_row, j = blk - r * blocks_per_row;
+                    *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) =
+                        sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+                }
+            } else if ((lane % LPB) == 0 && c < nchunks) {
+                uint32_t r = blk / blocks_per_row, j = blk - r * blocks_per_row;
+                scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Tile kernel for column-wise and both: 128 x 128 BF16 tile in smem.
+// ---------------------------------------------------------------------------
+constexpr int kTile = 128;
+constexpr int kTileThreads = 256;
+constexpr int kPitchW = kTile / 2 + 4;      // row pitch in 32-bit words (272 B)
+
+template <int FMT, bool ROW, bool COL>
+__global__ void __launch_bounds__(kTileThreads)
+quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
+                     uint8_t* __restrict__ codes_r, uint8_t* __restrict__ scales_r, int64_t s_tiles_r,
+                     uint8_t* __restrict__ codes_c, uint8_t* __restrict__ scales_c, int64_t s_tiles_c,
+                     const unsigned* __restrict__ nv_amax) {
+    constexpr int BLK = block_of(FMT);
+    constexpr int NB = kTile / BLK;                 // blocks per tile edge: 4 or 8
+    __shared__ __align__(16) uint32_t tile[kTile * kPitchW];
+    __shared__ __align__(16) uint8_t sf_col[kTile * NB];   // [column][row-block]
+    __shared__ __align__(16) uint8_t sf_row[kTile * NB];   // [row][col-block]
+
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.y * kTile;
+    const int64_t c0 = (int64_t)blockIdx.x * kTile;
+    float s_t = 1.0f;
+    if (FMT == kNVFP4) s_t = nv_tensor_scale(nv_amax);
+
+    // load: 128 rows x 16 chunks of 8 bf16
+#pragma unroll
+    for (int i = 0; i < (kTile * 16) / kTileThreads; i++) {
+        int idx = tid + i * kTileThreads;
+        int rr = idx >> 4, ch = idx & 15;
+        int64_t gr = r0 + rr, gc = c0 + ch * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (gr < R && gc < C) v = ld_stream(reinterpret_cast<const uint4*>(src + gr * C + gc));
+        *reinterpret_cast<uint4*>(&tile[rr * kPitchW + ch * 4]) = v;
+    }
+    __syncthreads();
+
+    if (COL) {
+        // task = (row-block rb, column pair cp): two columns x BLK rows
+        constexpr int TASKS = NB * (kTile / 2);
+#pragma unroll 1
+        for (int id = tid; id < TASKS; id += kTileThreads) {
+            const int cp = id % (kTile / 2), rb = id / (kTile / 2);
+            uint32_t w[BLK];
+            uint32_t am_lo = 0, am_hi = 0;
+#pragma unroll
+            for (int r = 0; r < BLK; r++) {
+                w[r] = tile[(rb * BLK + r) * kPitchW + cp];
+                am_lo = max(am_lo, w[r] & 0x7FFFu);
+                am_hi = max(am_hi, (w[r] >> 16) & 0x7FFFu);
+            }
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                const uint32_t am = half ? am_hi : am_lo;
+                float f[BLK];
+#pragma unroll
+                for (int r = 0; r < BLK; r++) f[r] = half ? bf16hi(w[r]) : bf16lo(w[r]);
+                uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t) : mx_scale_byte<FMT>(am);
+                uint32_t out[BLK / 4];
+                if (FMT == kNVFP4) nv_encode<BLK>(f, sb, s_t, out);
+                else mx_encode<FMT, BLK>(f, sb, out);
+                const int cl = 2 * cp + half;
+                sf_col[cl * NB + rb] = (uint8_t)sb;
+                const int64_t gc = c0 + cl, gr = r0 + rb * BLK;
+                if (gc < C && gr < R) {
+                    if (is_fp4(FMT)) {
+                        uint8_t* dst = codes_c + gc * (R / 2) + gr / 2;
+                        if (BLK == 32) *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+                        else *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
+                    } else {
+                        uint8_t* dst = codes_c + gc * R + gr;
+                        *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+                        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(out[4], out[5], out[6], out[7]);
+                    }
+                }
+            }
+        }
+    }
+    if (ROW) {
+        // task = (row rr, column block cb): BLK contiguous elements
+        constexpr int TASKS = kTile * NB;
+#pragma unroll 1
+        for (int id = tid; id < TASKS; id += kTileThreads) {
+            const int rr = id % kTile, cb = id / kTile;
+            float f[BLK];
+            uint32_t am = 0;
+#pragma unroll
+            for (int q = 0; q < BLK / 8; q++) {
+                uint4 v = *reinterpret_cast<const uint4*>(&tile[rr * kPitchW + cb * (BLK / 2) + q * 4]);
+                am = max(am, absmax8(v));
+                unpack8(v, f + 8 * q);
+            }
+            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t) : mx_scale_byte<FMT>(am);
+            uint32_t out[BLK / 4];
+            if (FMT == kNVFP4) nv_encode<BLK>(f, sb, s_t, out);
+            else mx_encode<FMT, BLK>(f, sb, out);
+            sf_row[rr * NB + cb] = (uint8_t)sb;
+            const int64_t gr = r0 + rr, gc = c0 + cb * BLK;
+            if (gr < R && gc < C) {
+                if (is_fp4(FMT)) {
+                    uint8_t* dst = codes_r + gr * (C / 2) + gc / 2;
+                    if (BLK == 32) *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+                    else *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
+                } else {
+                    uint8_t* dst = codes_r + gr * C + gc;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+                    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(out[4], out[5], out[6], out[7]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    // scale stores: groups of 4 consecutive blocks -> one 32-bit word
+    constexpr int G = NB / 4;
+    if (COL) {
+        const int64_t S = R / BLK;                       // scale columns of the [C, R] output
+        for (int id = tid; id < kTile * G; id += kTileThreads) {
+            const int cl = id / G, g = id % G;
+            const int64_t gc = c0 + cl, sc = r0 / BLK + 4 * g;
+            if (gc < C && sc < S)
+                *reinterpret_cast<uint32_t*>(scales_c + sf_offset(gc, sc, s_tiles_c)) =
+                    *reinterpret_cast<const uint32_t*>(&sf_col[cl * NB + 4 * g]);
+        }
+    }
+    if (ROW) {
+        const int64_t S = C / BLK;
+        for (int id = tid; id < kTile * G; id += kTileThreads) {
+            const int rr = id / G, g = id % G;
+            const int64_t gr = r0 + rr, sc = c0 / BLK + 4 * g;
+            if (gr < R && sc < S)
+                *reinterpret_cast<uint32_t*>(scales_r + sf_offset(gr, sc, s_tiles_r)) =
+                    *reinterpret_cast<const uint32_t*>(&sf_row[rr * NB + 4 * g]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 tensor amax: max over finite |x| as FP32 bits (atomicMax on the
+// non-negative float bit pattern equals the float max).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+amax_kernel(const uint4* __restrict__ src, int64_t nchunks, unsigned* __restrict__ amax_bits) {
+    uint32_t am = 0;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < nchunks; i += 4 * stride) {
+        uint4 a = ld_stream(src + i), b = ld_stream(src + i + stride);
+        uint4 c = ld_stream(src + i + 2 * stride), d = ld_stream(src + i + 3 * stride);
+        uint32_t m[4] = {absmax8(a), absmax8(b), absmax8(c), absmax8(d)};
+#pragma unroll
+        for (int k = 0; k < 4; k++) if (m[k] < 0x7F80u) am = max(am, m[k]);
+        // a chunk holding a non-finite value can still hold finite ones
+#pragma unroll
+        for (int k = 0; k < 4; k++) if (m[k] >= 0x7F80u) {
+            const uint4 v = k == 0 ? a : (k == 1 ? b : (k == 2 ? c : d));
+            const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                uint32_t lo = ws[q] & 0x7FFFu, hi = (ws[q] >> 16) & 0x7FFFu;
+                if (lo < 0x7F80u) am = max(am, lo);
+                if (hi < 0x7F80u) am = max(am, hi);
+            }
+        }
+    }
+    for (; i < nchunks; i += stride) {
+        uint4 v = ld_stream(src + i);
+        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint32_t lo = ws[q] & 0x7FFFu, hi = (ws[q] >> 16) & 0x7FFFu;
+            if (lo < 0x7F80u) am = max(am, lo);
+            if (hi < 0x7F80u) am = max(am, hi);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
+    __shared__ uint32_t red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = am;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t m = 0;
+        for (int k = 0; k < (int)(blockDim.x >> 5); k++) m = max(m, red[k]);
+        if (m) atomicMax(amax_bits, m << 16);
+    }
+}
+
+// amax bits -> tensor scale s_t, written to one or two outputs.
+__global__ void nv_finalize_kernel(float* ts0, float* ts1) {
+    float s = nv_tensor_scale(reinterpret_cast<const unsigned*>(ts0));
+    *ts0 = s;
+    if (ts1) *ts1 = s;
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+template <int FMT>
+static cudaError_t launch_rows(const void* src, int64_t R, int64_t C, uint8_t* codes, uint8_t* scales,
+                               const unsigned* nv_amax, cudaStream_t st, int num_sms) {
+    const int64_t nchunks = R * C / 8;
+    const int64_t per_cta = (int64_t)kRowThreads * kRowUnroll;
+    int64_t grid = (nchunks + per_cta - 1) / per_cta;
+    grid = grid < (int64_t)num_sms * 8 ? grid : (int64_t)num_sms * 8;
+    if (grid < 1) grid = 1;
+    const int64_t S = C / block_of(FMT);
+    quantize_rows_kernel<FMT><<<(unsigned)grid, kRowThreads, 0, st>>>(
+        reinterpret_cast<const uint4*>(src), nchunks, (uint32_t)S, (S + 3) / 4, codes, scales, nv_amax);
+    return cudaGetLastError();
+}
+
+template <int FMT>
+static cudaError_t launch_tile(const void* src, int64_t R, int64_t C, int axis,
+                               uint8_t* cr, uint8_t* sr, uint8_t* cc, uint8_t* sc,
+                               const unsigned* nv_amax, cudaStream_t st) {
+    dim3 grid((unsigned)((C + kTile - 1) / kTile), (unsigned)((R + kTile - 1) / kTile));
+    const int BLK = block_of(FMT);
+    const int64_t str = (C / BLK + 3) / 4, stc = (R / BLK + 3) / 4;
+    const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
+    if (axis == 3)
+        quantize_tile_kernel<FMT, true, true><<<grid, kTileThreads, 0, st>>>(s, R, C, cr, sr, str, cc, sc, stc, nv_amax);
+    else
+        quantize_tile_kernel<FMT, false, true><<<grid, kTileThreads, 0, st>>>(s, R, C, cr, sr, str, cc, sc, stc, nv_amax);
+    return cudaGetLastError();
+}
+
+cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
+    cudaError_t e;
+    const int64_t R = a.rows, C = a.cols;
+    // zero the padding of the tiled scale buffers when there is any
+    if (a.row_scales && a.row_scales_pad) {
+        if ((e = cudaMemsetAsync(a.row_scales, 0, a.row_scales_bytes, st)) != cudaSuccess) return e;
+    }
+    if (a.col_scales && a.col_scales_pad) {
+        if ((e = cudaMemsetAsync(a.col_scales, 0, a.col_scales_bytes, st)) != cudaSuccess) return e;
+    }
+    unsigned* amax = nullptr;
+    if (a.fmt == kNVFP4) {
+        amax = reinterpret_cast<unsigned*>(a.axis & 1 ? a.row_ts : a.col_ts);
+        if ((e = cudaMemsetAsync(amax, 0, sizeof(float), st)) != cudaSuccess) return e;
+        int64_t nchunks = R * C / 8;
+        int64_t grid = (nchunks + 256 * 4 - 1) / (256 * 4);
+        if (grid > (int64_t)a.num_sms * 8) grid = (int64_t)a.num_sms * 8;
+        if (grid < 1) grid = 1;
+        amax_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(a.src), nchunks, amax);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (a.axis == 1) {
+        switch (a.fmt) {
+        case kE4M3: e = launch_rows<kE4M3>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
+        case kE5M2: e = launch_rows<kE5M2>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
+        case kMXFP4: e = launch_rows<kMXFP4>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
+        default: e = launch_rows<kNVFP4>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
+        }
+    } else {
+        switch (a.fmt) {
+        case kE4M3: e = launch_tile<kE4M3>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, amax, st); break;
+        case kE5M2: e = launch_tile<kE5M2>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, amax, st); break;
+        case kMXFP4: e = launch_tile<kMXFP4>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, amax, st); break;
+        default: e = launch_tile<kNVFP4>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, amax, st); break;
+        }
+    }
+    if (e != cudaSuccess) return e;
+    if (a.fmt == kNVFP4) {
+        float* other = (a.axis == 3) ? a.col_ts : nullptr;
+        nv_finalize_kernel<<<1, 1, 0, st>>>(reinterpret_cast<float*>(amax), other);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace bsq

@@ -1,0 +1,182 @@
+/*
+ * bsq.h -- C ABI of libbsq.so: block-scaled low-precision linear layer on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (the pages give the method in prose only):
+ *  - Quantize BF16 tensors to MXFP8 (E4M3 for forward activations and
+ *    weights, E5M2 for gradients), to MXFP4 and to NVFP4, row-wise and
+ *    column-wise ("FP8 Training Infrastructure", sections "O panorama da
+ *    precisao numerica" and "Estrategias de escalonamento"; "Practical FP4
+ *    Training for Large-Scale MoE Models on Hopper GPUs", section 2,
+ *    kernel BF16ToFP4Row and the transposed FP4RowToFP8Col layout).
+ *  - A block-scaled GEMM with FP32 accumulation that consumes codes and
+ *    scales directly on the tensor cores (MoE FP4 page, section 2, heavy
+ *    GEMMs stay on native FP8 tensor cores), dense and grouped over ragged
+ *    expert batches (same section, "tensores ragged").
+ *  - The direct integer-domain MXFP4 -> MXFP8 re-encode (same section,
+ *    "Algoritmo de Conversao Direta"; kernel FP4RowToFP8Row).
+ *
+ * Conventions shared by every entry point
+ *  - Matrices are row-major.  A GEMM computes C[M,N] = A[M,K] * B[N,K]^T:
+ *    both operands are stored K-major (K is the contiguous last axis).
+ *  - "Row-wise" quantization puts blocks along the last (contiguous) axis.
+ *    "Column-wise" puts blocks along axis 0 and stores the TRANSPOSE: the
+ *    column-wise output of a [R, C] input is a [C, R] tensor whose blocks
+ *    run along its last axis, so every GEMM operand is K-major.
+ *  - Codes: FP8 formats one byte per element; FP4 formats two elements per
+ *    byte, the even-index element in the low nibble.
+ *  - Scales: one byte per block (E8M0 for the MX formats, UE4M3 for NVFP4),
+ *    stored in 512-byte tiles of 128 rows x 4 scale columns: the byte of
+ *    scale (r, c) of a [rows, S] scale matrix is at
+ *        ((r/128) * ceil(S/4) + c/4) * 512 + (r%32)*16 + ((r/32)%4)*4 + c%4.
+ *    Rows are padded to a multiple of 128, scale columns to a multiple of
+ *    4, and padding bytes are zero.  This is the scale-operand layout the
+ *    tcgen05 block-scaled MMA reads.
+ *  - MX block scale: e = floor(log2(block amax)) - emax, emax = 8 (E4M3),
+ *    15 (E5M2), 2 (E2M1), clamped to [-127, 127]; an all-zero block gets
+ *    e = -127; a block holding NaN/Inf gets scale 0xFF and NaN codes
+ *    (E2M1: zero codes).  Codes are round-to-nearest-even of x * 2^-e with
+ *    saturation to +-448 / +-57344 / +-6; the sign of zero is kept.
+ *  - NVFP4: s_t = amax(finite |x|) / 2688 in FP32 (1 when the amax is 0);
+ *    per 16-block s_b = UE4M3(RNE((amax_b / 6) / s_t)); codes are
+ *    E2M1(RNE(x / (s_b * s_t))) with each step an IEEE FP32 operation; a
+ *    zero s_b gives zero codes; a block holding NaN/Inf gets s_b = 0x7F and
+ *    zero codes.
+ *
+ * Ownership: the caller allocates and frees every buffer (sizes from
+ * bsq_codes_bytes / bsq_scales_bytes).  Pointers passed to the compute
+ * calls are DEVICE pointers.  The library keeps no allocation between calls;
+ * its only state is a device status word in static device memory.
+ *
+ * Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  All
+ * compute calls are asynchronous on that stream.
+ *
+ * Errors: arguments are checked on the host before any launch; on failure
+ * the call returns a status, launches nothing and writes nothing.  No C++
+ * exception crosses this boundary.  Faults detected on the device (a wait
+ * that exceeded its limit) set the device status word, which
+ * bsq_sync_status() returns and clears.
+ */
+#ifndef BSQ_H
+#define BSQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BSQ_OK = 0,
+    BSQ_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, shape mismatch        */
+    BSQ_ERR_UNSUPPORTED = 2,   /* valid request this library does not handle    */
+    BSQ_ERR_ALIGNMENT = 3,     /* a pointer or a row pitch is not 16-byte aligned */
+    BSQ_ERR_CUDA = 4,          /* a CUDA runtime call failed                    */
+    BSQ_ERR_TIMEOUT = 5        /* a device-side wait ran past its limit         */
+} bsq_status;
+
+typedef enum {
+    BSQ_MXFP8_E4M3 = 0,        /* E4M3 codes, 32-element blocks, E8M0 scales    */
+    BSQ_MXFP8_E5M2 = 1,        /* E5M2 codes, 32-element blocks, E8M0 scales    */
+    BSQ_MXFP4_E2M1 = 2,        /* E2M1 codes, 32-element blocks, E8M0 scales    */
+    BSQ_NVFP4_E2M1 = 3         /* E2M1 codes, 16-element blocks, UE4M3 scales,
+                                  plus one FP32 tensor scale                    */
+} bsq_format;
+
+typedef enum { BSQ_ROWWISE = 1, BSQ_COLWISE = 2, BSQ_BOTH = 3 } bsq_axis;
+
+typedef enum { BSQ_OUT_F32 = 0, BSQ_OUT_BF16 = 1 } bsq_out;
+
+/* A quantized tensor as stored: `rows` x `cols` logical elements with blocks
+ * along `cols`.  codes / scales / tensor_scale are device pointers;
+ * tensor_scale (one float) is used by NVFP4 only and may be NULL otherwise. */
+typedef struct {
+    int32_t fmt;               /* bsq_format */
+    int32_t reserved;          /* must be 0  */
+    int64_t rows;
+    int64_t cols;
+    void* codes;
+    uint8_t* scales;
+    float* tensor_scale;
+} bsq_tensor;
+
+/* Bytes of the code buffer of a rows x cols tensor (0 on a bad format). */
+size_t bsq_codes_bytes(int32_t fmt, int64_t rows, int64_t cols);
+
+/* Bytes of the tiled scale buffer: ceil(rows/128)*128 * ceil(S/4)*4 with
+ * S = cols / block (0 on a bad format or when cols is not a block multiple). */
+size_t bsq_scales_bytes(int32_t fmt, int64_t rows, int64_t cols);
+
+/* Quantize a row-major BF16 matrix src[rows, cols] (device).
+ *   axis BSQ_ROWWISE: out_row gets a [rows, cols] tensor (cols % block == 0).
+ *   axis BSQ_COLWISE: out_col gets the transposed [cols, rows] tensor
+ *                     (rows % block == 0).
+ *   axis BSQ_BOTH:    both, from one read of src.
+ * The caller fills the out tensors' fmt / rows / cols / pointers; they must
+ * match the request.  For NVFP4 each written tensor's tensor_scale must be a
+ * device float; the call computes the tensor amax first (two passes).
+ * Citations: FP8 page "Estrategias de escalonamento" (block scaling); MoE
+ * FP4 page section 2, BF16ToFP4Row (row quantize and pack) and the
+ * transposed operand of FP4RowToFP8Col. */
+bsq_status bsq_quantize(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
+                        bsq_tensor* out_row, bsq_tensor* out_col, void* stream);
+
+/* Exact dequantization dst[rows, cols] = code * scale (* tensor scale),
+ * rounded once to FP32 or BF16 (nearest-even).  dst is device memory,
+ * 16-byte aligned.  Citation: MoE FP4 page section 2 (the dequantization
+ * step that FP4RowToFP8Row replaces). */
+bsq_status bsq_dequantize(const bsq_tensor* in, void* dst, int32_t dst_type, void* stream);
+
+/* C[M,N] = A[M,K] * B[N,K]^T with FP32 accumulation on tcgen05 block-scaled
+ * tensor-core MMAs; C row-major with leading dimension N, FP32 or BF16.
+ * Supported pairs: any of MXFP8 E4M3 / E5M2 with each other; NVFP4 with
+ * NVFP4 (the result is multiplied by both tensor scales).  K = A.cols =
+ * B.cols; K % 32 == 0.  M, N >= 1 of any size.  Citation: MoE FP4 page
+ * section 2 ("Calculo Intenso": GEMMs stay on native FP8 tensor cores);
+ * FP8 page "MXFP8 e NVFP4 do Blackwell" (hardware block scaling). */
+bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type, void* stream);
+
+/* Grouped GEMM over ragged expert batches: for g in [0, num_groups)
+ *   C[o_g:o_{g+1}, :] = A[o_g:o_{g+1}, :] * B_g^T
+ * where o = group_offsets_dev (DEVICE int64[num_groups+1], o_0 = 0,
+ * non-decreasing, o_G = A.rows).  B_groups is a HOST array of num_groups
+ * tensors of identical shape [N, K] and format; their code buffers must be
+ * consecutive slices of one allocation (B_g.codes = B_0.codes + g * codes
+ * bytes); scale buffers may be anywhere.  A's scales use the plain tiled
+ * layout of the whole [A.rows, K] matrix.  num_groups <= 256; MXFP8 only.
+ * Citation: MoE FP4 page section 2, ragged tensors whose per-expert token
+ * counts vary. */
+bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_dev, int32_t num_groups,
+                            const bsq_tensor* B_groups, void* C, int32_t out_type, void* stream);
+
+/* Direct MXFP4 -> MXFP8 (E4M3) re-encode in the integer domain, same shape
+ * and block grid.  Per 32-block with scale exponent e and largest code
+ * magnitude exponent e_c: new scale e + e_c - 8 (clamped at -127), every
+ * code moved to the E4M3 code of the same value.  The result equals the
+ * E4M3 MX quantization of the exactly dequantized MXFP4 block.  Citation:
+ * MoE FP4 page section 2, "Algoritmo de Conversao Direta" and kernel
+ * FP4RowToFP8Row. */
+bsq_status bsq_mxfp4_to_mxfp8(const bsq_tensor* in_mxfp4, bsq_tensor* out_e4m3, void* stream);
+
+/* Synchronize `stream`, read and clear the device status word, and return
+ * BSQ_ERR_TIMEOUT if any kernel recorded a timed-out wait since the last
+ * call, BSQ_ERR_CUDA if the stream reported an error, else BSQ_OK. */
+bsq_status bsq_sync_status(void* stream);
+
+/* Test hook for the failure path: launches one kernel that waits on a
+ * barrier nothing ever arrives on, gives up after `limit_ns` nanoseconds
+ * (capped at 1e9) and records BSQ_ERR_TIMEOUT in the status word.  It
+ * touches no memory besides the status word. */
+bsq_status bsq_debug_timeout_probe(uint64_t limit_ns, void* stream);
+
+/* Static description of a status code. */
+const char* bsq_status_string(int32_t status);
+
+/* Library version string. */
+const char* bsq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BSQ_H */

@@ -1,0 +1,80 @@
+"""Shared helpers for the parity tests: move seeded inputs to the device and
+build the oracle's expected bytes in the library's storage layout."""
+import numpy as np
+
+import oracle
+
+BLOCK = oracle.BLOCK
+
+
+def dev_bf16(bits: np.ndarray):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host_u8(t) -> np.ndarray:
+    return t.detach().cpu().numpy().astype(np.uint8)
+
+
+def dev_u8(a: np.ndarray):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
+
+
+def expected(x_bits: np.ndarray, fmt: str, axis: str):
+    """Oracle result in storage layout: {'row': (codes, scales, s_t), 'col': ...}."""
+    out = {}
+    if axis in ("row", "both"):
+        c, s, t = oracle.quantize_rows(x_bits, fmt)
+        out["row"] = (oracle.storage_codes(c, fmt), oracle.swizzle_scales(s), t, c, s)
+    if axis in ("col", "both"):
+        c, s, t = oracle.quantize_cols(x_bits, fmt)
+        out["col"] = (oracle.storage_codes(c, fmt), oracle.swizzle_scales(s), t, c, s)
+    return out
+
+
+def assert_qtensor_equal(q, exp, what=""):
+    codes, scales, s_t = exp[0], exp[1], exp[2]
+    got_c = host_u8(q.codes).reshape(codes.shape)
+    got_s = host_u8(q.scales)
+    if not np.array_equal(got_c, codes):
+        bad = np.argwhere(got_c != codes)
+        r, k = bad[0]
+        raise AssertionError(f"{what}: {len(bad)} code bytes differ; first at {tuple(bad[0])}: "
+                             f"got {got_c[r, k]:#04x} want {codes[r, k]:#04x}")
+    if not np.array_equal(got_s, scales):
+        bad = np.flatnonzero(got_s != scales)
+        raise AssertionError(f"{what}: {len(bad)} scale bytes differ; first at {bad[0]}: "
+                             f"got {got_s[bad[0]]:#04x} want {scales[bad[0]]:#04x}")
+    if s_t is not None:
+        got_t = float(q.tensor_scale.cpu().numpy()[0])
+        assert np.float32(got_t) == np.float32(s_t), (what, got_t, s_t)
+
+
+def upload_q(bsq, fmt: str, codes_unpacked: np.ndarray, scales_rowmajor: np.ndarray, s_t=None):
+    """Oracle-made quantized tensor -> device QTensor (storage layout)."""
+    import torch
+    R, C = codes_unpacked.shape
+    q = bsq.empty(fmt, R, C)
+    q.codes.copy_(dev_u8(oracle.storage_codes(codes_unpacked, fmt).ravel()))
+    q.scales.copy_(dev_u8(oracle.swizzle_scales(scales_rowmajor)))
+    if s_t is not None:
+        q.tensor_scale.copy_(torch.tensor([s_t], dtype=torch.float32))
+    return q
+
+
+def round_to_bf16(d: np.ndarray) -> np.ndarray:
+    """Exact doubles -> nearest-even BF16 bit patterns (normal range)."""
+    d = np.asarray(d, dtype=np.float64)
+    m, e = np.frexp(d)
+    r = np.ldexp(np.rint(m * 256.0), e - 8)
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def gemm_tol_ok(C: np.ndarray, ref: np.ndarray, mag: np.ndarray, bf16: bool):
+    """|C - ref| <= 1e-5 * sum|a*b| (+ BF16 output rounding, half an ulp)."""
+    tol = 1e-5 * mag
+    if bf16:
+        tol = tol * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(ref)
+    err = np.abs(C.astype(np.float64) - ref)
+    return err <= tol, err, tol

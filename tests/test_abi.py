@@ -1,0 +1,72 @@
+"""CPU-side checks of the C ABI: the library builds, loads without a GPU and
+exports every entry point declared in include/bsq.h; the size functions and
+host-side argument checks behave as documented (no device work)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_scaled_precision_03_gb300 import _build
+    import block_scaled_precision_03_gb300 as bsq
+    _build.build()
+    return bsq.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "bsq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_boundary():
+    names = declared_functions()
+    for need in ["bsq_quantize", "bsq_dequantize", "bsq_gemm", "bsq_grouped_gemm", "bsq_mxfp4_to_mxfp8",
+                 "bsq_codes_bytes", "bsq_scales_bytes", "bsq_sync_status", "bsq_status_string"]:
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_size_functions(lib):
+    import block_scaled_precision_03_gb300 as bsq
+    assert bsq.codes_bytes("mxfp8_e4m3", 8192, 4096) == 8192 * 4096
+    assert bsq.codes_bytes("nvfp4", 8192, 4096) == 8192 * 2048
+    assert bsq.scales_bytes("mxfp8_e4m3", 8192, 4096) == 8192 * 128
+    assert bsq.scales_bytes("nvfp4", 8192, 4096) == 8192 * 256
+    assert bsq.scales_bytes("mxfp4", 130, 96) == 256 * 4        # rows -> 256, 3 scales -> 4
+    assert bsq.scales_bytes("mxfp8_e4m3", 10, 48) == 0           # cols not a block multiple
+    assert bsq.codes_bytes(7, 1, 1) == 0
+
+
+def test_host_argument_checks_launch_nothing(lib):
+    import block_scaled_precision_03_gb300 as bsq
+    T = bsq.BsqTensorC
+    null = ctypes.c_void_p(None)
+    # null source, bad axis, bad format: rejected before any CUDA call
+    assert lib.bsq_quantize(None, 128, 128, 0, 1, None, None, null) == 1
+    assert lib.bsq_quantize(ctypes.c_void_p(256), 128, 128, 0, 9, None, None, null) == 1
+    assert lib.bsq_quantize(ctypes.c_void_p(256), 128, 128, 9, 1, None, None, null) == 1
+    # misaligned source pointer
+    t = T(0, 0, 128, 128, 256, 256, None)
+    assert lib.bsq_quantize(ctypes.c_void_p(258), 128, 128, 0, 1, ctypes.byref(t), None, null) == 3
+    # shape mismatch between request and output descriptor
+    t2 = T(0, 0, 64, 128, 256, 256, None)
+    assert lib.bsq_quantize(ctypes.c_void_p(256), 128, 128, 0, 1, ctypes.byref(t2), None, null) == 1
+    # unsupported GEMM pairs
+    a = T(0, 0, 128, 256, 256, 256, None)
+    b = T(3, 0, 128, 256, 256, 256, 256)
+    assert lib.bsq_gemm(ctypes.byref(a), ctypes.byref(b), ctypes.c_void_p(256), 0, null) == 2
+    b2 = T(0, 0, 128, 512, 256, 256, None)
+    assert lib.bsq_gemm(ctypes.byref(a), ctypes.byref(b2), ctypes.c_void_p(256), 0, null) == 1
+    # repack needs MXFP4 in, E4M3 out
+    assert lib.bsq_mxfp4_to_mxfp8(ctypes.byref(a), ctypes.byref(a), null) == 2
+    assert lib.bsq_status_string(5) == b"device wait timed out"

@@ -1,0 +1,297 @@
+"""GPU-vs-oracle parity on small and ragged shapes, through the C ABI.
+
+Codes, scales and repacked bytes must match the oracle bit for bit; GEMM
+outputs must satisfy |C - ref| <= 1e-5 * sum_k |a_k b_k| against the
+oracle's FP64 sum of exactly dequantized products (plus half a BF16 ulp for
+BF16 output)."""
+import numpy as np
+import pytest
+
+import oracle
+from block_scaled_precision_03_gb300 import inputs
+from _util import (expected, assert_qtensor_equal, dev_bf16, host_u8, dev_u8, upload_q, round_to_bf16,
+                   gemm_tol_ok)
+
+pytestmark = pytest.mark.gpu
+
+FMTS = ["mxfp8_e4m3", "mxfp8_e5m2", "mxfp4", "nvfp4"]
+
+
+@pytest.fixture(scope="module")
+def bsq():
+    import block_scaled_precision_03_gb300 as b
+    b.lib()
+    return b
+
+
+def _gen(shape, seed, kind):
+    if kind == "outlier":
+        return inputs.outlier_activations_bf16(shape, seed)
+    if kind == "grad":
+        return inputs.loguniform_grad_bf16(shape, seed)
+    return inputs.normal_bf16(shape, seed, std=0.02 if kind == "weight" else 1.0)
+
+
+# ------------------------------------------------------------------ quantize
+ROW_SHAPES = [(256, 256), (130, 96), (7, 32), (1, 4096), (384, 1056), (129, 160)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", ROW_SHAPES)
+@pytest.mark.parametrize("kind", ["outlier", "grad", "weight"])
+def test_quantize_rows(bsq, fmt, shape, kind):
+    x = _gen(shape, 11, kind)
+    row, _ = bsq.quantize(dev_bf16(x), fmt, "row")
+    assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} row {shape}")
+
+
+COL_SHAPES = [(256, 256), (96, 130), (32, 8), (4096, 16), (1056, 384), (160, 136)]
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", COL_SHAPES)
+@pytest.mark.parametrize("axis", ["col", "both"])
+def test_quantize_cols_and_both(bsq, fmt, shape, axis):
+    R, C = shape
+    if axis == "both" and C % oracle.BLOCK[fmt]:
+        pytest.skip("row-wise blocks need cols % block == 0")
+    x = _gen(shape, 5, "grad" if fmt == "mxfp8_e5m2" else "outlier")
+    row, col = bsq.quantize(dev_bf16(x), fmt, axis)
+    exp = expected(x, fmt, axis)
+    assert_qtensor_equal(col, exp["col"], f"{fmt} col {shape}")
+    if axis == "both":
+        assert_qtensor_equal(row, exp["row"], f"{fmt} both/row {shape}")
+
+
+def _all_bf16_patterns(order_seed=None):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    if order_seed is not None:
+        bits = np.random.default_rng(order_seed).permutation(bits)
+    return bits.reshape(2048, 32)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("order", [None, 1, 2])
+def test_quantize_every_bf16_pattern(bsq, fmt, order):
+    """All 65536 BF16 bit patterns (NaN, Inf, subnormals, zeros included) in
+    natural and shuffled block groupings."""
+    x = _all_bf16_patterns(order)
+    if fmt == "nvfp4":
+        # the tensor amax ignores non-finite values; keep them in blocks
+        pass
+    row, _ = bsq.quantize(dev_bf16(x), fmt, "row")
+    assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} all-bf16 order={order}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_quantize_every_bf16_pattern_scaled_blocks(bsq, fmt):
+    """Each block = 31 patterns + an anchor 2^k above them: every finite BF16
+    value is encoded at many block scales."""
+    rng = np.random.default_rng(3)
+    fin = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    fin = fin[(fin & 0x7F80) != 0x7F80]
+    blocks = []
+    for shift in (0, 1, 3, 7):
+        v = rng.permutation(fin)
+        n = len(v) // 31 * 31
+        body = v[:n].reshape(-1, 31)
+        mags = (body & 0x7FFF).max(axis=1)
+        anchor = np.minimum(mags.astype(np.int64) + (shift << 7), 0x7F7F).astype(np.uint16)
+        blocks.append(np.concatenate([body, anchor[:, None]], axis=1))
+    x = np.ascontiguousarray(np.concatenate(blocks)[:, :32])
+    if fmt == "nvfp4":
+        x = np.ascontiguousarray(x.reshape(-1, 16))
+    row, _ = bsq.quantize(dev_bf16(x), fmt, "row")
+    assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} anchored")
+
+
+def test_quantize_zero_and_nonfinite_blocks(bsq):
+    x = np.zeros((4, 64), dtype=np.uint16)
+    x[1, 3] = 0x7FC0          # NaN
+    x[2, 40] = 0xFF80         # -Inf
+    x[3, :] = 0x8000          # -0
+    x[3, 33] = 0x3F80
+    for fmt in FMTS:
+        row, col = bsq.quantize(dev_bf16(x), fmt, "row")
+        assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} special")
+
+
+def test_nvfp4_tensor_scale_shared(bsq):
+    x = inputs.outlier_activations_bf16((128, 256), 9)
+    row, col = bsq.quantize(dev_bf16(x), "nvfp4", "both")
+    st = oracle.nvfp4_tensor_scale(x)
+    assert float(row.tensor_scale.cpu()[0]) == st == float(col.tensor_scale.cpu()[0])
+
+
+# -------------------------------------------------------------------- repack
+def _random_mxfp4(R, C, seed, scale_lo=0, scale_hi=256):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, (R, C)).astype(np.uint8)
+    # some all-zero and single-magnitude blocks
+    codes[0, :32] = 0
+    if R > 1:
+        codes[1, :32] = rng.choice([0, 8, 1, 9], 32)
+    scales = rng.integers(scale_lo, scale_hi, (R, C // 32)).astype(np.uint8)
+    return codes, scales
+
+
+@pytest.mark.parametrize("shape", [(64, 256), (130, 96), (1, 32), (300, 7168)])
+def test_repack_bitexact(bsq, shape):
+    R, C = shape
+    codes, scales = _random_mxfp4(R, C, R + C)
+    scales.ravel()[:12] = [0, 1, 2, 5, 6, 7, 8, 9, 250, 253, 254, 255][:scales.size]
+    q = upload_q(bsq, "mxfp4", codes, scales)
+    out = bsq.mxfp4_to_mxfp8(q)
+    c8, s8 = oracle.mxfp4_to_mxfp8_rows(codes, scales)
+    assert_qtensor_equal(out, (c8, oracle.swizzle_scales(s8), None), f"repack {shape}")
+
+
+def test_repack_every_nibble_pair_every_scale(bsq):
+    rows = []
+    for a in range(16):
+        for b in range(16):
+            blk = np.zeros(32, dtype=np.uint8)
+            blk[0], blk[1] = a, b
+            blk[2:] = (np.arange(30) * 5 + b) % 16
+            rows.append(blk)
+    base = np.array(rows, dtype=np.uint8)
+    codes = np.tile(base, (1, 8))                         # 256 rows x 256
+    scales = np.arange(256 * 8, dtype=np.uint32).reshape(256, 8).astype(np.uint8)
+    q = upload_q(bsq, "mxfp4", codes, scales)
+    out = bsq.mxfp4_to_mxfp8(q)
+    c8, s8 = oracle.mxfp4_to_mxfp8_rows(codes, scales)
+    assert_qtensor_equal(out, (c8, oracle.swizzle_scales(s8), None), "repack exhaustive")
+
+
+# ------------------------------------------------------------------- dequant
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_dequantize_exact(bsq, fmt, out):
+    import torch
+    x = inputs.outlier_activations_bf16((130, 256), 21)
+    c, s, t = oracle.quantize_rows(x, fmt)
+    q = upload_q(bsq, fmt, c, s, t)
+    ref = oracle.dequant_rows(c, s, fmt, t)
+    got = bsq.dequantize(q, torch.float32 if out == "f32" else torch.bfloat16)
+    if out == "f32":
+        np.testing.assert_array_equal(got.cpu().numpy(), ref.astype(np.float32))
+    else:
+        g = got.view(torch.int16).cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(g, round_to_bf16(ref))
+
+
+# ---------------------------------------------------------------------- GEMM
+def _q_oracle(x, fmt):
+    c, s, t = oracle.quantize_rows(x, fmt)
+    return c, s, t
+
+
+def _check_gemm(bsq, xa, fa, xb, fb, dtype_name, full=True):
+    import torch
+    ca, sa, ta = _q_oracle(xa, fa)
+    cb, sb, tb = _q_oracle(xb, fb)
+    A = upload_q(bsq, fa, ca, sa, ta)
+    B = upload_q(bsq, fb, cb, sb, tb)
+    dt = torch.float32 if dtype_name == "f32" else torch.bfloat16
+    C = bsq.gemm(A, B, dt).float().cpu().numpy()
+    Ad = oracle.dequant_rows(ca, sa, fa, ta)
+    Bd = oracle.dequant_rows(cb, sb, fb, tb)
+    ref, mag = oracle.gemm_full(Ad, Bd)
+    ok, err, tol = gemm_tol_ok(C, ref, mag, dtype_name == "bf16")
+    if not ok.all():
+        i = np.unravel_index(np.argmax(err - tol), err.shape)
+        raise AssertionError(f"{(~ok).sum()} of {ok.size} outside bound; worst {i}: got {C[i]} ref {ref[i]} "
+                             f"mag {mag[i]} err {err[i]} tol {tol[i]}")
+    return C, ref
+
+
+def test_gemm_tiny_mxfp8_linear(bsq):
+    """A 256x256 @ B 256x256^T, E4M3, FP32 out: every element."""
+    d = inputs.tiny_linear()
+    _check_gemm(bsq, d["A"], "mxfp8_e4m3", d["B"], "mxfp8_e4m3", "f32")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (1, 1, 32), (200, 300, 96), (257, 513, 4160), (64, 640, 1024)])
+@pytest.mark.parametrize("fa,fb", [("mxfp8_e4m3", "mxfp8_e4m3"), ("mxfp8_e5m2", "mxfp8_e4m3"),
+                                   ("mxfp8_e4m3", "mxfp8_e5m2")])
+def test_gemm_mxfp8_shapes(bsq, M, N, K, fa, fb):
+    xa = inputs.loguniform_grad_bf16((M, K), 1) if fa == "mxfp8_e5m2" else inputs.outlier_activations_bf16((M, K), 1)
+    xb = inputs.normal_bf16((N, K), 2, std=0.02)
+    _check_gemm(bsq, xa, fa, xb, fb, "f32")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (200, 300, 96), (130, 260, 4128), (33, 512, 640)])
+def test_gemm_nvfp4_shapes(bsq, M, N, K):
+    xa = inputs.normal_bf16((M, K), 3)
+    xb = inputs.normal_bf16((N, K), 4, std=0.02)
+    _check_gemm(bsq, xa, "nvfp4", xb, "nvfp4", "f32")
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8_e4m3", "nvfp4"])
+def test_gemm_bf16_output(bsq, fmt):
+    xa = inputs.outlier_activations_bf16((300, 512), 5)
+    xb = inputs.normal_bf16((520, 512), 6, std=0.02)
+    _check_gemm(bsq, xa, fmt, xb, fmt, "bf16")
+
+
+def test_gemm_single_scale_probe(bsq):
+    """One non-unit scale per 128x4 tile position: checks that every scale
+    byte reaches the MMA for the row / block it belongs to."""
+    import torch
+    M, N, K = 128, 256, 256
+    ca = np.full((M, K), oracle.encode(oracle.E4M3, 1.0), np.uint8)
+    cb = np.full((N, K), oracle.encode(oracle.E4M3, 1.0), np.uint8)
+    rng = np.random.default_rng(0)
+    sa = (127 + rng.integers(-3, 4, (M, K // 32))).astype(np.uint8)
+    sb = (127 + rng.integers(-3, 4, (N, K // 32))).astype(np.uint8)
+    A = upload_q(bsq, "mxfp8_e4m3", ca, sa)
+    B = upload_q(bsq, "mxfp8_e4m3", cb, sb)
+    C = bsq.gemm(A, B, torch.float32).cpu().numpy()
+    ref = 32.0 * (np.exp2(sa.astype(np.float64) - 127) @ np.exp2(sb.astype(np.float64) - 127).T)
+    np.testing.assert_array_equal(C, ref.astype(np.float32))
+
+
+def test_grouped_gemm_small(bsq):
+    import torch
+    counts = np.array([100, 0, 300, 1, 129, 70], dtype=np.int64)
+    G, N, K = len(counts), 256, 384
+    off = inputs.group_offsets(counts)
+    xa = inputs.normal_bf16((int(off[-1]), K), 7)
+    xw = inputs.normal_bf16((G * N, K), 8, std=0.02)
+    ca, sa, _ = _q_oracle(xa, "mxfp8_e4m3")
+    cw, sw, _ = _q_oracle(xw, "mxfp8_e4m3")
+    A = upload_q(bsq, "mxfp8_e4m3", ca, sa)
+    W = upload_q(bsq, "mxfp8_e4m3", cw, sw)
+    offd = torch.from_numpy(off).cuda()
+    C = bsq.grouped_gemm(A, offd, bsq.group_views(W, G), torch.float32).cpu().numpy()
+    Ad = oracle.dequant_rows(ca, sa, "mxfp8_e4m3")
+    Wd = oracle.dequant_rows(cw, sw, "mxfp8_e4m3")
+    for g in range(G):
+        lo, hi = off[g], off[g + 1]
+        if hi == lo:
+            continue
+        ref, mag = oracle.gemm_full(Ad[lo:hi], Wd[g * N:(g + 1) * N])
+        ok, err, tol = gemm_tol_ok(C[lo:hi], ref, mag, False)
+        assert ok.all(), (g, (~ok).sum())
+
+
+# ----------------------------------------------------------------- failures
+def test_timeout_probe_reports_status(bsq):
+    bsq.sync_status()
+    bsq.debug_timeout_probe(2_000_000)          # 2 ms limit, nothing ever arrives
+    with pytest.raises(bsq.BsqError) as ei:
+        bsq.sync_status()
+    assert ei.value.status == 5
+    bsq.sync_status()                           # cleared; context still usable
+
+
+def test_gemm_rejects_bad_args(bsq):
+    import torch
+    A = bsq.empty("mxfp8_e4m3", 128, 256)
+    B = bsq.empty("mxfp8_e4m3", 128, 512)
+    with pytest.raises(bsq.BsqError):
+        bsq.gemm(A, B)
+    Bn = bsq.empty("nvfp4", 128, 256)
+    with pytest.raises(bsq.BsqError) as ei:
+        bsq.gemm(A, Bn)
+    assert ei.value.status == 2
