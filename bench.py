@@ -1,0 +1,490 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-scaled low-precision linear layer on GB300.
+
+One step is one pass of the whole hot path over one synthetic batch, with
+every input resident in HBM when the timed region starts:
+
+  forward  (Llama-3-8B MLP up-projection, MXFP8 E4M3)
+      quantize X[8192,4096] row, W[14336,4096] row; Y = X W^T (BF16 out)
+  backward (MXFP8, gradients E5M2)
+      quantize dY[8192,14336] both (row + column), W column, X column;
+      dX = dY W (8192x4096, K=14336); dW = dY^T X (14336x4096, K=8192)
+  NVFP4 forward
+      quantize X[8192,4096], W[4096,4096], X'[8192,14336], W'[4096,14336]
+      (tensor amax + 16-block quantize); Y = X W^T, Y' = X' W'^T
+  MoE grouped (64 experts, 32768 rows, Zipf(1.1) counts, K=7168, N=2048)
+      quantize activations to MXFP4, re-encode MXFP4 -> MXFP8, quantize the
+      expert weights to E4M3, grouped GEMM (BF16 out)
+
+value = block-scaled GEMM FLOPs of the step / device time of the whole step
+(quantize + re-encode + GEMMs), TFLOP/s.  Per-kernel times come from CUDA
+events on the launching stream inside the timed region; the roofline of the
+dominant kernel (the FP8 GEMM) and of every step are reported against the
+measured peaks.  e2e repeats the step through the same C ABI with the BF16
+inputs copied from pinned host memory and the outputs read back, every step.
+
+Run: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+Under torchrun each rank runs its own replica of the step (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantize GB/s vs HBM peak; block-scaled GEMM TFLOP/s vs dense FP8/FP4 peak"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--small", action="store_true", help="1/8-size shapes (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-reps", type=int, default=4)
+    ap.add_argument("--part", default="all", choices=["all", "fwd", "bwd", "nv", "moe"],
+                    help="run one part of the step only (profiling)")
+    return ap.parse_args()
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")})
+        p["source"] = "measured"
+    except Exception:
+        pass
+    p["fp8_tflops"] = 2 * p["bf16_tflops"]
+    p["fp4_tflops"] = 4 * p["bf16_tflops"]
+    return p
+
+
+# ----------------------------------------------------------------- shapes
+def shapes(small: bool):
+    d = 8 if small else 1
+    return {
+        "fwd": dict(M=8192 // d, N=14336 // d, K=4096),
+        "nv": dict(M=8192 // d, N=4096 // d, K=4096, K2=14336),
+        "moe": dict(rows=32768 // d, experts=64, K=7168, N=2048 // d if small else 2048),
+    }
+
+
+def make_inputs(sh, part="all"):
+    from block_scaled_precision_03_gb300 import inputs
+    f, n, m = sh["fwd"], sh["nv"], sh["moe"]
+    h = {}
+    if part in ("all", "fwd", "bwd"):
+        h["X"] = inputs.outlier_activations_bf16((f["M"], f["K"]), 0)
+        h["W"] = inputs.normal_bf16((f["N"], f["K"]), 1, std=0.02)
+    if part in ("all", "bwd"):
+        h["dY"] = inputs.loguniform_grad_bf16((f["M"], f["N"]), 2)
+    if part in ("all", "nv"):
+        nv = inputs.nvfp4_forward(n["M"], n["N"], n["K"], n["K2"], seed=10)
+        h.update({"X4": nv["X"], "W4": nv["W"], "X42": nv["X2"], "W42": nv["W2"]})
+    if part in ("all", "moe"):
+        moe = inputs.moe_grouped(m["rows"], m["experts"], m["K"], m["N"], seed=20)
+        h.update({"A_moe": moe["A"], "W_moe": moe["W"].reshape(-1, m["K"]), "offsets": moe["offsets"],
+                  "counts": moe["counts"]})
+    return h
+
+
+# ------------------------------------------------------------- GPU step
+class Step:
+    """Device buffers and the ordered list of C-ABI calls of one step."""
+
+    def __init__(self, host, sh, part="all"):
+        import numpy as np
+        import torch
+        import block_scaled_precision_03_gb300 as bsq
+        self.bsq, self.torch, self.sh = bsq, torch, sh
+        bsq.lib()
+
+        def dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+        self.host = host
+        self.inp = {k: dev(host[k]) for k in ("X", "W", "dY", "X4", "W4", "X42", "W42", "A_moe", "W_moe")
+                    if k in host}
+        self.offsets = torch.from_numpy(host["offsets"]).cuda() if "offsets" in host else None
+        want = {"all": ("fwd", "bwd", "nv", "moe")}.get(part, (part,))
+        f, n, m = sh["fwd"], sh["nv"], sh["moe"]
+        M, N, K = f["M"], f["N"], f["K"]
+        E = bsq.empty
+        o = {}
+        if "fwd" in want or "bwd" in want:
+            o["Xq"] = E("mxfp8_e4m3", M, K)
+            o["Wq"] = E("mxfp8_e4m3", N, K)
+            o["Y"] = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        if "bwd" in want:
+            o["dYr"] = E("mxfp8_e5m2", M, N)
+            o["dYc"] = E("mxfp8_e5m2", N, M)
+            o["Wc"] = E("mxfp8_e4m3", K, N)
+            o["Xc"] = E("mxfp8_e4m3", K, M)
+            o["dX"] = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+            o["dW"] = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+        if "nv" in want:
+            o["X4q"] = E("nvfp4", n["M"], n["K"])
+            o["W4q"] = E("nvfp4", n["N"], n["K"])
+            o["X42q"] = E("nvfp4", n["M"], n["K2"])
+            o["W42q"] = E("nvfp4", n["N"], n["K2"])
+            o["Y4"] = torch.empty((n["M"], n["N"]), dtype=torch.bfloat16, device="cuda")
+            o["Y42"] = torch.empty((n["M"], n["N"]), dtype=torch.bfloat16, device="cuda")
+        if "moe" in want:
+            o["A4"] = E("mxfp4", m["rows"], m["K"])
+            o["A8"] = E("mxfp8_e4m3", m["rows"], m["K"])
+            o["Wm"] = E("mxfp8_e4m3", m["experts"] * m["N"], m["K"])
+            o["Ym"] = torch.empty((m["rows"], m["N"]), dtype=torch.bfloat16, device="cuda")
+        self.out = o
+        self.wm_groups = bsq.group_views(o["Wm"], m["experts"]) if "moe" in want else None
+        i = self.inp
+        q = bsq.quantize_into
+        # (name, row, kind, fn, bytes, flops, kernels)
+        B_ROW8, B_ROW4, B_BOTH, B_NV, B_REPACK = 2 + 1 + 1 / 32, 2 + 0.5 + 1 / 32, 2 + 2 * (1 + 1 / 32), \
+            2 + 2 + 0.5 + 1 / 16, 0.5 + 1 / 32 + 1 + 1 / 32
+        mn = m["rows"] * m["K"]
+        ops = [
+            ("quant X e4m3 row", "a1", "quant", lambda: q(i["X"], "mxfp8_e4m3", "row", o["Xq"], None), M * K * B_ROW8, 0, 1),
+            ("quant W e4m3 row", "a1", "quant", lambda: q(i["W"], "mxfp8_e4m3", "row", o["Wq"], None), N * K * B_ROW8, 0, 1),
+            ("gemm fwd Y=XW^T", "a4", "gemm8", lambda: bsq.gemm_into(o["Xq"], o["Wq"], o["Y"]), 0, 2 * M * N * K, 1),
+            ("quant dY e5m2 both", "a2", "quant", lambda: q(i["dY"], "mxfp8_e5m2", "both", o["dYr"], o["dYc"]), M * N * B_BOTH, 0, 1),
+            ("quant W e4m3 col", "a2", "quant", lambda: q(i["W"], "mxfp8_e4m3", "col", None, o["Wc"]), N * K * B_ROW8, 0, 1),
+            ("quant X e4m3 col", "a2", "quant", lambda: q(i["X"], "mxfp8_e4m3", "col", None, o["Xc"]), M * K * B_ROW8, 0, 1),
+            ("gemm dgrad dX=dY W", "a4", "gemm8", lambda: bsq.gemm_into(o["dYr"], o["Wc"], o["dX"]), 0, 2 * M * K * N, 1),
+            ("gemm wgrad dW=dY^T X", "a4", "gemm8", lambda: bsq.gemm_into(o["dYc"], o["Xc"], o["dW"]), 0, 2 * N * K * M, 1),
+            ("quant X nvfp4", "a3", "quant", lambda: q(i["X4"], "nvfp4", "row", o["X4q"], None), n["M"] * n["K"] * B_NV, 0, 3),
+            ("quant W nvfp4", "a3", "quant", lambda: q(i["W4"], "nvfp4", "row", o["W4q"], None), n["N"] * n["K"] * B_NV, 0, 3),
+            ("quant X' nvfp4", "a3", "quant", lambda: q(i["X42"], "nvfp4", "row", o["X42q"], None), n["M"] * n["K2"] * B_NV, 0, 3),
+            ("quant W' nvfp4", "a3", "quant", lambda: q(i["W42"], "nvfp4", "row", o["W42q"], None), n["N"] * n["K2"] * B_NV, 0, 3),
+            ("gemm nvfp4 Y=XW^T", "a4", "gemm4", lambda: bsq.gemm_into(o["X4q"], o["W4q"], o["Y4"]), 0, 2 * n["M"] * n["N"] * n["K"], 1),
+            ("gemm nvfp4 Y'=X'W'^T", "a4", "gemm4", lambda: bsq.gemm_into(o["X42q"], o["W42q"], o["Y42"]), 0, 2 * n["M"] * n["N"] * n["K2"], 1),
+            ("quant A_moe mxfp4 row", "a1", "quant", lambda: q(i["A_moe"], "mxfp4", "row", o["A4"], None), mn * B_ROW4, 0, 1),
+            ("repack mxfp4->mxfp8", "a5", "repack", lambda: bsq.mxfp4_to_mxfp8_into(o["A4"], o["A8"]), mn * B_REPACK, 0, 1),
+            ("quant W_moe e4m3 row", "a1", "quant", lambda: q(i["W_moe"], "mxfp8_e4m3", "row", o["Wm"], None),
+             m["experts"] * m["N"] * m["K"] * B_ROW8, 0, 1),
+            ("grouped gemm moe", "a6", "gemm8", lambda: bsq.grouped_gemm_into(o["A8"], self.offsets, self.wm_groups, o["Ym"]),
+             0, 2 * m["rows"] * m["N"] * m["K"], 1),
+        ]
+        part_of = ["fwd"] * 3 + ["bwd"] * 5 + ["nv"] * 6 + ["moe"] * 4
+        if part == "bwd":
+            want = ("fwd", "bwd")      # the backward quantizes from the forward inputs
+        ops = [op for op, pt in zip(ops, part_of) if pt in want]
+        self.ops = ops
+        self.flops = sum(op[5] for op in ops)
+        self.kernels = sum(op[6] for op in ops)
+
+    def run(self, events=None):
+        for j, op in enumerate(self.ops):
+            if events is not None:
+                events[j][0].record()
+            op[3]()
+            if events is not None:
+                events[j][1].record()
+
+    # e2e: host (pinned) -> device copies of every BF16 input, the step, and a
+    # device -> host read of every output, all inside the timed region
+    def setup_e2e(self):
+        import numpy as np
+        torch = self.torch
+        self.pinned_in = {k: torch.from_numpy(np.ascontiguousarray(self.host[k]).view(np.int16))
+                          .view(torch.bfloat16).pin_memory() for k in self.inp}
+        outs = [k for k in ("Y", "dX", "dW", "Y4", "Y42", "Ym") if k in self.out]
+        self.pinned_out = {k: torch.empty(self.out[k].shape, dtype=torch.bfloat16).pin_memory() for k in outs}
+        self.h2d = sum(t.numel() * 2 for t in self.pinned_in.values())
+        self.d2h = sum(t.numel() * 2 for t in self.pinned_out.values())
+
+    def run_e2e(self):
+        for k, h in self.pinned_in.items():
+            self.inp[k].copy_(h, non_blocking=True)
+        self.run()
+        for k, h in self.pinned_out.items():
+            h.copy_(self.out[k], non_blocking=True)
+
+
+# ------------------------------------------------------------- clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        mx = max(float(r[2]) for r in rows)
+        load = [s for s, r in zip(sm, rows) if float(r[3]) > 300.0] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def cpu_forward_slice(host, rows=64, wrows=2048):
+    """The oracle's forward on a slice: quantize X[:rows] and W[:wrows] (E4M3),
+    dequantize, FP64 GEMM.  Returns (seconds, flops)."""
+    import oracle
+    X, W = host["X"][:rows], host["W"][:wrows]
+    t0 = time.perf_counter()
+    cx, sx = oracle.mx_quantize_rows(X, "mxfp8_e4m3")
+    cw, sw = oracle.mx_quantize_rows(W, "mxfp8_e4m3")
+    A = oracle.dequant_rows(cx, sx, "mxfp8_e4m3")
+    B = oracle.dequant_rows(cw, sw, "mxfp8_e4m3")
+    oracle.gemm_full(A, B)
+    return time.perf_counter() - t0, 2.0 * rows * wrows * X.shape[1]
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+CPU_SAMPLE = "oracle forward slice: E4M3 quantize of X[:64,4096] and W[:2048,4096], exact dequantize, FP64 GEMM 64x2048x4096"
+
+
+# ------------------------------------------------------------------ main
+def dist_setup(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores: each step is the
+    bounded forward slice of the same workload."""
+    if rank != 0:
+        return
+    sh = shapes(args.small)
+    from block_scaled_precision_03_gb300 import inputs
+    f = sh["fwd"]
+    host = {"X": inputs.outlier_activations_bf16((64, f["K"]), 0),
+            "W": inputs.normal_bf16((2048, f["K"]), 1, std=0.02)}
+    for _ in range(args.warmup):
+        cpu_forward_slice(host)
+    ts, fl = [], 0.0
+    for _ in range(args.steps):
+        t, fl = cpu_forward_slice(host)
+        ts.append(t)
+    total = sum(ts)
+    value = fl * args.steps / total / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": "llama3-8b block-scaled linear layer (CPU oracle slice)",
+                                            "sample": CPU_SAMPLE},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": CPU_SAMPLE},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    import torch.distributed as dist
+    assert torch.cuda.is_available(), "bench needs a CUDA device"
+    torch.cuda.set_device(local)
+    pk = peaks()
+    sh = shapes(args.small)
+    host = make_inputs(sh, args.part)
+    step = Step(host, sh, args.part)
+    nops = len(step.ops)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 0)):
+        step.run()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, per-op events on the launching stream
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nops)]
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(local)
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    start.record()
+    for s in range(args.steps):
+        step.run(ev[s])
+    stop.record()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    value = world * step.flops / (ms_step * 1e-3) / 1e12
+
+    # per-op averages
+    op_ms = [statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)) for j in range(nops)]
+    rows, agg = {}, {}
+    for (name, row, kind, _, nbytes, flops, nk), ms in zip(step.ops, op_ms):
+        if flops:
+            peak = pk["fp4_tflops"] if kind == "gemm4" else pk["fp8_tflops"]
+            ach = flops / (ms * 1e-3) / 1e12
+            rec = {"ms": round(ms, 4), "tflops": round(ach, 1), "frac": round(ach / peak, 4)}
+        else:
+            ach = nbytes / (ms * 1e-3) / 1e9
+            rec = {"ms": round(ms, 4), "gbs": round(ach, 1), "frac": round(ach / pk["hbm_gbs"], 4),
+                   "frac_spec_8tbs": round(ach / 8000.0, 4)}
+        rows[name] = dict(row=row, **rec)
+        a = agg.setdefault(kind, [0.0, 0.0, 0.0])
+        a[0] += ms
+        a[1] += nbytes
+        a[2] += flops
+    for kind in ("quant", "repack", "gemm8", "gemm4"):
+        agg.setdefault(kind, [1e-30, 0.0, 0.0])
+    q_ms, q_bytes = agg["quant"][0] + agg["repack"][0], agg["quant"][1] + agg["repack"][1]
+    g8_ms, g8_fl = agg["gemm8"][0], agg["gemm8"][2]
+    g4_ms, g4_fl = agg["gemm4"][0], agg["gemm4"][2]
+    g8 = g8_fl / (g8_ms * 1e-3) / 1e12
+    # roofline of the dominant kernel (FP8 GEMM), taken on its largest launch:
+    # the forward GEMM (2*M*N*K FLOPs per launch / its average event time)
+    fwd = next((j for j, op in enumerate(step.ops) if op[0].startswith("gemm fwd")), None)
+    jr = fwd if fwd is not None else next(j for j, op in enumerate(step.ops) if op[2] == "gemm8")
+    ach = step.ops[jr][5] / (op_ms[jr] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["fp8_tflops"], 4), "traffic": None,
+                "kernel": "gemm_kernel<fp8> (tcgen05 mxf8f6f4 block_scale), launch: " + step.ops[jr][0],
+                "flops_per_launch": step.ops[jr][5], "ms_per_launch": round(op_ms[jr], 4),
+                "peak_note": f"2x {pk['source']} bf16 burst {pk['bf16_tflops']} TFLOP/s (FP8 = 2x BF16 rate)",
+                "frac_vs_sustained": round(ach / (2 * pk["bf16_tflops_sustained"]), 4),
+                "all_fp8_gemm_launches_tflops": round(g8, 1)}
+    traffic = _profile_traffic()
+    if traffic is not None:
+        roofline["traffic"] = traffic
+
+    # ---- e2e through the same C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        step.setup_e2e()
+        step.run_e2e()
+        torch.cuda.synchronize()
+        ke = max(1, min(args.steps, 5))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        s0.record()
+        for _ in range(ke):
+            step.run_e2e()
+        s1.record()
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = s0.elapsed_time(s1) / ke
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(world * step.flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e_ms, 3), "steps": ke,
+               "h2d_bytes_per_step": step.h2d, "d2h_bytes_per_step": step.d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu and "X" in host:
+        reps = max(1, args.cpu_reps)
+        ts = [cpu_forward_slice(host) for _ in range(reps)]
+        t_tot = sum(t for t, _ in ts)
+        cpu = {"value": ts[0][1] * reps / t_tot / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+               "kind": "oracle", "sample": CPU_SAMPLE, "seconds": round(t_tot, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3/e5m2/e2m1 codes, f32 accumulate", "data": "synthetic",
+            "config": {"workload": "llama3-8b block-scaled linear layer step: MXFP8 fwd 8192x14336x4096 + "
+                                   "MXFP8 bwd (dgrad, wgrad) + NVFP4 fwd (4096/14336) + MoE 64-expert grouped "
+                                   "(MXFP4 -> MXFP8 repack, 32768x2048x7168)" + (" [1/8 size]" if args.small else "") + ("" if args.part == "all" else f" [part {args.part}]"),
+                       "parallelism": f"replica x{world}",
+                       "l2": "inputs larger than L2: each step streams ~9 GB, evicting the previous step's data",
+                       "value_def": "GEMM FLOPs / whole-step device time"},
+            "quantize_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+            "quantize_frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "gemm_fp8_tflops": round(g8, 1), "gemm_nvfp4_tflops": round(g4_fl / (g4_ms * 1e-3) / 1e12, 1),
+            "roofline": roofline, "rows": rows, "gpu_launches": step.kernels * args.steps,
+            "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "peaks": {k: pk[k] for k in ("hbm_gbs", "fp8_tflops", "fp4_tflops", "source")},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _profile_traffic():
+    """DRAM bytes per launch of the FP8 GEMM from the committed ncu summary,
+    only if that summary was taken on the current GEMM source."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, "block_scaled_precision_03_gb300", "csrc", "gemm.cu"), "rb").read()
+        sha = hashlib.sha256(src).hexdigest()[:16]
+        vals = {}
+        with open(os.path.join(ROOT, "profiles", "gemm_fp8_fwd_8192x14336x4096.md")) as f:
+            for line in f:
+                if ":" in line and line.startswith("- "):
+                    k, v = line[2:].split(":", 1)
+                    vals[k.strip()] = v.strip().strip("`")
+        if vals.get("gemm.cu sha256[:16]") != sha:
+            return None
+        return float(vals["dram bytes per full launch"])
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()

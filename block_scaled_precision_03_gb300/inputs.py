@@ -44,15 +44,18 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def _chunked(n: int, seed: int, fill):
-    """Fill a float32 vector of n values chunk by chunk (deterministic)."""
-    out = np.empty(n, dtype=np.float32)
+def _chunked(n: int, seed: int, fill) -> np.ndarray:
+    """Draw n float32 values chunk by chunk (deterministic chunk seeds) and
+    return them rounded to BF16 bit patterns."""
+    out = np.empty(n, dtype=np.uint16)
     nchunks = max(1, (n + CHUNK - 1) // CHUNK)
     seeds = np.random.SeedSequence(seed).spawn(nchunks)
 
     def work(i):
         lo, hi = i * CHUNK, min(n, (i + 1) * CHUNK)
-        fill(np.random.default_rng(seeds[i]), out[lo:hi])
+        buf = np.empty(hi - lo, dtype=np.float32)
+        fill(np.random.default_rng(seeds[i]), buf)
+        out[lo:hi] = f32_to_bf16_bits(buf)
 
     threads = min(nchunks, os.cpu_count() or 1, 16)
     if threads <= 1:
@@ -73,7 +76,7 @@ def normal_bf16(shape, seed: int, std: float = 1.0) -> np.ndarray:
         if std != 1.0:
             dst *= np.float32(std)
 
-    return f32_to_bf16_bits(_chunked(n, seed, fill)).reshape(shape)
+    return _chunked(n, seed, fill).reshape(shape)
 
 
 def outlier_activations_bf16(shape, seed: int, rate: float = 0.001, factor: float = 50.0):
@@ -85,7 +88,7 @@ def outlier_activations_bf16(shape, seed: int, rate: float = 0.001, factor: floa
         mask = rng.random(dst.size, dtype=np.float32) < rate
         dst[mask] *= np.float32(factor)
 
-    return f32_to_bf16_bits(_chunked(n, seed, fill)).reshape(shape)
+    return _chunked(n, seed, fill).reshape(shape)
 
 
 def loguniform_grad_bf16(shape, seed: int, lo_exp: float = -20.0, hi_exp: float = 4.0):
@@ -97,7 +100,7 @@ def loguniform_grad_bf16(shape, seed: int, lo_exp: float = -20.0, hi_exp: float 
         sign = np.where(rng.random(dst.size, dtype=np.float32) < 0.5, -1.0, 1.0).astype(np.float32)
         dst[:] = sign * np.exp2(e)
 
-    return f32_to_bf16_bits(_chunked(n, seed, fill)).reshape(shape)
+    return _chunked(n, seed, fill).reshape(shape)
 
 
 def zipf_group_counts(total_rows: int, groups: int, s: float, seed: int) -> np.ndarray:

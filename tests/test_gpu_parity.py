@@ -45,7 +45,7 @@ def test_quantize_rows(bsq, fmt, shape, kind):
     assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} row {shape}")
 
 
-COL_SHAPES = [(256, 256), (96, 130), (32, 8), (4096, 16), (1056, 384), (160, 136)]
+COL_SHAPES = [(256, 256), (96, 200), (32, 8), (4096, 16), (1056, 384), (160, 136)]
 
 
 @pytest.mark.parametrize("fmt", FMTS)
@@ -283,6 +283,13 @@ def test_timeout_probe_reports_status(bsq):
         bsq.sync_status()
     assert ei.value.status == 5
     bsq.sync_status()                           # cleared; context still usable
+
+
+def test_quantize_rejects_unaligned_cols(bsq):
+    x = inputs.normal_bf16((96, 130), 1)
+    with pytest.raises(bsq.BsqError) as ei:
+        bsq.quantize(dev_bf16(x), "mxfp8_e4m3", "col")
+    assert ei.value.status == 3
 
 
 def test_gemm_rejects_bad_args(bsq):
