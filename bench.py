@@ -396,7 +396,8 @@ def main():
     # roofline of the dominant kernel (FP8 GEMM), taken on its largest launch:
     # the forward GEMM (2*M*N*K FLOPs per launch / its average event time)
     fwd = next((j for j, op in enumerate(step.ops) if op[0].startswith("gemm fwd")), None)
-    jr = fwd if fwd is not None else next(j for j, op in enumerate(step.ops) if op[2] == "gemm8")
+    jr = fwd if fwd is not None else next((j for j, op in enumerate(step.ops) if op[2] == "gemm8"),
+                                          next((j for j, op in enumerate(step.ops) if op[5]), 0))
     ach = step.ops[jr][5] / (op_ms[jr] * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
                 "frac": round(ach / pk["fp8_tflops"], 4), "traffic": None,

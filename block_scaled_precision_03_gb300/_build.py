@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbsq.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["api.cu", "quantize.cu", "convert.cu", "gemm.cu"]
+SOURCES = ["api.cu", "quantize.cu", "convert.cu", "gemm.cu", "gemm2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

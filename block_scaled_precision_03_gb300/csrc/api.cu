@@ -2,6 +2,7 @@
 // Every check runs on the host before anything is launched; a rejected call
 // launches nothing and writes nothing.
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include "../../include/bsq.h"
 #include "common.cuh"
@@ -55,6 +56,14 @@ bsq_status check_tensor(const bsq_tensor* t, bool need_ts) {
 }
 
 bsq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? BSQ_OK : BSQ_ERR_CUDA; }
+
+// BSQ_GEMM_1CTA=1 routes dense GEMMs to the single-CTA kernel (the grouped
+// GEMM's kernel) instead of the CTA-pair kernel; used by the test suite to
+// check both tile shapes.
+bool env_single_cta() {
+    const char* v = std::getenv("BSQ_GEMM_1CTA");
+    return v && v[0] == '1';
+}
 
 const uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
 
@@ -173,6 +182,7 @@ bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t o
     a.C = C;
     a.out_bf16 = out_type == BSQ_OUT_BF16;
     a.num_groups = 0;
+    a.single_cta = env_single_cta();
     a.num_sms = num_sms();
     a.status = st;
     a.timeout_ns = kDefaultTimeoutNs;

@@ -25,9 +25,13 @@
 #include <cuda.h>
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
+#include "epilogue.cuh"
+#include "tmap.h"
 
 namespace bsq {
 namespace {
+using namespace tc;
 
 constexpr int BM = 128;            // tile rows (A)
 constexpr int BN = 256;            // tile columns (B rows)
@@ -74,97 +78,6 @@ struct Params {
     uint64_t timeout_ns;
     const uint8_t* sfb_group[kMaxGroups];
 };
-
-// ------------------------------------------------------------------ PTX
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred P;\n\t"
-                 "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, P;\n\t}"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
-// Bounded wait: false when the CTA is aborting or the time limit passed.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       unsigned* status, uint64_t limit_ns) {
-    uint64_t t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 255u) == 255u) {
-            if (*abort_flag) return false;
-            const uint64_t now = globaltimer_ns();
-            if (t0 == 0) t0 = now;
-            else if (now - t0 > limit_ns) {
-                *abort_flag = 1;
-                record_status(status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
-    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar) : "memory");
-}
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
-}
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
-}
-template <bool FP4>
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                       uint32_t sfb, uint32_t acc) {
-    if (FP4) {
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
-                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb) : "memory");
-    } else {
-        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
-                     :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb) : "memory");
-    }
-}
-#define BSQ_LD32(r, taddr)                                                                              \
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"  \
-                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"              \
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),   \
-                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),            \
-                   "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),         \
-                   "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),         \
-                   "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),         \
-                   "=r"(r[31])                                                                           \
-                 : "r"(taddr))
-
-// Shared-memory matrix descriptor, K-major operand tile with 128-byte
-// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// Descriptor of one 512-byte scale atom: 32 rows of 16 bytes, no swizzle,
-// 8-row core matrices 128 bytes apart.
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
-}
 
 struct TileInfo {
     int32_t a_row0;       // first A row of the tile (multiple of 128)
@@ -238,13 +151,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tmem_alloc<1>(smem_u32(tmem_slot), kTmemCols);
     }
     int total = p.total_tiles;
     if (p.num_groups > 0 && warp == 2 && lane == 0) {
@@ -259,9 +170,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             gt->prefix[g + 1] = acc;
         }
     }
-    tc_fence_before();
+    fence_before();
     __syncthreads();
-    tc_fence_after();
+    fence_after();
     if (p.num_groups > 0) total = gt->prefix[p.num_groups];
     const uint32_t tmem = *tmem_slot;
 
@@ -310,46 +221,73 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // Software-pipelined: the scale copies of step i+1 are issued right
+        // after the MMAs of step i (steps run across tile boundaries).
         if (lane == 0) {
+            auto issue_cp = [&](int st) {
+                const uint32_t sfa_t = tmem + kSfCol0 + st * CF::SF_COLS;
+                const uint32_t sfb_t = sfa_t + (FP4 ? 16 : 4);
+                const uint32_t sf_s = smem_u32(smSF + st * CF::SF_STAGE);
+#pragma unroll
+                for (int a = 0; a < CF::SF_ATOMS; a++) {
+                    cp_sf<1>(sfa_t + 4 * a, desc_sf(sf_s + a * 512));
+#pragma unroll
+                    for (int rt = 0; rt < 2; rt++)
+                        cp_sf<1>(sfb_t + 8 * a + 4 * rt, desc_sf(sf_s + CF::SFA_BYTES + (rt * CF::SF_ATOMS + a) * 512));
+                }
+            };
             int stage = 0;
             uint32_t phase = 0;
             int iter = 0;
             bool ok = true, any = false;
+            if ((int)blockIdx.x < total) {
+                ok = mbar_wait(full0, 0, abort_flag, p.status, p.timeout_ns);
+                if (ok) {
+                    fence_after();
+                    issue_cp(0);
+                }
+            }
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++iter) {
                 if (!mbar_wait(tempty, (iter & 1) ^ 1, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
-                tc_fence_after();
+                fence_after();
+                const bool more_tiles = t + (int)gridDim.x < total;
                 for (int kb = 0; kb < p.k_stages; kb++) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
-                    tc_fence_after();
                     const uint32_t sfa_t = tmem + kSfCol0 + stage * CF::SF_COLS;
                     const uint32_t sfb_t = sfa_t + (FP4 ? 16 : 4);
-                    const uint32_t sf_s = smem_u32(smSF + stage * CF::SF_STAGE);
-                    for (int a = 0; a < CF::SF_ATOMS; a++) {
-                        tc_cp_sf(sfa_t + 4 * a, desc_sf(sf_s + a * 512));
-                        for (int rt = 0; rt < 2; rt++)
-                            tc_cp_sf(sfb_t + 8 * a + 4 * rt, desc_sf(sf_s + CF::SFA_BYTES + (rt * CF::SF_ATOMS + a) * 512));
-                    }
-                    const uint32_t a_s = smem_u32(smA + stage * A_BYTES), b_s = smem_u32(smB + stage * B_BYTES);
+                    const uint64_t ad0 = desc_sw128(smem_u32(smA + stage * A_BYTES));
+                    const uint64_t bd0 = desc_sw128(smem_u32(smB + stage * B_BYTES));
                     const int nk = kb == p.k_stages - 1 ? p.mma_last : 4;
                     for (int k = 0; k < nk; k++) {
-                        const uint64_t ad = desc_sw128(a_s + 32 * k), bd = desc_sw128(b_s + 32 * k);
-                        if (FP4) {
-                            tc_mma<true>(tmem, ad, bd, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k, (kb | k) != 0);
-                        } else {
-                            const uint32_t id = p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29);
-                            tc_mma<false>(tmem, ad, bd, id, sfa_t, sfb_t, (kb | k) != 0);
-                        }
+                        // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
+                        const uint64_t ad = ad0 + 2 * k, bd = bd0 + 2 * k;
+                        if (FP4)
+                            mma<1, true>(tmem, ad, bd, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k, (kb | k) != 0);
+                        else
+                            mma<1, false>(tmem, ad, bd, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa_t, sfb_t,
+                                          (kb | k) != 0);
                     }
                     any = true;
-                    tc_commit(empty0 + 8 * stage);
-                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                    int nstage = stage + 1;
+                    uint32_t nphase = phase;
+                    if (nstage == STAGES) { nstage = 0; nphase ^= 1; }
+                    if (kb + 1 < p.k_stages || more_tiles) {
+                        if (mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status, p.timeout_ns)) {
+                            fence_after();
+                            issue_cp(nstage);
+                        } else {
+                            ok = false;
+                        }
+                    }
+                    commit<1>(empty0 + 8 * stage);
+                    if (kb == p.k_stages - 1) commit<1>(tfull);
+                    stage = nstage;
+                    phase = nphase;
+                    if (!ok) break;
                 }
-                if (!ok) break;
-                tc_commit(tfull);
             }
             if (!ok && any) {
                 // wait for the MMAs already issued before TMEM is released
-                tc_commit(drain);
+                commit<1>(drain);
                 volatile int no_abort = 0;
                 mbar_wait(drain, 0, &no_abort, nullptr, 100000000ull);
             }
@@ -364,107 +302,34 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++iter) {
             const TileInfo ti = tile_info(p, t, gt, gcur);
             if (!mbar_wait(tfull, iter & 1, abort_flag, p.status, p.timeout_ns)) break;
-            tc_fence_after();
+            fence_after();
             uint32_t r[4][32];
             const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
-            BSQ_LD32(r[0], ta);
-            BSQ_LD32(r[1], ta + 32);
-            BSQ_LD32(r[2], ta + 64);
-            BSQ_LD32(r[3], ta + 96);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            tc_fence_before();
+            BSQ_TMEM_LD32(r[0], ta);
+            BSQ_TMEM_LD32(r[1], ta + 32);
+            BSQ_TMEM_LD32(r[2], ta + 64);
+            BSQ_TMEM_LD32(r[3], ta + 96);
+            tmem_wait_ld();
+            fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty);
 
             const int row = ti.a_row0 + q * 32 + lane;
             const int col0 = ti.n0 + h * 128;
             if (row < ti.row_lo || row >= ti.row_hi || col0 >= p.N) continue;
-            if (p.out_bf16) {
-                __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + (int64_t)row * p.ldc + col0;
-                if (p.vec_ok && col0 + 128 <= p.N) {
-#pragma unroll
-                    for (int j = 0; j < 16; j++) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; e++) {
-                            const float x0 = __uint_as_float(r[j >> 2][(j & 3) * 8 + 2 * e]) * alpha;
-                            const float x1 = __uint_as_float(r[j >> 2][(j & 3) * 8 + 2 * e + 1]) * alpha;
-                            w[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x0)) |
-                                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x1)) << 16);
-                        }
-                        *reinterpret_cast<uint4*>(out + 8 * j) = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 128; j++)
-                        if (col0 + j < p.N) out[j] = __float2bfloat16_rn(__uint_as_float(r[j >> 5][j & 31]) * alpha);
-                }
-            } else {
-                float* out = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + col0;
-                if (p.vec_ok && col0 + 128 <= p.N) {
-#pragma unroll
-                    for (int j = 0; j < 32; j++) {
-                        float4 v;
-                        v.x = __uint_as_float(r[j >> 3][(j & 7) * 4 + 0]) * alpha;
-                        v.y = __uint_as_float(r[j >> 3][(j & 7) * 4 + 1]) * alpha;
-                        v.z = __uint_as_float(r[j >> 3][(j & 7) * 4 + 2]) * alpha;
-                        v.w = __uint_as_float(r[j >> 3][(j & 7) * 4 + 3]) * alpha;
-                        *reinterpret_cast<float4*>(out + 4 * j) = v;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 128; j++)
-                        if (col0 + j < p.N) out[j] = __uint_as_float(r[j >> 5][j & 31]) * alpha;
-                }
-            }
+            store_row128(r, p.C, p.ldc, row, col0, p.N, p.out_bf16, p.vec_ok, alpha);
         }
     }
 
-    tc_fence_before();
+    fence_before();
     __syncthreads();
     if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols) : "memory");
+        fence_after();
+        tmem_dealloc<1>(tmem, kTmemCols);
     }
 }
 
 // ----------------------------------------------------------------- host
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
-    return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t row_bytes, uint32_t box_rows) {
-    EncodeTiledFn enc = get_encode();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)BKB, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// tcgen05 instruction descriptor (block-scaled kinds), without scale ids:
-// bits 7-9 A type, 10-12 B type, 17-22 N>>3, 23 scale type (1 = UE8M0),
-// 24-28 M>>4; K-major A and B, no negation, dense.
-uint32_t make_idesc(uint32_t atype, uint32_t btype, bool ue8m0) {
-    return (atype << 7) | (btype << 10) | ((uint32_t)(BN >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
-           ((uint32_t)(BM >> 4) << 24);
-}
-
 template <bool FP4>
 cudaError_t launch(const GemmArgs& a, const Params& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
                    cudaStream_t st) {
@@ -482,6 +347,7 @@ cudaError_t launch(const GemmArgs& a, const Params& p, const CUtensorMap& ta, co
 }  // namespace
 
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st) {
+    if (a.num_groups == 0 && !a.single_cta) return run_gemm_pair(a, st);
     const bool fp4 = a.fmt_a == kNVFP4;
     const int64_t kbytes = fp4 ? a.K / 2 : a.K;
     const int blk = fp4 ? 16 : 32;
@@ -507,8 +373,8 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st) {
     p.vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && ((a.N * esz) % 16 == 0);
     p.ts_a = a.ts_a;
     p.ts_b = a.ts_b;
-    if (fp4) p.idesc = make_idesc(1, 1, false);
-    else p.idesc = make_idesc(a.fmt_a == kE5M2 ? 1 : 0, a.fmt_b == kE5M2 ? 1 : 0, true);
+    if (fp4) p.idesc = make_idesc(1, 1, false, BM, BN);
+    else p.idesc = make_idesc(a.fmt_a == kE5M2 ? 1 : 0, a.fmt_b == kE5M2 ? 1 : 0, true, BM, BN);
     p.num_groups = a.num_groups;
     p.offsets = a.offsets;
     p.status = a.status;
@@ -517,8 +383,8 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st) {
 
     CUtensorMap ta, tb;
     const int64_t b_rows = a.num_groups ? a.N * a.num_groups : a.N;
-    if (!make_map(&ta, a.a_codes, a.M, kbytes, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&tb, a.b_codes, b_rows, kbytes, BN)) return cudaErrorInvalidValue;
+    if (!tmap::codes_2d(&ta, a.a_codes, a.M, kbytes, BM)) return cudaErrorInvalidValue;
+    if (!tmap::codes_2d(&tb, a.b_codes, b_rows, kbytes, BN)) return cudaErrorInvalidValue;
     int grid = a.num_sms;
     if (a.num_groups == 0 && p.total_tiles < grid) grid = p.total_tiles;
     if (grid < 1) grid = 1;

@@ -1,0 +1,353 @@
+// Dense block-scaled GEMM on a CTA pair (tcgen05 cta_group::2), sm_103a.
+//
+// C[M,N] = A[M,K] * B[N,K]^T with per-block scales and FP32 accumulation
+// ("Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
+// section 2, "Calculo Intenso": the heavy GEMMs run on the native low-
+// precision tensor cores; "FP8 Training Infrastructure", section "MXFP8 e
+// NVFP4 do Blackwell": hardware block scaling).
+//
+// Two CTAs of a cluster (one per SM of a TPC) compute one 256 x 256 output
+// tile with M=256 MMAs issued by the even CTA.  Each CTA stages only its
+// own 128 rows of A and its own 128 rows of B per K step, so a CTA holds
+// 32 KB of operands per stage (a 1-CTA 128 x 256 tile needs 48 KB) and the
+// ring is 6 stages deep (5 for NVFP4) -- enough in-flight data to cover the
+// load round trip.  Each CTA also keeps the full 256-row B scale tile so
+// its tensor memory holds the scales its half of the MMA reads.
+//
+// Roles (both CTAs, 10 warps each):
+//   warp 0      TMA producer: own A / B halves and scale atoms; completion is
+//               signalled on the even CTA's stage barrier (cta_group::2 TMA)
+//   warp 1      TMEM owner (both CTAs); the even CTA's lane 0 issues the
+//               scale copies (tcgen05.cp) and MMAs and multicasts commits
+//   warps 2-9   epilogue on each CTA's own 128 accumulator rows
+// Every wait is bounded; a timed-out CTA records the status and exits after
+// its in-flight work drains.
+#include <cuda.h>
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+#include "epilogue.cuh"
+#include "tmap.h"
+
+namespace bsq {
+namespace {
+
+constexpr int BN = 256;              // output columns per pair
+constexpr int BKB = 128;             // K bytes per stage
+constexpr int HALF = 128 * BKB;      // 16 KB: one CTA's 128 rows of A (or B)
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 256;
+constexpr int kRasterGroup = 8;      // 256-row m-tiles per raster group
+
+template <bool FP4>
+struct Cfg2 {
+    static constexpr int STAGES = FP4 ? 5 : 6;
+    static constexpr int SF_ATOMS = FP4 ? 4 : 1;
+    static constexpr int SFA_BYTES = SF_ATOMS * 512;
+    static constexpr int SFB_BYTES = 2 * SF_ATOMS * 512;
+    static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
+    static constexpr uint32_t SF_COLS = FP4 ? 48 : 12;
+    static constexpr uint32_t CTA_TX = 2 * HALF + SF_STAGE;     // bytes one CTA loads per stage
+    static constexpr int SMEM = 1024 + STAGES * (2 * HALF + SF_STAGE) + 256;
+};
+
+struct Params2 {
+    int32_t M, N;
+    int32_t k_stages, mma_last;
+    int32_t m_tiles, n_tiles, total_tiles;
+    void* C;
+    int64_t ldc;
+    int32_t out_bf16, vec_ok;
+    const float* ts_a;
+    const float* ts_b;
+    uint32_t idesc;
+    unsigned* status;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ void tile_mn(const Params2& p, int t, int& mt, int& nt) {
+    const int per_group = kRasterGroup * p.n_tiles;
+    const int g = t / per_group;
+    const int first_m = g * kRasterGroup;
+    const int gm = min(kRasterGroup, p.m_tiles - first_m);
+    const int local = t - g * per_group;
+    mt = first_m + local % gm;
+    nt = local / gm;
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) {
+    }
+}
+
+template <bool FP4>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
+             const __grid_constant__ Params2 p) {
+    using CF = Cfg2<FP4>;
+    constexpr int S = CF::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smA = base;
+    uint8_t* smB = base + S * HALF;
+    uint8_t* smSF = smB + S * HALF;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smSF + S * CF::SF_STAGE);
+    // bars: full[S], empty[S], tfull, tempty, drain
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = tc::cluster_rank();
+    const bool leader = rank == 0;
+    const uint32_t full0 = tc::smem_u32(bars), empty0 = tc::smem_u32(bars + S);
+    const uint32_t tfull = tc::smem_u32(bars + 2 * S), tempty = tc::smem_u32(bars + 2 * S + 1);
+    const uint32_t drain = tc::smem_u32(bars + 2 * S + 2);
+    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < S; s++) {
+            tc::mbar_init(full0 + 8 * s, 1);
+            tc::mbar_init(empty0 + 8 * s, 1);
+        }
+        tc::mbar_init(tfull, 1);
+        tc::mbar_init(tempty, 2 * kEpiWarps);
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tc::prefetch_tmap(&tmA);
+        tc::prefetch_tmap(&tmB);
+        tc::prefetch_tmap(&tmSFA);
+        tc::prefetch_tmap(&tmSFB);
+    }
+    if (warp == 1) tc::tmem_alloc<2>(tc::smem_u32(tmem_slot), kTmemCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::cluster_sync();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool aborted = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint32_t full_c0 = tc::mapa(full0, 0);       // even CTA's stage barriers
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cid; t < p.total_tiles && ok; t += ncl) {
+                int mt, nt;
+                tile_mn(p, t, mt, nt);
+                const int arow = mt * 256 + (int)rank * 128, brow = nt * BN + (int)rank * 128;
+                for (int kb = 0; kb < p.k_stages; kb++) {
+                    if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_c0 + 8 * stage;
+                    if (leader) tc::mbar_expect_tx(full0 + 8 * stage, 2 * CF::CTA_TX);
+                    uint8_t* sf = smSF + stage * CF::SF_STAGE;
+                    tc::tma_load_2d_pair(tc::smem_u32(smA + stage * HALF), &tmA, kb * BKB, arow, fb);
+                    tc::tma_load_2d_pair(tc::smem_u32(smB + stage * HALF), &tmB, kb * BKB, brow, fb);
+                    tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, mt * 2 + (int)rank, fb);
+                    tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS, nt * 2, fb);
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            aborted = !ok;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        // The tcgen05 instruction queue is about one MMA deep, so the issuing
+        // thread runs in lockstep with the tensor pipe and any bookkeeping
+        // between two MMAs idles the pipe.  The per-step bookkeeping (test of
+        // the next stage's barrier, the next stage's scale copies, the commit
+        // freeing this stage) is therefore spread between the four MMAs of
+        // the step, and descriptors advance by plain additions.
+        if (lane == 0 && leader) {
+            constexpr uint32_t A_STEP = HALF >> 4;                  // descriptor address units per stage
+            constexpr uint32_t SF_STEP = CF::SF_STAGE >> 4;
+            const uint64_t ad_base = tc::desc_sw128(tc::smem_u32(smA));
+            const uint64_t bd_base = tc::desc_sw128(tc::smem_u32(smB));
+            const uint64_t sfd_base = tc::desc_sf(tc::smem_u32(smSF));
+            const uint32_t sf_t0 = tmem + kSfCol0;
+            // scale copies of stage `st`, part `part` of 3 (spread over the MMAs)
+            auto issue_cp = [&](int st, int part) {
+                const uint64_t sd = sfd_base + (uint64_t)(st * SF_STEP);
+                const uint32_t sfa_t = sf_t0 + st * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
+                if (FP4) {
+                    // 12 atoms: 4 per part (SFA atom a, SFB atoms (a, rt)) for a = part, part+... spread
+#pragma unroll
+                    for (int a = 0; a < 4; a++) {
+                        const int idx = part * 4 + a;                // 0..11
+                        if (idx < 4) tc::cp_sf<2>(sfa_t + 4 * idx, sd + 32 * idx);
+                        else {
+                            const int j = idx - 4, aa = j >> 1, rt = j & 1;
+                            tc::cp_sf<2>(sfb_t + 8 * aa + 4 * rt, sd + ((CF::SFA_BYTES + (rt * 4 + aa) * 512) >> 4));
+                        }
+                    }
+                } else {
+                    if (part == 0) tc::cp_sf<2>(sfa_t, sd);
+                    else tc::cp_sf<2>(sfb_t + 4 * (part - 1), sd + ((CF::SFA_BYTES + (part - 1) * 512) >> 4));
+                }
+            };
+            int stage = 0;
+            uint32_t phase = 0;
+            int iter = 0;
+            bool ok = true, any = false;
+            if (cid < p.total_tiles) {
+                ok = tc::mbar_wait(full0, 0, abort_flag, p.status, p.timeout_ns);
+                if (ok) {
+                    tc::fence_after();
+                    issue_cp(0, 0); issue_cp(0, 1); issue_cp(0, 2);
+                }
+            }
+            for (int t = cid; t < p.total_tiles && ok; t += ncl, ++iter) {
+                if (!tc::mbar_wait<true>(tempty, (iter & 1) ^ 1, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+                tc::fence_after();
+                const bool more_tiles = t + ncl < p.total_tiles;
+                for (int kb = 0; kb < p.k_stages; kb++) {
+                    const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
+                    const uint64_t ad = ad_base + (uint64_t)(stage * A_STEP), bd = bd_base + (uint64_t)(stage * A_STEP);
+                    const int nk = kb == p.k_stages - 1 ? p.mma_last : 4;
+                    int nstage = stage + 1;
+                    uint32_t nphase = phase;
+                    if (nstage == S) { nstage = 0; nphase ^= 1; }
+                    const bool has_next = kb + 1 < p.k_stages || more_tiles;
+                    bool ready = false;
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        if (k < nk) {
+                            // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
+                            if (FP4)
+                                tc::mma<2, true>(tmem, ad + 2 * k, bd + 2 * k, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k,
+                                                 (kb | k) != 0);
+                            else
+                                tc::mma<2, false>(tmem, ad + 2 * k, bd + 2 * k,
+                                                  p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa_t, sfb_t,
+                                                  (kb | k) != 0);
+                        }
+                        if (!has_next) continue;
+                        if (k == 0) {
+                            ready = tc::mbar_test(full0 + 8 * nstage, nphase);
+                        } else {
+                            if (!ready) {
+                                ready = tc::mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status, p.timeout_ns);
+                                if (!ready) { ok = false; break; }
+                            }
+                            if (k == 1) tc::fence_after();
+                            issue_cp(nstage, k - 1);
+                        }
+                    }
+                    any = true;
+                    tc::commit<2>(empty0 + 8 * stage, 3);
+                    if (kb == p.k_stages - 1) tc::commit<2>(tfull, 3);
+                    stage = nstage;
+                    phase = nphase;
+                    if (!ok) break;
+                }
+            }
+            if (!ok && any) {
+                tc::commit<2>(drain, 1);
+                volatile int no_abort = 0;
+                tc::mbar_wait(drain, 0, &no_abort, nullptr, 100000000ull);
+            }
+            aborted = !ok;
+        }
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const uint32_t tempty_c0 = tc::mapa(tempty, 0);
+        float alpha = 1.0f;
+        if (FP4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+        int iter = 0;
+        for (int t = cid; t < p.total_tiles; t += ncl, ++iter) {
+            int mt, nt;
+            tile_mn(p, t, mt, nt);
+            if (!tc::mbar_wait(tfull, iter & 1, abort_flag, p.status, p.timeout_ns)) { aborted = true; break; }
+            tc::fence_after();
+            uint32_t r[4][32];
+            const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
+            BSQ_TMEM_LD32(r[0], ta);
+            BSQ_TMEM_LD32(r[1], ta + 32);
+            BSQ_TMEM_LD32(r[2], ta + 64);
+            BSQ_TMEM_LD32(r[3], ta + 96);
+            tc::tmem_wait_ld();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive_cluster(tempty_c0);
+            const int row = mt * 256 + (int)rank * 128 + q * 32 + lane;
+            const int col0 = nt * BN + h * 128;
+            if (row < p.M && col0 < p.N) store_row128(r, p.C, p.ldc, row, col0, p.N, p.out_bf16, p.vec_ok, alpha);
+        }
+    }
+
+    // a CTA that gave up lets copies still in flight into its shared memory land
+    if (aborted) spin_ns(200000);
+    tc::fence_before();
+    __syncthreads();
+    tc::cluster_sync();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc<2>(tmem, kTmemCols);
+    }
+}
+
+template <bool FP4>
+cudaError_t launch2(const Params2& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
+                    const CUtensorMap& tsb, int grid, cudaStream_t st) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(gemm2_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<FP4>::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    gemm2_kernel<FP4><<<grid, kThreads, Cfg2<FP4>::SMEM, st>>>(ta, tb, tsa, tsb, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Dense GEMM on CTA pairs; grouped GEMMs use the 1-CTA kernel (run_gemm).
+cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
+    const bool fp4 = a.fmt_a == kNVFP4;
+    const int64_t kbytes = fp4 ? a.K / 2 : a.K;
+    const int64_t S = a.K / (fp4 ? 16 : 32);
+    const int64_t n_atoms = (S + 3) / 4;
+    Params2 p{};
+    p.M = (int32_t)a.M;
+    p.N = (int32_t)a.N;
+    p.k_stages = (int32_t)((kbytes + BKB - 1) / BKB);
+    p.mma_last = (int32_t)((kbytes - (int64_t)(p.k_stages - 1) * BKB + 31) / 32);
+    p.m_tiles = (int32_t)((a.M + 255) / 256);
+    p.n_tiles = (int32_t)((a.N + BN - 1) / BN);
+    p.total_tiles = p.m_tiles * p.n_tiles;
+    p.C = a.C;
+    p.ldc = a.N;
+    p.out_bf16 = a.out_bf16;
+    const int esz = a.out_bf16 ? 2 : 4;
+    p.vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && ((a.N * esz) % 16 == 0);
+    p.ts_a = a.ts_a;
+    p.ts_b = a.ts_b;
+    p.idesc = fp4 ? make_idesc(1, 1, false, 256, BN)
+                  : make_idesc(a.fmt_a == kE5M2 ? 1 : 0, a.fmt_b == kE5M2 ? 1 : 0, true, 256, BN);
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+
+    const int sf_atoms = fp4 ? 4 : 1;
+    CUtensorMap ta, tb, tsa, tsb;
+    if (!tmap::codes_2d(&ta, a.a_codes, a.M, kbytes, 128)) return cudaErrorInvalidValue;
+    if (!tmap::codes_2d(&tb, a.b_codes, a.N, kbytes, 128)) return cudaErrorInvalidValue;
+    if (!tmap::scales_3d(&tsa, a.a_scales, (a.M + 127) / 128, n_atoms, sf_atoms, 1)) return cudaErrorInvalidValue;
+    if (!tmap::scales_3d(&tsb, a.b_scales, (a.N + 127) / 128, n_atoms, sf_atoms, 2)) return cudaErrorInvalidValue;
+    int pairs = a.num_sms / 2;
+    if (p.total_tiles < pairs) pairs = p.total_tiles;
+    if (pairs < 1) pairs = 1;
+    return fp4 ? launch2<true>(p, ta, tb, tsa, tsb, 2 * pairs, st) : launch2<false>(p, ta, tb, tsa, tsb, 2 * pairs, st);
+}
+
+}  // namespace bsq

@@ -69,9 +69,22 @@ __device__ __forceinline__ void nv_encode(const float* x, uint32_t sb, float s_t
         return;
     }
     const float d = __fmul_rn(e4m3_to_float(sb), s_t);
+    // The E2M1 code of RN(x / d) only depends on which side of the rounding
+    // midpoints {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5} (and of the binade
+    // edges) the quotient falls.  q0 = RN(x * RN(1/d)) is within about one
+    // ulp of x / d, so whenever q0 is more than two ulps away from every
+    // value with at most two significant mantissa bits (the midpoints are
+    // such values) it yields the same code; otherwise the exact IEEE
+    // division decides.
+    const float r = __frcp_rn(d);
     float v[N];
 #pragma unroll
-    for (int i = 0; i < N; i++) v[i] = __fdiv_rn(x[i], d);
+    for (int i = 0; i < N; i++) {
+        float q = __fmul_rn(x[i], r);
+        const uint32_t low = __float_as_uint(q) & 0x1FFFFFu;
+        if (low < 4u || low > 0x1FFFFBu) q = __fdiv_rn(x[i], d);
+        v[i] = q;
+    }
 #pragma unroll
     for (int i = 0; i < N / 8; i++) out[i] = pack8_fp4(v + 8 * i);
 }

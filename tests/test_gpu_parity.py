@@ -302,3 +302,25 @@ def test_gemm_rejects_bad_args(bsq):
     with pytest.raises(bsq.BsqError) as ei:
         bsq.gemm(A, Bn)
     assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("M,N,K,fmt", [(300, 520, 384, "mxfp8_e4m3"), (256, 256, 4096, "mxfp8_e5m2"),
+                                       (130, 260, 640, "nvfp4"), (513, 257, 1056, "mxfp8_e4m3")])
+def test_gemm_single_cta_tile_path(bsq, M, N, K, fmt, monkeypatch):
+    """The dense GEMM normally runs on CTA pairs (256 x 256 tiles); the
+    single-CTA 128 x 256 kernel (the grouped GEMM's) must agree as well."""
+    monkeypatch.setenv("BSQ_GEMM_1CTA", "1")
+    xa = inputs.loguniform_grad_bf16((M, K), 3) if fmt == "mxfp8_e5m2" else inputs.outlier_activations_bf16((M, K), 3)
+    xb = inputs.normal_bf16((N, K), 4, std=0.02)
+    fb = "mxfp8_e4m3" if fmt == "mxfp8_e5m2" else fmt
+    _check_gemm(bsq, xa, fmt, xb, fb, "f32")
+
+
+def test_gemm_pair_tile_tails(bsq):
+    """Tails of the 256 x 256 pair tile: the odd CTA's rows fully past M,
+    the second B half past N, and a K tail inside the last stage."""
+    for M, N, K in [(129, 129, 160), (100, 384, 4128), (384, 100, 96)]:
+        xa = inputs.outlier_activations_bf16((M, K), 8)
+        xb = inputs.normal_bf16((N, K), 9, std=0.02)
+        _check_gemm(bsq, xa, "mxfp8_e4m3", xb, "mxfp8_e4m3", "f32")
+        _check_gemm(bsq, xa, "nvfp4", xb, "nvfp4", "bf16")
