@@ -401,7 +401,7 @@ def main():
     ach = step.ops[jr][5] / (op_ms[jr] * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
                 "frac": round(ach / pk["fp8_tflops"], 4), "traffic": None,
-                "kernel": "gemm_kernel<fp8> (tcgen05 mxf8f6f4 block_scale), launch: " + step.ops[jr][0],
+                "kernel": "gemm2_kernel<fp8> (CTA pair, tcgen05 mxf8f6f4 block_scale), launch: " + step.ops[jr][0],
                 "flops_per_launch": step.ops[jr][5], "ms_per_launch": round(op_ms[jr], 4),
                 "peak_note": f"2x {pk['source']} bf16 burst {pk['bf16_tflops']} TFLOP/s (FP8 = 2x BF16 rate)",
                 "frac_vs_sustained": round(ach / (2 * pk["bf16_tflops_sustained"]), 4),
@@ -472,15 +472,15 @@ def _profile_traffic():
     only if that summary was taken on the current GEMM source."""
     import hashlib
     try:
-        src = open(os.path.join(ROOT, "block_scaled_precision_03_gb300", "csrc", "gemm.cu"), "rb").read()
+        src = open(os.path.join(ROOT, "block_scaled_precision_03_gb300", "csrc", "gemm2.cu"), "rb").read()
         sha = hashlib.sha256(src).hexdigest()[:16]
         vals = {}
-        with open(os.path.join(ROOT, "profiles", "gemm_fp8_fwd_8192x14336x4096.md")) as f:
+        with open(os.path.join(ROOT, "profiles", "gemm2_fp8_fwd_8192x14336x4096.md")) as f:
             for line in f:
                 if ":" in line and line.startswith("- "):
-                    k, v = line[2:].split(":", 1)
+                    k, v = line[2:].rsplit(":", 1)
                     vals[k.strip()] = v.strip().strip("`")
-        if vals.get("gemm.cu sha256[:16]") != sha:
+        if vals.get("gemm2.cu sha256[:16]") != sha:
             return None
         return float(vals["dram bytes per full launch"])
     except Exception:

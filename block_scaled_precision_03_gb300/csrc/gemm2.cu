@@ -10,8 +10,10 @@
 // tile with M=256 MMAs issued by the even CTA.  Each CTA stages only its
 // own 128 rows of A and its own 128 rows of B per K step, so a CTA holds
 // 32 KB of operands per stage (a 1-CTA 128 x 256 tile needs 48 KB) and the
-// ring is 6 stages deep (5 for NVFP4) -- enough in-flight data to cover the
-// load round trip.  Each CTA also keeps the full 256-row B scale tile so
+// ring holds 3 stages of 256 K-bytes (5 of 128 for NVFP4).  The tcgen05
+// instruction queue is about one MMA deep, so the issuing thread runs in
+// lockstep with the tensor pipe; every barrier handshake costs pipe time,
+// and larger stages (8 MMAs per handshake) amortize it.  Each CTA also keeps the full 256-row B scale tile so
 // its tensor memory holds the scales its half of the MMA reads.
 //
 // Roles (both CTAs, 10 warps each):
@@ -43,14 +45,20 @@ constexpr int kRasterGroup = 8;      // 256-row m-tiles per raster group
 
 template <bool FP4>
 struct Cfg2 {
-    static constexpr int STAGES = FP4 ? 5 : 6;
-    static constexpr int SF_ATOMS = FP4 ? 4 : 1;
+    // KSUB 128-byte K sub-steps per stage: more MMAs per barrier handshake
+    static constexpr int KSUB = FP4 ? 1 : 2;
+    static constexpr int STAGES = FP4 ? 5 : 3;
+    static constexpr int MPS = 4 * KSUB;                  // MMAs per stage
+    static constexpr int OP_BYTES = KSUB * HALF;          // one CTA's A (or B) bytes per stage
+    static constexpr int SF_ATOMS = KSUB * (FP4 ? 4 : 1); // 512-byte scale atoms per 128 rows per stage
     static constexpr int SFA_BYTES = SF_ATOMS * 512;
     static constexpr int SFB_BYTES = 2 * SF_ATOMS * 512;
     static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
-    static constexpr uint32_t SF_COLS = FP4 ? 48 : 12;
-    static constexpr uint32_t CTA_TX = 2 * HALF + SF_STAGE;     // bytes one CTA loads per stage
-    static constexpr int SMEM = 1024 + STAGES * (2 * HALF + SF_STAGE) + 256;
+    static constexpr uint32_t SFA_COLS = 4 * SF_ATOMS;    // TMEM columns: SFA atoms, then SFB atom pairs
+    static constexpr uint32_t SF_COLS = 12 * SF_ATOMS;
+    static constexpr uint32_t CTA_TX = 2 * OP_BYTES + SF_STAGE;     // bytes one CTA loads per stage
+    static constexpr int SMEM = 1024 + STAGES * (2 * OP_BYTES + SF_STAGE) + 256;
+    static_assert(kSfCol0 + STAGES * SF_COLS <= kTmemCols, "TMEM columns");
 };
 
 struct Params2 {
@@ -93,8 +101,8 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* smA = base;
-    uint8_t* smB = base + S * HALF;
-    uint8_t* smSF = smB + S * HALF;
+    uint8_t* smB = base + S * CF::OP_BYTES;
+    uint8_t* smSF = smB + S * CF::OP_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smSF + S * CF::SF_STAGE);
     // bars: full[S], empty[S], tfull, tempty, drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 3);
@@ -150,8 +158,12 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     const uint32_t fb = full_c0 + 8 * stage;
                     if (leader) tc::mbar_expect_tx(full0 + 8 * stage, 2 * CF::CTA_TX);
                     uint8_t* sf = smSF + stage * CF::SF_STAGE;
-                    tc::tma_load_2d_pair(tc::smem_u32(smA + stage * HALF), &tmA, kb * BKB, arow, fb);
-                    tc::tma_load_2d_pair(tc::smem_u32(smB + stage * HALF), &tmB, kb * BKB, brow, fb);
+#pragma unroll
+                    for (int j = 0; j < CF::KSUB; j++) {
+                        const int kx = (kb * CF::KSUB + j) * BKB;
+                        tc::tma_load_2d_pair(tc::smem_u32(smA + stage * CF::OP_BYTES + j * HALF), &tmA, kx, arow, fb);
+                        tc::tma_load_2d_pair(tc::smem_u32(smB + stage * CF::OP_BYTES + j * HALF), &tmB, kx, brow, fb);
+                    }
                     tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, mt * 2 + (int)rank, fb);
                     tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS, nt * 2, fb);
                     if (++stage == S) { stage = 0; phase ^= 1; }
@@ -161,38 +173,28 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
-        // The tcgen05 instruction queue is about one MMA deep, so the issuing
-        // thread runs in lockstep with the tensor pipe and any bookkeeping
-        // between two MMAs idles the pipe.  The per-step bookkeeping (test of
-        // the next stage's barrier, the next stage's scale copies, the commit
-        // freeing this stage) is therefore spread between the four MMAs of
-        // the step, and descriptors advance by plain additions.
+        // The issuing thread runs in lockstep with the tensor pipe, so the
+        // per-step bookkeeping (test of the next stage's barrier, the next
+        // stage's scale copies, the commit freeing this stage) is spread
+        // between the MMAs of the step, and descriptors advance by plain
+        // additions.
         if (lane == 0 && leader) {
-            constexpr uint32_t A_STEP = HALF >> 4;                  // descriptor address units per stage
+            constexpr int MPS = CF::MPS, NCP = 3 * CF::SF_ATOMS;
+            constexpr int CHUNK = (NCP + MPS - 2) / (MPS - 1);      // copies issued after each of MMAs 1..MPS-1
+            constexpr uint32_t OP_STEP = CF::OP_BYTES >> 4, SUB_STEP = HALF >> 4;  // descriptor address units
             constexpr uint32_t SF_STEP = CF::SF_STAGE >> 4;
             const uint64_t ad_base = tc::desc_sw128(tc::smem_u32(smA));
             const uint64_t bd_base = tc::desc_sw128(tc::smem_u32(smB));
             const uint64_t sfd_base = tc::desc_sf(tc::smem_u32(smSF));
             const uint32_t sf_t0 = tmem + kSfCol0;
-            // scale copies of stage `st`, part `part` of 3 (spread over the MMAs)
-            auto issue_cp = [&](int st, int part) {
+            // scale copy c of stage st: atom c / 3, part c % 3 (A; B rows 0-127; B rows 128-255)
+            auto cp_one = [&](int st, int c) {
+                const int a = c / 3, part = c % 3;
                 const uint64_t sd = sfd_base + (uint64_t)(st * SF_STEP);
-                const uint32_t sfa_t = sf_t0 + st * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
-                if (FP4) {
-                    // 12 atoms: 4 per part (SFA atom a, SFB atoms (a, rt)) for a = part, part+... spread
-#pragma unroll
-                    for (int a = 0; a < 4; a++) {
-                        const int idx = part * 4 + a;                // 0..11
-                        if (idx < 4) tc::cp_sf<2>(sfa_t + 4 * idx, sd + 32 * idx);
-                        else {
-                            const int j = idx - 4, aa = j >> 1, rt = j & 1;
-                            tc::cp_sf<2>(sfb_t + 8 * aa + 4 * rt, sd + ((CF::SFA_BYTES + (rt * 4 + aa) * 512) >> 4));
-                        }
-                    }
-                } else {
-                    if (part == 0) tc::cp_sf<2>(sfa_t, sd);
-                    else tc::cp_sf<2>(sfb_t + 4 * (part - 1), sd + ((CF::SFA_BYTES + (part - 1) * 512) >> 4));
-                }
+                const uint32_t sfa_t = sf_t0 + st * CF::SF_COLS, sfb_t = sfa_t + CF::SFA_COLS;
+                if (part == 0) tc::cp_sf<2>(sfa_t + 4 * a, sd + 32 * a);
+                else tc::cp_sf<2>(sfb_t + 8 * a + 4 * (part - 1),
+                                  sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + a) * 512) >> 4));
             };
             int stage = 0;
             uint32_t phase = 0;
@@ -202,7 +204,8 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 ok = tc::mbar_wait(full0, 0, abort_flag, p.status, p.timeout_ns);
                 if (ok) {
                     tc::fence_after();
-                    issue_cp(0, 0); issue_cp(0, 1); issue_cp(0, 2);
+#pragma unroll
+                    for (int c = 0; c < NCP; c++) cp_one(0, c);
                 }
             }
             for (int t = cid; t < p.total_tiles && ok; t += ncl, ++iter) {
@@ -210,36 +213,38 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 tc::fence_after();
                 const bool more_tiles = t + ncl < p.total_tiles;
                 for (int kb = 0; kb < p.k_stages; kb++) {
-                    const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
-                    const uint64_t ad = ad_base + (uint64_t)(stage * A_STEP), bd = bd_base + (uint64_t)(stage * A_STEP);
-                    const int nk = kb == p.k_stages - 1 ? p.mma_last : 4;
+                    const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + CF::SFA_COLS;
+                    const uint64_t ad = ad_base + (uint64_t)(stage * OP_STEP), bd = bd_base + (uint64_t)(stage * OP_STEP);
+                    const int nk = kb == p.k_stages - 1 ? p.mma_last : MPS;
                     int nstage = stage + 1;
                     uint32_t nphase = phase;
                     if (nstage == S) { nstage = 0; nphase ^= 1; }
                     const bool has_next = kb + 1 < p.k_stages || more_tiles;
                     bool ready = false;
 #pragma unroll
-                    for (int k = 0; k < 4; k++) {
-                        if (k < nk) {
-                            // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
+                    for (int m = 0; m < MPS; m++) {
+                        if (m < nk) {
+                            const int sub = m >> 2, k = m & 3;
+                            // +32 bytes along K inside a 128-byte swizzle row = +2 in the address field
+                            const uint64_t adm = ad + sub * SUB_STEP + 2 * k, bdm = bd + sub * SUB_STEP + 2 * k;
+                            const uint32_t acc = (kb | m) != 0;
                             if (FP4)
-                                tc::mma<2, true>(tmem, ad + 2 * k, bd + 2 * k, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k,
-                                                 (kb | k) != 0);
+                                tc::mma<2, true>(tmem, adm, bdm, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
                             else
-                                tc::mma<2, false>(tmem, ad + 2 * k, bd + 2 * k,
-                                                  p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa_t, sfb_t,
-                                                  (kb | k) != 0);
+                                tc::mma<2, false>(tmem, adm, bdm, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29),
+                                                  sfa_t + 4 * sub, sfb_t + 8 * sub, acc);
                         }
                         if (!has_next) continue;
-                        if (k == 0) {
+                        if (m == 0) {
                             ready = tc::mbar_test(full0 + 8 * nstage, nphase);
                         } else {
                             if (!ready) {
                                 ready = tc::mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status, p.timeout_ns);
                                 if (!ready) { ok = false; break; }
                             }
-                            if (k == 1) tc::fence_after();
-                            issue_cp(nstage, k - 1);
+                            if (m == 1) tc::fence_after();
+#pragma unroll
+                            for (int c = (m - 1) * CHUNK; c < m * CHUNK && c < NCP; c++) cp_one(nstage, c);
                         }
                     }
                     any = true;
@@ -321,8 +326,9 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     Params2 p{};
     p.M = (int32_t)a.M;
     p.N = (int32_t)a.N;
-    p.k_stages = (int32_t)((kbytes + BKB - 1) / BKB);
-    p.mma_last = (int32_t)((kbytes - (int64_t)(p.k_stages - 1) * BKB + 31) / 32);
+    const int64_t stage_kb = (int64_t)BKB * (fp4 ? Cfg2<true>::KSUB : Cfg2<false>::KSUB);
+    p.k_stages = (int32_t)((kbytes + stage_kb - 1) / stage_kb);
+    p.mma_last = (int32_t)((kbytes - (int64_t)(p.k_stages - 1) * stage_kb + 31) / 32);
     p.m_tiles = (int32_t)((a.M + 255) / 256);
     p.n_tiles = (int32_t)((a.N + BN - 1) / BN);
     p.total_tiles = p.m_tiles * p.n_tiles;
@@ -338,7 +344,7 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
 
-    const int sf_atoms = fp4 ? 4 : 1;
+    const int sf_atoms = fp4 ? Cfg2<true>::SF_ATOMS : Cfg2<false>::SF_ATOMS;
     CUtensorMap ta, tb, tsa, tsb;
     if (!tmap::codes_2d(&ta, a.a_codes, a.M, kbytes, 128)) return cudaErrorInvalidValue;
     if (!tmap::codes_2d(&tb, a.b_codes, a.N, kbytes, 128)) return cudaErrorInvalidValue;
