@@ -52,12 +52,33 @@ __device__ __forceinline__ void mx_encode(const float* x, uint32_t sbyte, uint32
     }
 }
 
-// NVFP4 per-block scale byte from the block amax and the tensor scale.
-__device__ __forceinline__ uint32_t nv_scale_byte(uint32_t amax_bits, float s_t) {
+// NVFP4 per-block scale byte from the block amax and the tensor scale:
+// UE4M3(RNE((amax_b / 6) / s_t)) with both divisions IEEE FP32.  The E4M3
+// code only depends on which side of its rounding boundaries (values with at
+// most 5 significant bits, including the saturation point 464) the quotient
+// falls.  q0 = amax_b * RN(1/6) * RN(1/s_t) is within about 5 ulp of the
+// two-step quotient, so it decides the code unless it lies within 15 ulp of
+// a value whose low 18 mantissa bits are zero; then the exact divisions do.
+// The exact divisions are out of line so the compiler branches around them
+// instead of issuing them predicated on every lane.
+__device__ __noinline__ float nv_exact_block_q(float amax_b, float s_t) {
+    return __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_t);
+}
+__device__ __noinline__ float nv_exact_div(float x, float d) { return __fdiv_rn(x, d); }
+
+__device__ __forceinline__ uint32_t nv_scale_byte(uint32_t amax_bits, float s_t, float inv_st) {
     if (amax_bits >= 0x7F80u) return 0x7Fu;      // NaN/Inf in the block
-    float amax_b = __uint_as_float(amax_bits << 16);
-    float q = __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_t);
+    const float amax_b = __uint_as_float(amax_bits << 16);
+    float q = __fmul_rn(__fmul_rn(amax_b, 1.0f / 6.0f), inv_st);
+    const uint32_t low = __float_as_uint(q) & 0x3FFFFu;
+    if (low < 16u || low > 0x3FFEFu) q = nv_exact_block_q(amax_b, s_t);
     return cvt_e4m3x2(q, 0.0f) & 0xFFu;
+}
+
+__device__ __forceinline__ float rcp_approx(float d) {
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
 }
 
 // NVFP4: encode n values (multiple of 8) of one block with scale byte sb.
@@ -71,18 +92,18 @@ __device__ __forceinline__ void nv_encode(const float* x, uint32_t sb, float s_t
     const float d = __fmul_rn(e4m3_to_float(sb), s_t);
     // The E2M1 code of RN(x / d) only depends on which side of the rounding
     // midpoints {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5} (and of the binade
-    // edges) the quotient falls.  q0 = RN(x * RN(1/d)) is within about one
-    // ulp of x / d, so whenever q0 is more than two ulps away from every
-    // value with at most two significant mantissa bits (the midpoints are
-    // such values) it yields the same code; otherwise the exact IEEE
-    // division decides.
-    const float r = __frcp_rn(d);
+    // edges) the quotient falls.  With r within one ulp of 1/d (hardware
+    // reciprocal), q0 = RN(x * r) is within about 3 ulp of x / d, so whenever
+    // q0 is more than 15 ulps away from every value with at most two
+    // significant mantissa bits (the midpoints are such values) it yields
+    // the same code; otherwise the exact IEEE division decides.
+    const float r = rcp_approx(d);
     float v[N];
 #pragma unroll
     for (int i = 0; i < N; i++) {
         float q = __fmul_rn(x[i], r);
         const uint32_t low = __float_as_uint(q) & 0x1FFFFFu;
-        if (low < 4u || low > 0x1FFFFBu) q = __fdiv_rn(x[i], d);
+        if (low < 16u || low > 0x1FFFEFu) q = nv_exact_div(x[i], d);
         v[i] = q;
     }
 #pragma unroll
@@ -127,15 +148,28 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
     const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
     const bool vec_sf = (blocks_per_row & 3u) == 0;
-    float s_t = 1.0f;
-    if (FMT == kNVFP4) s_t = nv_tensor_scale(nv_amax);
+    float s_t = 1.0f, inv_st = 1.0f;
+    if (FMT == kNVFP4) {
+        s_t = nv_tensor_scale(nv_amax);
+        inv_st = __frcp_rn(s_t);
+    }
 
-    for (int64_t base = warp * 32 * kRowUnroll; base < nchunks; base += nwarps * 32 * kRowUnroll) {
-        uint4 w[kRowUnroll];
+    // software pipeline: the loads of the next iteration are in flight while
+    // the current chunks are encoded
+    const int64_t step = nwarps * 32 * kRowUnroll;
+    uint4 w[kRowUnroll];
+    int64_t base = warp * 32 * kRowUnroll;
+#pragma unroll
+    for (int u = 0; u < kRowUnroll; u++) {
+        const int64_t c = base + u * 32 + lane;
+        w[u] = c < nchunks ? ld_stream(src + c) : make_uint4(0, 0, 0, 0);
+    }
+    for (; base < nchunks; base += step) {
+        uint4 wn[kRowUnroll];
 #pragma unroll
         for (int u = 0; u < kRowUnroll; u++) {
-            int64_t c = base + u * 32 + lane;
-            w[u] = c < nchunks ? ld_stream(src + c) : make_uint4(0, 0, 0, 0);
+            const int64_t c = base + step + u * 32 + lane;
+            wn[u] = c < nchunks ? ld_stream(src + c) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kRowUnroll; u++) {
@@ -143,7 +177,7 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
             uint32_t am = absmax8(w[u]);
             am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
             if (LPB == 4) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t) : mx_scale_byte<FMT>(am);
+            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t, inv_st) : mx_scale_byte<FMT>(am);
             float f[8];
             unpack8(w[u], f);
             uint32_t out[2];
@@ -170,6 +204,8 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
                 scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb;
             }
         }
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; u++) w[u] = wn[u];
     }
 }
 
@@ -195,8 +231,11 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
     const int tid = threadIdx.x;
     const int64_t r0 = (int64_t)blockIdx.y * kTile;
     const int64_t c0 = (int64_t)blockIdx.x * kTile;
-    float s_t = 1.0f;
-    if (FMT == kNVFP4) s_t = nv_tensor_scale(nv_amax);
+    float s_t = 1.0f, inv_st = 1.0f;
+    if (FMT == kNVFP4) {
+        s_t = nv_tensor_scale(nv_amax);
+        inv_st = __frcp_rn(s_t);
+    }
 
     // load: 128 rows x 16 chunks of 8 bf16
 #pragma unroll
@@ -230,7 +269,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
                 float f[BLK];
 #pragma unroll
                 for (int r = 0; r < BLK; r++) f[r] = half ? bf16hi(w[r]) : bf16lo(w[r]);
-                uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t) : mx_scale_byte<FMT>(am);
+                uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t, inv_st) : mx_scale_byte<FMT>(am);
                 uint32_t out[BLK / 4];
                 if (FMT == kNVFP4) nv_encode<BLK>(f, sb, s_t, out);
                 else mx_encode<FMT, BLK>(f, sb, out);
@@ -265,7 +304,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
                 am = max(am, absmax8(v));
                 unpack8(v, f + 8 * q);
             }
-            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t) : mx_scale_byte<FMT>(am);
+            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t, inv_st) : mx_scale_byte<FMT>(am);
             uint32_t out[BLK / 4];
             if (FMT == kNVFP4) nv_encode<BLK>(f, sb, s_t, out);
             else mx_encode<FMT, BLK>(f, sb, out);
