@@ -294,6 +294,17 @@ def dist_setup(args):
     return rank, world, local
 
 
+def reduce_max(x: float, device="cpu") -> float:
+    """Max of x over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands, timed on the host cores: each step is the
     bounded forward slice of the same workload."""
@@ -362,11 +373,7 @@ def main():
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = reduce_max(start.elapsed_time(stop), "cuda")
     ms_step = elapsed_ms / args.steps
     value = world * step.flops / (ms_step * 1e-3) / 1e12
 
@@ -399,14 +406,18 @@ def main():
     jr = fwd if fwd is not None else next((j for j, op in enumerate(step.ops) if op[2] == "gemm8"),
                                           next((j for j, op in enumerate(step.ops) if op[5]), 0))
     ach = step.ops[jr][5] / (op_ms[jr] * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
-                "frac": round(ach / pk["fp8_tflops"], 4), "traffic": None,
-                "kernel": "gemm2_kernel<fp8> (CTA pair, tcgen05 mxf8f6f4 block_scale), launch: " + step.ops[jr][0],
+    fp4_gemm = step.ops[jr][2] == "gemm4"
+    rpeak = pk["fp4_tflops"] if fp4_gemm else pk["fp8_tflops"]
+    roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": rpeak, "unit": "TFLOP/s",
+                "frac": round(ach / rpeak, 4), "traffic": None,
+                "kernel": ("gemm2_kernel<nvfp4> (CTA pair, tcgen05 mxf4nvf4 block_scale)" if fp4_gemm else
+                           "gemm2_kernel<fp8> (CTA pair, tcgen05 mxf8f6f4 block_scale)") + ", launch: " + step.ops[jr][0],
                 "flops_per_launch": step.ops[jr][5], "ms_per_launch": round(op_ms[jr], 4),
-                "peak_note": f"2x {pk['source']} bf16 burst {pk['bf16_tflops']} TFLOP/s (FP8 = 2x BF16 rate)",
-                "frac_vs_sustained": round(ach / (2 * pk["bf16_tflops_sustained"]), 4),
+                "peak_note": f"{'4' if fp4_gemm else '2'}x {pk['source']} bf16 burst {pk['bf16_tflops']} TFLOP/s "
+                             f"(nominal FP8 = 2x, FP4 = 4x the BF16 rate)",
+                "frac_vs_sustained": round(ach / ((4 if fp4_gemm else 2) * pk["bf16_tflops_sustained"]), 4),
                 "all_fp8_gemm_launches_tflops": round(g8, 1)}
-    traffic = _profile_traffic()
+    traffic = None if fp4_gemm else _profile_traffic()
     if traffic is not None:
         roofline["traffic"] = traffic
 
@@ -426,11 +437,7 @@ def main():
         s1.record()
         torch.cuda.synchronize()
         barrier()
-        e_ms = s0.elapsed_time(s1) / ke
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = reduce_max(s0.elapsed_time(s1) / ke, "cuda")
         e2e = {"value": round(world * step.flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(e_ms, 3), "steps": ke,
                "h2d_bytes_per_step": step.h2d, "d2h_bytes_per_step": step.d2h}
