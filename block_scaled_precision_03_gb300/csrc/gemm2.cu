@@ -221,6 +221,31 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     if (nstage == S) { nstage = 0; nphase ^= 1; }
                     const bool has_next = kb + 1 < p.k_stages || more_tiles;
                     bool ready = false;
+                    if (nk == MPS && has_next) {
+                        // common step: no tail, a next stage exists -- straight-line issue
+#pragma unroll
+                        for (int m = 0; m < MPS; m++) {
+                            const int sub = m >> 2, k = m & 3;
+                            const uint64_t adm = ad + sub * SUB_STEP + 2 * k, bdm = bd + sub * SUB_STEP + 2 * k;
+                            const uint32_t acc = m == 0 ? (uint32_t)(kb != 0) : 1u;
+                            if (FP4)
+                                tc::mma<2, true>(tmem, adm, bdm, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
+                            else
+                                tc::mma<2, false>(tmem, adm, bdm, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29),
+                                                  sfa_t + 4 * sub, sfb_t + 8 * sub, acc);
+                            if (m == 0) {
+                                ready = tc::mbar_test(full0 + 8 * nstage, nphase);
+                            } else {
+                                if (m == 1) {
+                                    if (!ready && !tc::mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status,
+                                                                 p.timeout_ns)) { ok = false; break; }
+                                    tc::fence_after();
+                                }
+#pragma unroll
+                                for (int c = (m - 1) * CHUNK; c < m * CHUNK && c < NCP; c++) cp_one(nstage, c);
+                            }
+                        }
+                    } else
 #pragma unroll
                     for (int m = 0; m < MPS; m++) {
                         if (m < nk) {

@@ -99,12 +99,16 @@ __device__ __forceinline__ void nv_encode(const float* x, uint32_t sb, float s_t
     // the same code; otherwise the exact IEEE division decides.
     const float r = rcp_approx(d);
     float v[N];
+    bool near = false;          // any quotient within 15 ulp of a 2-bit value
 #pragma unroll
     for (int i = 0; i < N; i++) {
-        float q = __fmul_rn(x[i], r);
-        const uint32_t low = __float_as_uint(q) & 0x1FFFFFu;
-        if (low < 16u || low > 0x1FFFEFu) q = nv_exact_div(x[i], d);
-        v[i] = q;
+        v[i] = __fmul_rn(x[i], r);
+        near |= ((__float_as_uint(v[i]) & 0x1FFFFFu) - 16u) > (0x1FFFEFu - 16u);
+    }
+    if (near) {
+#pragma unroll
+        for (int i = 0; i < N; i++)
+            if (((__float_as_uint(v[i]) & 0x1FFFFFu) - 16u) > (0x1FFFEFu - 16u)) v[i] = __fdiv_rn(x[i], d);
     }
 #pragma unroll
     for (int i = 0; i < N / 8; i++) out[i] = pack8_fp4(v + 8 * i);
@@ -127,8 +131,13 @@ __device__ __forceinline__ void unpack8(const uint4& w, float* f) {
     f[4] = bf16lo(w.z); f[5] = bf16hi(w.z); f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
 }
 
+// largest |x| bit pattern of 8 bf16 values (packed 16-bit max on the
+// sign-cleared halves; for non-negative finite values and NaN/Inf the
+// integer order is the order the block scale needs)
 __device__ __forceinline__ uint32_t absmax8(const uint4& w) {
-    return absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(0u, w.x), w.y), w.z), w.w);
+    const uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                                __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+    return max(m & 0xFFFFu, m >> 16);
 }
 
 // ---------------------------------------------------------------------------
@@ -206,6 +215,74 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
         }
 #pragma unroll
         for (int u = 0; u < kRowUnroll; u++) w[u] = wn[u];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 row-wise kernel: one thread = one 16-element block (two 16-byte
+// loads), so the per-block scale work is done once and needs no shuffle.
+// ---------------------------------------------------------------------------
+constexpr int kNvUnroll = 2;
+
+__device__ __forceinline__ uint4 ld_cached(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__global__ void __launch_bounds__(kRowThreads)
+quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row, int64_t s_tiles,
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const unsigned* __restrict__ nv_amax) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
+    const bool vec_sf = (blocks_per_row & 3u) == 0;
+    const float s_t = nv_tensor_scale(nv_amax);
+    const float inv_st = __frcp_rn(s_t);
+    const int64_t step = nwarps * 32 * kNvUnroll;
+    uint4 w[kNvUnroll][2];
+    int64_t base = warp * 32 * kNvUnroll;
+#pragma unroll
+    for (int u = 0; u < kNvUnroll; u++) {
+        const int64_t b = base + u * 32 + lane;
+        w[u][0] = b < nblocks ? ld_cached(src + 2 * b) : make_uint4(0, 0, 0, 0);
+        w[u][1] = b < nblocks ? ld_cached(src + 2 * b + 1) : make_uint4(0, 0, 0, 0);
+    }
+    for (; base < nblocks; base += step) {
+        uint4 wn[kNvUnroll][2];
+#pragma unroll
+        for (int u = 0; u < kNvUnroll; u++) {
+            const int64_t b = base + step + u * 32 + lane;
+            wn[u][0] = b < nblocks ? ld_cached(src + 2 * b) : make_uint4(0, 0, 0, 0);
+            wn[u][1] = b < nblocks ? ld_cached(src + 2 * b + 1) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kNvUnroll; u++) {
+            const int64_t b = base + u * 32 + lane;
+            const uint32_t am = max(absmax8(w[u][0]), absmax8(w[u][1]));
+            const uint32_t sb = nv_scale_byte(am, s_t, inv_st);
+            float f[16];
+            unpack8(w[u][0], f);
+            unpack8(w[u][1], f + 8);
+            uint32_t out[2];
+            nv_encode<16>(f, sb, s_t, out);
+            if (b < nblocks) reinterpret_cast<uint2*>(codes)[b] = make_uint2(out[0], out[1]);
+            const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
+            const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+            const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
+            if (b < nblocks) {
+                const uint32_t r = (uint32_t)(b / blocks_per_row), j = (uint32_t)(b - (int64_t)r * blocks_per_row);
+                if (vec_sf) {
+                    if ((lane & 3) == 0)
+                        *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) =
+                            sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+                } else {
+                    scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kNvUnroll; u++) { w[u][0] = wn[u][0]; w[u][1] = wn[u][1]; }
     }
 }
 
@@ -463,7 +540,18 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
         case kE4M3: e = launch_rows<kE4M3>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
         case kE5M2: e = launch_rows<kE5M2>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
         case kMXFP4: e = launch_rows<kMXFP4>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
-        default: e = launch_rows<kNVFP4>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
+        default: {
+            const int64_t nblocks = R * C / 16;
+            const int64_t per_cta = (int64_t)kRowThreads * kNvUnroll;
+            int64_t grid = (nblocks + per_cta - 1) / per_cta;
+            if (grid > (int64_t)a.num_sms * 8) grid = (int64_t)a.num_sms * 8;
+            if (grid < 1) grid = 1;
+            const int64_t S = C / 16;
+            quantize_rows_nv_kernel<<<(unsigned)grid, kRowThreads, 0, st>>>(
+                reinterpret_cast<const uint4*>(a.src), nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, amax);
+            e = cudaGetLastError();
+            break;
+        }
         }
     } else {
         switch (a.fmt) {
