@@ -221,20 +221,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        // Software-pipelined: the scale copies of step i+1 are issued right
-        // after the MMAs of step i (steps run across tile boundaries).
+        // The issuing thread runs in lockstep with the tensor pipe (the
+        // tcgen05 queue holds about one MMA), so the next stage's barrier test
+        // and scale copies are interleaved between this stage's MMAs, and the
+        // common step (full stage, a next stage exists) is branch-free.
         if (lane == 0) {
-            auto issue_cp = [&](int st) {
-                const uint32_t sfa_t = tmem + kSfCol0 + st * CF::SF_COLS;
-                const uint32_t sfb_t = sfa_t + (FP4 ? 16 : 4);
-                const uint32_t sf_s = smem_u32(smSF + st * CF::SF_STAGE);
-#pragma unroll
-                for (int a = 0; a < CF::SF_ATOMS; a++) {
-                    cp_sf<1>(sfa_t + 4 * a, desc_sf(sf_s + a * 512));
-#pragma unroll
-                    for (int rt = 0; rt < 2; rt++)
-                        cp_sf<1>(sfb_t + 8 * a + 4 * rt, desc_sf(sf_s + CF::SFA_BYTES + (rt * CF::SF_ATOMS + a) * 512));
-                }
+            constexpr int MPS = 4, NCP = 3 * CF::SF_ATOMS;
+            constexpr int CHUNK = (NCP + MPS - 2) / (MPS - 1);
+            const uint64_t ad_base = desc_sw128(smem_u32(smA));
+            const uint64_t bd_base = desc_sw128(smem_u32(smB));
+            const uint64_t sfd_base = desc_sf(smem_u32(smSF));
+            const uint32_t sf_t0 = tmem + kSfCol0;
+            // scale copy c of stage st: atom c / 3, part c % 3 (A; B rows 0-127; B rows 128-255)
+            auto cp_one = [&](int st, int c) {
+                const int at = c / 3, part = c % 3;
+                const uint64_t sd = sfd_base + (uint64_t)((st * CF::SF_STAGE) >> 4);
+                const uint32_t sfa_t = sf_t0 + st * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
+                if (part == 0) cp_sf<1>(sfa_t + 4 * at, sd + 32 * at);
+                else cp_sf<1>(sfb_t + 8 * at + 4 * (part - 1),
+                              sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + at) * 512) >> 4));
+            };
+            auto issue = [&](int st, int m, uint32_t acc) {
+                const uint32_t sfa_t = sf_t0 + st * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
+                // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
+                const uint64_t ad = ad_base + (uint64_t)((st * A_BYTES) >> 4) + 2 * m;
+                const uint64_t bd = bd_base + (uint64_t)((st * B_BYTES) >> 4) + 2 * m;
+                if (FP4) mma<1, true>(tmem, ad, bd, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
+                else mma<1, false>(tmem, ad, bd, p.idesc | ((uint32_t)m << 4) | ((uint32_t)m << 29), sfa_t, sfb_t, acc);
             };
             int stage = 0;
             uint32_t phase = 0;
@@ -244,7 +257,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 ok = mbar_wait(full0, 0, abort_flag, p.status, p.timeout_ns);
                 if (ok) {
                     fence_after();
-                    issue_cp(0);
+#pragma unroll
+                    for (int c = 0; c < NCP; c++) cp_one(0, c);
                 }
             }
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++iter) {
@@ -252,32 +266,45 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 fence_after();
                 const bool more_tiles = t + (int)gridDim.x < total;
                 for (int kb = 0; kb < p.k_stages; kb++) {
-                    const uint32_t sfa_t = tmem + kSfCol0 + stage * CF::SF_COLS;
-                    const uint32_t sfb_t = sfa_t + (FP4 ? 16 : 4);
-                    const uint64_t ad0 = desc_sw128(smem_u32(smA + stage * A_BYTES));
-                    const uint64_t bd0 = desc_sw128(smem_u32(smB + stage * B_BYTES));
-                    const int nk = kb == p.k_stages - 1 ? p.mma_last : 4;
-                    for (int k = 0; k < nk; k++) {
-                        // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
-                        const uint64_t ad = ad0 + 2 * k, bd = bd0 + 2 * k;
-                        if (FP4)
-                            mma<1, true>(tmem, ad, bd, p.idesc, sfa_t + 4 * k, sfb_t + 8 * k, (kb | k) != 0);
-                        else
-                            mma<1, false>(tmem, ad, bd, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sfa_t, sfb_t,
-                                          (kb | k) != 0);
-                    }
-                    any = true;
+                    const int nk = kb == p.k_stages - 1 ? p.mma_last : MPS;
                     int nstage = stage + 1;
                     uint32_t nphase = phase;
                     if (nstage == STAGES) { nstage = 0; nphase ^= 1; }
-                    if (kb + 1 < p.k_stages || more_tiles) {
-                        if (mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status, p.timeout_ns)) {
-                            fence_after();
-                            issue_cp(nstage);
-                        } else {
-                            ok = false;
+                    const bool has_next = kb + 1 < p.k_stages || more_tiles;
+                    bool ready = false;
+                    if (nk == MPS && has_next) {
+#pragma unroll
+                        for (int m = 0; m < MPS; m++) {
+                            issue(stage, m, m == 0 ? (uint32_t)(kb != 0) : 1u);
+                            if (m == 0) {
+                                ready = mbar_test(full0 + 8 * nstage, nphase);
+                            } else {
+                                if (m == 1) {
+                                    if (!ready && !mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status,
+                                                             p.timeout_ns)) { ok = false; break; }
+                                    fence_after();
+                                }
+#pragma unroll
+                                for (int c = (m - 1) * CHUNK; c < m * CHUNK && c < NCP; c++) cp_one(nstage, c);
+                            }
+                        }
+                    } else {
+                        for (int m = 0; m < MPS; m++) {
+                            if (m < nk) issue(stage, m, (kb | m) != 0);
+                            if (!has_next) continue;
+                            if (m == 0) {
+                                ready = mbar_test(full0 + 8 * nstage, nphase);
+                            } else {
+                                if (!ready) {
+                                    ready = mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status, p.timeout_ns);
+                                    if (!ready) { ok = false; break; }
+                                }
+                                if (m == 1) fence_after();
+                                for (int c = (m - 1) * CHUNK; c < m * CHUNK && c < NCP; c++) cp_one(nstage, c);
+                            }
                         }
                     }
+                    any = true;
                     commit<1>(empty0 + 8 * stage);
                     if (kb == p.k_stages - 1) commit<1>(tfull);
                     stage = nstage;
