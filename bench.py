@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--small", action="store_true", help="1/8-size shapes (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-reps", type=int, default=4)
+    ap.add_argument("--cpu-reps", type=int, default=12)
     ap.add_argument("--part", default="all", choices=["all", "fwd", "bwd", "nv", "moe"],
                     help="run one part of the step only (profiling)")
     return ap.parse_args()
@@ -277,7 +277,23 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-CPU_SAMPLE = "oracle forward slice: E4M3 quantize of X[:64,4096] and W[:2048,4096], exact dequantize, FP64 GEMM 64x2048x4096"
+def cpu_sample(rows, wrows):
+    return (f"oracle forward slice: E4M3 quantize of X[:{rows},4096] and W[:{wrows},4096], exact dequantize, "
+            f"FP64 GEMM {rows}x{wrows}x4096")
+
+
+CPU_SAMPLE = cpu_sample(64, 2048)
+REF_ROWS, REF_WROWS = 64, 256      # one reference-arm step: a bounded slice (~0.1 s of CPU work)
+
+
+def workload_config(args, world):
+    return {"workload": "llama3-8b block-scaled linear layer step: MXFP8 fwd 8192x14336x4096 + "
+                        "MXFP8 bwd (dgrad, wgrad) + NVFP4 fwd (4096/14336) + MoE 64-expert grouped "
+                        "(MXFP4 -> MXFP8 repack, 32768x2048x7168)" + (" [1/8 size]" if args.small else "")
+                        + ("" if args.part == "all" else f" [part {args.part}]"),
+            "parallelism": f"replica x{world}",
+            "l2": "inputs larger than L2: each step streams ~9 GB, evicting the previous step's data",
+            "value_def": "GEMM FLOPs / whole-step device time"}
 
 
 # ------------------------------------------------------------------ main
@@ -313,23 +329,22 @@ def run_reference(args, rank, world):
     sh = shapes(args.small)
     from block_scaled_precision_03_gb300 import inputs
     f = sh["fwd"]
-    host = {"X": inputs.outlier_activations_bf16((64, f["K"]), 0),
-            "W": inputs.normal_bf16((2048, f["K"]), 1, std=0.02)}
+    host = {"X": inputs.outlier_activations_bf16((REF_ROWS, f["K"]), 0),
+            "W": inputs.normal_bf16((REF_WROWS, f["K"]), 1, std=0.02)}
     for _ in range(args.warmup):
-        cpu_forward_slice(host)
+        cpu_forward_slice(host, REF_ROWS, REF_WROWS)
     ts, fl = [], 0.0
     for _ in range(args.steps):
-        t, fl = cpu_forward_slice(host)
+        t, fl = cpu_forward_slice(host, REF_ROWS, REF_WROWS)
         ts.append(t)
     total = sum(ts)
     value = fl * args.steps / total / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": "llama3-8b block-scaled linear layer (CPU oracle slice)",
-                                            "sample": CPU_SAMPLE},
+            "data": "synthetic", "config": workload_config(args, world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                             "sample": CPU_SAMPLE},
+                             "sample": cpu_sample(REF_ROWS, REF_WROWS) + " per step"},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -456,12 +471,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3/e5m2/e2m1 codes, f32 accumulate", "data": "synthetic",
-            "config": {"workload": "llama3-8b block-scaled linear layer step: MXFP8 fwd 8192x14336x4096 + "
-                                   "MXFP8 bwd (dgrad, wgrad) + NVFP4 fwd (4096/14336) + MoE 64-expert grouped "
-                                   "(MXFP4 -> MXFP8 repack, 32768x2048x7168)" + (" [1/8 size]" if args.small else "") + ("" if args.part == "all" else f" [part {args.part}]"),
-                       "parallelism": f"replica x{world}",
-                       "l2": "inputs larger than L2: each step streams ~9 GB, evicting the previous step's data",
-                       "value_def": "GEMM FLOPs / whole-step device time"},
+            "config": workload_config(args, world),
             "quantize_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
             "quantize_frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "gemm_fp8_tflops": round(g8, 1), "gemm_nvfp4_tflops": round(g4_fl / (g4_ms * 1e-3) / 1e12, 1),
