@@ -24,6 +24,7 @@
 //   warps 2-9   epilogue on each CTA's own 128 accumulator rows
 // Every wait is bounded; a timed-out CTA records the status and exits after
 // its in-flight work drains.
+#include <algorithm>
 #include <cuda.h>
 #include "common.cuh"
 #include "internal.h"
@@ -41,7 +42,8 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;
-constexpr int kRasterGroup = 8;      // 256-row m-tiles per raster group
+constexpr int kRasterGroup = 8;      // default tiles per raster group
+constexpr int64_t kL2Resident = 48ll << 20;   // operand bytes that stay in L2 while the other streams
 
 template <bool FP4>
 struct Cfg2 {
@@ -57,8 +59,9 @@ struct Cfg2 {
     static constexpr uint32_t SFA_COLS = 4 * SF_ATOMS;    // TMEM columns: SFA atoms, then SFB atom pairs
     static constexpr uint32_t SF_COLS = 12 * SF_ATOMS;
     static constexpr uint32_t CTA_TX = 2 * OP_BYTES + SF_STAGE;     // bytes one CTA loads per stage
-    static constexpr int SMEM = 1024 + STAGES * (2 * OP_BYTES + SF_STAGE) + 256;
+    static constexpr int SMEM = 1024 + STAGES * (2 * OP_BYTES + SF_STAGE) + kEpiWarps * 2048 + 256;
     static_assert(kSfCol0 + STAGES * SF_COLS <= kTmemCols, "TMEM columns");
+    static_assert(SMEM <= 232448, "shared memory per block");
 };
 
 struct Params2 {
@@ -67,22 +70,28 @@ struct Params2 {
     int32_t m_tiles, n_tiles, total_tiles;
     void* C;
     int64_t ldc;
-    int32_t out_bf16, vec_ok;
+    int32_t out_bf16, vec_ok, tma_store;
     const float* ts_a;
     const float* ts_b;
     uint32_t idesc;
+    int32_t raster, raster_n;
     unsigned* status;
     uint64_t timeout_ns;
 };
 
+// Tile order: groups of `raster` tiles along one dimension, swept along the
+// other (raster_n: the groups run along n).  A group spanning the whole of
+// the smaller operand keeps that operand resident in L2 while the other one
+// streams through once.
 __device__ __forceinline__ void tile_mn(const Params2& p, int t, int& mt, int& nt) {
-    const int per_group = kRasterGroup * p.n_tiles;
+    const int MT = p.raster_n ? p.n_tiles : p.m_tiles, NT = p.raster_n ? p.m_tiles : p.n_tiles;
+    const int per_group = p.raster * NT;
     const int g = t / per_group;
-    const int first_m = g * kRasterGroup;
-    const int gm = min(kRasterGroup, p.m_tiles - first_m);
+    const int first = g * p.raster;
+    const int gm = min(p.raster, MT - first);
     const int local = t - g * per_group;
-    mt = first_m + local % gm;
-    nt = local / gm;
+    const int a = first + local % gm, b = local / gm;
+    if (p.raster_n) { mt = b; nt = a; } else { mt = a; nt = b; }
 }
 
 __device__ __forceinline__ void spin_ns(uint64_t ns) {
@@ -95,7 +104,7 @@ template <bool FP4>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-             const __grid_constant__ Params2 p) {
+             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params2 p) {
     using CF = Cfg2<FP4>;
     constexpr int S = CF::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -103,7 +112,8 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     uint8_t* smA = base;
     uint8_t* smB = base + S * CF::OP_BYTES;
     uint8_t* smSF = smB + S * CF::OP_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smSF + S * CF::SF_STAGE);
+    uint8_t* smOut = smSF + S * CF::SF_STAGE;             // epilogue staging, 2 KB per warp
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smOut + kEpiWarps * 2048);
     // bars: full[S], empty[S], tfull, tempty, drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -310,10 +320,19 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tempty_c0);
-            const int row = mt * 256 + (int)rank * 128 + q * 32 + lane;
+            const int row0 = mt * 256 + (int)rank * 128 + q * 32;
             const int col0 = nt * BN + h * 128;
-            if (row < p.M && col0 < p.N) store_row128(r, p.C, p.ldc, row, col0, p.N, p.out_bf16, p.vec_ok, alpha);
+            if (p.tma_store) {
+                if (row0 < p.M && col0 < p.N) {
+                    const uint32_t buf = tc::smem_u32(smOut + (warp - 2) * 2048);
+                    if (p.out_bf16) store_tile_tma<true>(r, buf, &tmC, col0, row0, alpha, lane);
+                    else store_tile_tma<false>(r, buf, &tmC, col0, row0, alpha, lane);
+                }
+            } else if (row0 + lane < p.M && col0 < p.N) {
+                store_row128(r, p.C, p.ldc, row0 + lane, col0, p.N, p.out_bf16, p.vec_ok, alpha);
+            }
         }
+        if (lane == 0) tc::bulk_wait_all();
     }
 
     // a CTA that gave up lets copies still in flight into its shared memory land
@@ -329,14 +348,14 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
 
 template <bool FP4>
 cudaError_t launch2(const Params2& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
-                    const CUtensorMap& tsb, int grid, cudaStream_t st) {
+                    const CUtensorMap& tsb, const CUtensorMap& tc_, int grid, cudaStream_t st) {
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(gemm2_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<FP4>::SMEM);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    gemm2_kernel<FP4><<<grid, kThreads, Cfg2<FP4>::SMEM, st>>>(ta, tb, tsa, tsb, p);
+    gemm2_kernel<FP4><<<grid, kThreads, Cfg2<FP4>::SMEM, st>>>(ta, tb, tsa, tsb, tc_, p);
     return cudaGetLastError();
 }
 
@@ -368,6 +387,17 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
                   : make_idesc(a.fmt_a == kE5M2 ? 1 : 0, a.fmt_b == kE5M2 ? 1 : 0, true, 256, BN);
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
+    // raster order: sweep the larger operand past the whole of the smaller one
+    // when the smaller one fits in L2 with room to spare
+    {
+        const int64_t a_bytes = a.M * kbytes, b_bytes = a.N * kbytes;
+        p.raster = kRasterGroup;
+        p.raster_n = 0;
+        if (std::min(a_bytes, b_bytes) <= kL2Resident) {
+            p.raster_n = b_bytes < a_bytes;
+            p.raster = p.raster_n ? p.n_tiles : p.m_tiles;
+        }
+    }
 
     const int sf_atoms = fp4 ? Cfg2<true>::SF_ATOMS : Cfg2<false>::SF_ATOMS;
     CUtensorMap ta, tb, tsa, tsb;
@@ -375,10 +405,14 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     if (!tmap::codes_2d(&tb, a.b_codes, a.N, kbytes, 128)) return cudaErrorInvalidValue;
     if (!tmap::scales_3d(&tsa, a.a_scales, (a.M + 127) / 128, n_atoms, sf_atoms, 1)) return cudaErrorInvalidValue;
     if (!tmap::scales_3d(&tsb, a.b_scales, (a.N + 127) / 128, n_atoms, sf_atoms, 2)) return cudaErrorInvalidValue;
+    // TMA stores of the output when its base and row pitch allow them
+    CUtensorMap tcm = ta;
+    p.tma_store = p.vec_ok && tmap::out_2d(&tcm, a.C, a.M, a.N, a.N, a.out_bf16 != 0);
+    if (!p.tma_store) tcm = ta;
     int pairs = a.num_sms / 2;
     if (p.total_tiles < pairs) pairs = p.total_tiles;
     if (pairs < 1) pairs = 1;
-    return fp4 ? launch2<true>(p, ta, tb, tsa, tsb, 2 * pairs, st) : launch2<false>(p, ta, tb, tsa, tsb, 2 * pairs, st);
+    return fp4 ? launch2<true>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st) : launch2<false>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st);
 }
 
 }  // namespace bsq

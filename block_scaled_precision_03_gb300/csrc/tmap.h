@@ -53,5 +53,22 @@ inline bool scales_3d(CUtensorMap* m, const void* ptr, int64_t bands, int64_t at
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major output matrix [rows, cols] of BF16 or FP32 for TMA stores: box =
+// 64 bytes x 32 rows, 64-byte swizzle; elements outside the matrix are not
+// written.  Needs a 16-byte aligned base and a row pitch that is a multiple
+// of 16 bytes.
+inline bool out_2d(CUtensorMap* m, void* ptr, int64_t rows, int64_t cols, int64_t ld, bool bf16) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    const uint32_t esz = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * esz)};
+    cuuint32_t box[2] = {64u / esz, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tmap
 }  // namespace bsq
