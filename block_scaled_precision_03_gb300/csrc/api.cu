@@ -65,6 +65,13 @@ bool env_single_cta() {
     return v && v[0] == '1';
 }
 
+// BSQ_GEMM_GROUPED_PAIR=1 sends grouped GEMMs to the CTA-pair kernel whatever
+// the expert sizes (when their layout allows it); used by the test suite.
+bool env_grouped_pair() {
+    const char* v = std::getenv("BSQ_GEMM_GROUPED_PAIR");
+    return v && v[0] == '1';
+}
+
 const uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
 
 }  // namespace
@@ -227,6 +234,8 @@ bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_de
     a.num_groups = num_groups;
     a.offsets = group_offsets_dev;
     a.b_group_scales = sf;
+    a.single_cta = env_single_cta();
+    a.grouped_pair = env_grouped_pair();
     a.num_sms = num_sms();
     a.status = st;
     a.timeout_ns = kDefaultTimeoutNs;

@@ -102,6 +102,10 @@ __device__ __forceinline__ void record_status(unsigned* status, unsigned bits) {
     if (status) atomicOr(status, bits);
 }
 
+// v clamped to [lo, hi] (row offsets read from device memory)
+__device__ __forceinline__ int clamp_rows(int64_t v, int64_t lo, int64_t hi) {
+    return (int)(v < lo ? lo : (v > hi ? hi : v));
+}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));

@@ -52,7 +52,11 @@ struct Cfg {
     static constexpr int SFB_BYTES = 2 * SF_ATOMS * 512;
     static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
     static constexpr uint32_t SF_COLS = FP4 ? 48 : 12;   // TMEM columns per stage slot
-    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES + SF_STAGE) + 256 + 8 * (kMaxGroups + 1) + 8 * kMaxGroups;
+    // epilogue staging for TMA stores (FP8 only: the NVFP4 ring leaves no room)
+    static constexpr int OUT_STAGE = FP4 ? 0 : kEpiWarps * 2048;
+    static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES + SF_STAGE) + OUT_STAGE + 256 + 8 * (kMaxGroups + 1) +
+                                8 * kMaxGroups;
+    static_assert(SMEM <= 232448, "shared memory per block");
 };
 
 struct Params {
@@ -68,7 +72,7 @@ struct Params {
     int32_t b_bands;               // 128-row bands of B (per group)
     void* C;
     int64_t ldc;
-    int32_t out_bf16, vec_ok;
+    int32_t out_bf16, vec_ok, tma_store;
     const float* ts_a;
     const float* ts_b;
     uint32_t idesc;
@@ -123,14 +127,15 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int t, const Grou
 template <bool FP4>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            const __grid_constant__ Params p) {
+            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params p) {
     using CF = Cfg<FP4>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* smA = base;
     uint8_t* smB = base + STAGES * A_BYTES;
     uint8_t* smSF = smB + STAGES * B_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smSF + STAGES * CF::SF_STAGE);
+    uint8_t* smOut = smSF + STAGES * CF::SF_STAGE;      // epilogue staging, 2 KB per warp (FP8)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smOut + CF::OUT_STAGE);
     // bars: full[STAGES], empty[STAGES], tfull, tempty, drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -162,7 +167,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         int acc = 0;
         gt->prefix[0] = 0;
         for (int g = 0; g < p.num_groups; g++) {
-            const int lo = (int)p.offsets[g], hi = (int)p.offsets[g + 1];
+            const int lo = clamp_rows(p.offsets[g], 0, p.M);
+            const int hi = clamp_rows(p.offsets[g + 1], lo, p.M);
             const int b0 = lo / BM, b1 = (hi + BM - 1) / BM;
             const int cnt = hi > lo ? b1 - b0 : 0;
             gt->band0[g] = b0; gt->lo[g] = lo; gt->hi[g] = hi;
@@ -341,11 +347,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty);
 
-            const int row = ti.a_row0 + q * 32 + lane;
+            // this warp's 32 rows, clipped to the rows the tile may write
+            const int row0 = ti.a_row0 + q * 32;
             const int col0 = ti.n0 + h * 128;
-            if (row < ti.row_lo || row >= ti.row_hi || col0 >= p.N) continue;
-            store_row128(r, p.C, p.ldc, row, col0, p.N, p.out_bf16, p.vec_ok, alpha);
+            const int lo = max(row0, ti.row_lo), hi = min(row0 + 32, ti.row_hi);
+            if (lo >= hi || col0 >= p.N) continue;
+            if (!FP4 && p.tma_store && lo == row0 && hi == row0 + 32) {
+                const uint32_t buf = smem_u32(smOut + (warp - 2) * 2048);
+                if (p.out_bf16) store_tile_tma<true>(r, buf, &tmC, col0, row0, alpha, lane);
+                else store_tile_tma<false>(r, buf, &tmC, col0, row0, alpha, lane);
+            } else if (row0 + lane >= lo && row0 + lane < hi) {
+                store_row128(r, p.C, p.ldc, row0 + lane, col0, p.N, p.out_bf16, p.vec_ok, alpha);
+            }
         }
+        if (lane == 0) bulk_wait_all();
     }
 
     fence_before();
@@ -358,8 +373,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
 // ----------------------------------------------------------------- host
 template <bool FP4>
-cudaError_t launch(const GemmArgs& a, const Params& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
-                   cudaStream_t st) {
+cudaError_t launch(const GemmArgs& a, const Params& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                   const CUtensorMap& tc_, int grid, cudaStream_t st) {
     static bool attr_done = false;
     cudaError_t e;
     if (!attr_done) {
@@ -367,14 +382,23 @@ cudaError_t launch(const GemmArgs& a, const Params& p, const CUtensorMap& ta, co
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    gemm_kernel<FP4><<<grid, kThreads, Cfg<FP4>::SMEM, st>>>(ta, tb, p);
+    gemm_kernel<FP4><<<grid, kThreads, Cfg<FP4>::SMEM, st>>>(ta, tb, tc_, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st) {
-    if (a.num_groups == 0 && !a.single_cta) return run_gemm_pair(a, st);
+    // Grouped GEMMs go to CTA pairs when experts average at least
+    // kPairRowsPerGroup rows: a 256-row pair tile leaves on average half a
+    // tile idle per expert, against a quarter of a 256-row span for the
+    // 128-row tiles of the single-CTA kernel.
+    constexpr int64_t kPairRowsPerGroup = 1024;
+    if (!a.single_cta) {
+        if (a.num_groups == 0) return run_gemm_pair(a, st);
+        if (gemm_pair_grouped_ok(a) && (a.grouped_pair || a.M >= kPairRowsPerGroup * a.num_groups))
+            return run_gemm_pair(a, st);
+    }
     const bool fp4 = a.fmt_a == kNVFP4;
     const int64_t kbytes = fp4 ? a.K / 2 : a.K;
     const int blk = fp4 ? 16 : 32;
@@ -412,10 +436,14 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st) {
     const int64_t b_rows = a.num_groups ? a.N * a.num_groups : a.N;
     if (!tmap::codes_2d(&ta, a.a_codes, a.M, kbytes, BM)) return cudaErrorInvalidValue;
     if (!tmap::codes_2d(&tb, a.b_codes, b_rows, kbytes, BN)) return cudaErrorInvalidValue;
+    // TMA stores of whole 32-row boxes when the output's base and row pitch allow them
+    CUtensorMap tcm = ta;
+    p.tma_store = !fp4 && p.vec_ok && tmap::out_2d(&tcm, a.C, a.M, a.N, a.N, a.out_bf16 != 0);
+    if (!p.tma_store) tcm = ta;
     int grid = a.num_sms;
     if (a.num_groups == 0 && p.total_tiles < grid) grid = p.total_tiles;
     if (grid < 1) grid = 1;
-    return fp4 ? launch<true>(a, p, ta, tb, grid, st) : launch<false>(a, p, ta, tb, grid, st);
+    return fp4 ? launch<true>(a, p, ta, tb, tcm, grid, st) : launch<false>(a, p, ta, tb, tcm, grid, st);
 }
 
 // ------------------------------------------------------------ timeout probe

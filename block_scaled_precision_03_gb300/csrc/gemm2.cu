@@ -45,6 +45,18 @@ constexpr uint32_t kSfCol0 = 256;
 constexpr int kRasterGroup = 8;      // default tiles per raster group
 constexpr int64_t kL2Resident = 48ll << 20;   // operand bytes that stay in L2 while the other streams
 
+// Grouped mode: per expert g its rows [lo, hi) of A and C, its first 128-row
+// band of A and the number of 256-row tiles (pairs of bands) covering it;
+// prefix[g] = tiles of the experts before g.
+struct GroupTable2 {
+    int32_t prefix[kMaxGroups + 1];
+    int32_t band0[kMaxGroups];
+    int32_t pairs[kMaxGroups];
+    int32_t lo[kMaxGroups];
+    int32_t hi[kMaxGroups];
+};
+constexpr int kGroupTableBytes = (int)sizeof(GroupTable2);
+
 template <bool FP4>
 struct Cfg2 {
     // KSUB 128-byte K sub-steps per stage: more MMAs per barrier handshake
@@ -59,7 +71,7 @@ struct Cfg2 {
     static constexpr uint32_t SFA_COLS = 4 * SF_ATOMS;    // TMEM columns: SFA atoms, then SFB atom pairs
     static constexpr uint32_t SF_COLS = 12 * SF_ATOMS;
     static constexpr uint32_t CTA_TX = 2 * OP_BYTES + SF_STAGE;     // bytes one CTA loads per stage
-    static constexpr int SMEM = 1024 + STAGES * (2 * OP_BYTES + SF_STAGE) + kEpiWarps * 2048 + 256;
+    static constexpr int SMEM = 1024 + STAGES * (2 * OP_BYTES + SF_STAGE) + kEpiWarps * 2048 + 256 + kGroupTableBytes;
     static_assert(kSfCol0 + STAGES * SF_COLS <= kTmemCols, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory per block");
 };
@@ -75,6 +87,9 @@ struct Params2 {
     const float* ts_b;
     uint32_t idesc;
     int32_t raster, raster_n;
+    int32_t num_groups;            // 0 = dense
+    int32_t group_bands;           // 128-row bands of one expert's B
+    const int64_t* offsets;        // grouped: device row offsets, num_groups + 1
     unsigned* status;
     uint64_t timeout_ns;
 };
@@ -100,6 +115,46 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
     }
 }
 
+// What one CTA of the pair loads and stores for tile t.  The two CTAs own
+// one 128-row band of A each; in grouped mode both bands belong to the same
+// expert (any two of its bands: each CTA loads its own), so a tile never
+// mixes experts and at most half a tile is idle when an expert covers an odd
+// number of bands.
+struct Tile2 {
+    int32_t a_band;        // this CTA's 128-row band of A (also its scale band)
+    int32_t nt;            // 256-column tile of C
+    int32_t b_row;         // this CTA's first B row
+    int32_t sfb_band;      // first of the tile's two B scale bands
+    int32_t row_lo, row_hi;    // rows of C this CTA may write
+};
+
+__device__ __forceinline__ Tile2 tile2(const Params2& p, int t, const GroupTable2* gt, int& gcur, uint32_t rank) {
+    Tile2 ti;
+    if (p.num_groups == 0) {
+        int mt, nt;
+        tile_mn(p, t, mt, nt);
+        ti.a_band = mt * 2 + (int)rank;
+        ti.nt = nt;
+        ti.b_row = nt * BN + (int)rank * 128;
+        ti.sfb_band = nt * 2;
+        ti.row_lo = ti.a_band * 128;
+        ti.row_hi = min(p.M, ti.row_lo + 128);
+    } else {
+        while (t >= gt->prefix[gcur + 1]) ++gcur;
+        const int g = gcur;
+        const int pairs = gt->pairs[g];
+        const int local = t - gt->prefix[g];
+        const int pi = local % pairs;
+        ti.nt = local / pairs;
+        ti.a_band = gt->band0[g] + 2 * pi + (int)rank;
+        ti.b_row = g * p.N + ti.nt * BN + (int)rank * 128;
+        ti.sfb_band = g * p.group_bands + ti.nt * 2;
+        ti.row_lo = max(gt->lo[g], ti.a_band * 128);
+        ti.row_hi = min(gt->hi[g], ti.a_band * 128 + 128);
+    }
+    return ti;
+}
+
 template <bool FP4>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -114,6 +169,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     uint8_t* smSF = smB + S * CF::OP_BYTES;
     uint8_t* smOut = smSF + S * CF::SF_STAGE;             // epilogue staging, 2 KB per warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(smOut + kEpiWarps * 2048);
+    GroupTable2* gt = reinterpret_cast<GroupTable2*>(bars + 32);
     // bars: full[S], empty[S], tfull, tempty, drain
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 3);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -142,11 +198,39 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         tc::prefetch_tmap(&tmSFB);
     }
     if (warp == 1) tc::tmem_alloc<2>(tc::smem_u32(tmem_slot), kTmemCols);
+    if (p.num_groups > 0 && warp == 2) {
+        // expert table, 32 experts per pass; offsets are clamped to [0, M]
+        int carry = 0;
+        for (int g0 = 0; g0 < p.num_groups; g0 += 32) {
+            const int g = g0 + lane;
+            int pairs = 0;
+            if (g < p.num_groups) {
+                const int lo = clamp_rows(p.offsets[g], 0, p.M);
+                const int hi = clamp_rows(p.offsets[g + 1], lo, p.M);
+                const int b0 = lo / 128;
+                if (hi > lo) pairs = ((hi - 1) / 128 - b0 + 2) / 2;
+                gt->band0[g] = b0;
+                gt->pairs[g] = pairs;
+                gt->lo[g] = lo;
+                gt->hi[g] = hi;
+            }
+            int v = pairs * p.n_tiles;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, d);
+                if (lane >= d) v += u;
+            }
+            if (g < p.num_groups) gt->prefix[g + 1] = carry + v;
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) gt->prefix[0] = 0;
+    }
     tc::fence_before();
     __syncthreads();
     tc::cluster_sync();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int total = p.num_groups > 0 ? gt->prefix[p.num_groups] : p.total_tiles;
     bool aborted = false;
 
     if (warp == 0) {
@@ -156,10 +240,10 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = cid; t < p.total_tiles && ok; t += ncl) {
-                int mt, nt;
-                tile_mn(p, t, mt, nt);
-                const int arow = mt * 256 + (int)rank * 128, brow = nt * BN + (int)rank * 128;
+            int gcur = 0;
+            for (int t = cid; t < total && ok; t += ncl) {
+                const Tile2 ti = tile2(p, t, gt, gcur, rank);
+                const int arow = ti.a_band * 128, brow = ti.b_row;
                 for (int kb = 0; kb < p.k_stages; kb++) {
                     if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, p.timeout_ns)) {
                         ok = false;
@@ -174,8 +258,8 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                         tc::tma_load_2d_pair(tc::smem_u32(smA + stage * CF::OP_BYTES + j * HALF), &tmA, kx, arow, fb);
                         tc::tma_load_2d_pair(tc::smem_u32(smB + stage * CF::OP_BYTES + j * HALF), &tmB, kx, brow, fb);
                     }
-                    tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, mt * 2 + (int)rank, fb);
-                    tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS, nt * 2, fb);
+                    tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, ti.a_band, fb);
+                    tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS, ti.sfb_band, fb);
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
@@ -210,7 +294,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             uint32_t phase = 0;
             int iter = 0;
             bool ok = true, any = false;
-            if (cid < p.total_tiles) {
+            if (cid < total) {
                 ok = tc::mbar_wait(full0, 0, abort_flag, p.status, p.timeout_ns);
                 if (ok) {
                     tc::fence_after();
@@ -218,10 +302,10 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     for (int c = 0; c < NCP; c++) cp_one(0, c);
                 }
             }
-            for (int t = cid; t < p.total_tiles && ok; t += ncl, ++iter) {
+            for (int t = cid; t < total && ok; t += ncl, ++iter) {
                 if (!tc::mbar_wait<true>(tempty, (iter & 1) ^ 1, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
                 tc::fence_after();
-                const bool more_tiles = t + ncl < p.total_tiles;
+                const bool more_tiles = t + ncl < total;
                 for (int kb = 0; kb < p.k_stages; kb++) {
                     const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + CF::SFA_COLS;
                     const uint64_t ad = ad_base + (uint64_t)(stage * OP_STEP), bd = bd_base + (uint64_t)(stage * OP_STEP);
@@ -304,10 +388,9 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         const uint32_t tempty_c0 = tc::mapa(tempty, 0);
         float alpha = 1.0f;
         if (FP4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
-        int iter = 0;
-        for (int t = cid; t < p.total_tiles; t += ncl, ++iter) {
-            int mt, nt;
-            tile_mn(p, t, mt, nt);
+        int iter = 0, gcur = 0;
+        for (int t = cid; t < total; t += ncl, ++iter) {
+            const Tile2 ti = tile2(p, t, gt, gcur, rank);
             if (!tc::mbar_wait(tfull, iter & 1, abort_flag, p.status, p.timeout_ns)) { aborted = true; break; }
             tc::fence_after();
             uint32_t r[4][32];
@@ -320,15 +403,17 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tempty_c0);
-            const int row0 = mt * 256 + (int)rank * 128 + q * 32;
-            const int col0 = nt * BN + h * 128;
-            if (p.tma_store) {
-                if (row0 < p.M && col0 < p.N) {
-                    const uint32_t buf = tc::smem_u32(smOut + (warp - 2) * 2048);
-                    if (p.out_bf16) store_tile_tma<true>(r, buf, &tmC, col0, row0, alpha, lane);
-                    else store_tile_tma<false>(r, buf, &tmC, col0, row0, alpha, lane);
-                }
-            } else if (row0 + lane < p.M && col0 < p.N) {
+            // this warp's 32 rows, clipped to the rows the CTA may write
+            const int row0 = ti.a_band * 128 + q * 32;
+            const int col0 = ti.nt * BN + h * 128;
+            const int lo = max(row0, ti.row_lo), hi = min(row0 + 32, ti.row_hi);
+            if (lo >= hi || col0 >= p.N) continue;
+            if (p.tma_store && (hi == row0 + 32 || hi == p.M) && lo == row0) {
+                // whole box (rows past M are clipped by the tensor map)
+                const uint32_t buf = tc::smem_u32(smOut + (warp - 2) * 2048);
+                if (p.out_bf16) store_tile_tma<true>(r, buf, &tmC, col0, row0, alpha, lane);
+                else store_tile_tma<false>(r, buf, &tmC, col0, row0, alpha, lane);
+            } else if (row0 + lane >= lo && row0 + lane < hi) {
                 store_row128(r, p.C, p.ldc, row0 + lane, col0, p.N, p.out_bf16, p.vec_ok, alpha);
             }
         }
@@ -361,7 +446,20 @@ cudaError_t launch2(const Params2& p, const CUtensorMap& ta, const CUtensorMap& 
 
 }  // namespace
 
-// Dense GEMM on CTA pairs; grouped GEMMs use the 1-CTA kernel (run_gemm).
+// True when a grouped GEMM can run on CTA pairs: MXFP8, whole 128-row scale
+// bands per expert and the experts' scale buffers evenly spaced (one tensor
+// map then spans all of them).
+bool gemm_pair_grouped_ok(const GemmArgs& a) {
+    if (a.num_groups < 1 || a.fmt_a == kNVFP4 || a.N % 128 != 0) return false;
+    const int64_t n_atoms = (a.K / 32 + 3) / 4;
+    const int64_t stride = (a.N / 128) * n_atoms * 512;
+    for (int g = 0; g < a.num_groups; g++)
+        if (a.b_group_scales[g] != a.b_group_scales[0] + g * stride) return false;
+    return true;
+}
+
+// Block-scaled GEMM on CTA pairs: dense, or grouped over experts when
+// gemm_pair_grouped_ok() holds.
 cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     const bool fp4 = a.fmt_a == kNVFP4;
     const int64_t kbytes = fp4 ? a.K / 2 : a.K;
@@ -387,6 +485,10 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
                   : make_idesc(a.fmt_a == kE5M2 ? 1 : 0, a.fmt_b == kE5M2 ? 1 : 0, true, 256, BN);
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
+    const bool grouped = a.num_groups > 0;
+    p.num_groups = a.num_groups;
+    p.offsets = a.offsets;
+    p.group_bands = (int32_t)(a.N / 128);
     // raster order: sweep the larger operand past the whole of the smaller one
     // when the smaller one fits in L2 with room to spare
     {
@@ -402,15 +504,17 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     const int sf_atoms = fp4 ? Cfg2<true>::SF_ATOMS : Cfg2<false>::SF_ATOMS;
     CUtensorMap ta, tb, tsa, tsb;
     if (!tmap::codes_2d(&ta, a.a_codes, a.M, kbytes, 128)) return cudaErrorInvalidValue;
-    if (!tmap::codes_2d(&tb, a.b_codes, a.N, kbytes, 128)) return cudaErrorInvalidValue;
+    const int64_t b_rows = grouped ? a.N * a.num_groups : a.N;
+    const uint8_t* b_sf = grouped ? a.b_group_scales[0] : a.b_scales;
+    if (!tmap::codes_2d(&tb, a.b_codes, b_rows, kbytes, 128)) return cudaErrorInvalidValue;
     if (!tmap::scales_3d(&tsa, a.a_scales, (a.M + 127) / 128, n_atoms, sf_atoms, 1)) return cudaErrorInvalidValue;
-    if (!tmap::scales_3d(&tsb, a.b_scales, (a.N + 127) / 128, n_atoms, sf_atoms, 2)) return cudaErrorInvalidValue;
+    if (!tmap::scales_3d(&tsb, b_sf, (b_rows + 127) / 128, n_atoms, sf_atoms, 2)) return cudaErrorInvalidValue;
     // TMA stores of the output when its base and row pitch allow them
     CUtensorMap tcm = ta;
     p.tma_store = p.vec_ok && tmap::out_2d(&tcm, a.C, a.M, a.N, a.N, a.out_bf16 != 0);
     if (!p.tma_store) tcm = ta;
     int pairs = a.num_sms / 2;
-    if (p.total_tiles < pairs) pairs = p.total_tiles;
+    if (!grouped && p.total_tiles < pairs) pairs = p.total_tiles;
     if (pairs < 1) pairs = 1;
     return fp4 ? launch2<true>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st) : launch2<false>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st);
 }

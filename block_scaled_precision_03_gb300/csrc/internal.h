@@ -61,10 +61,12 @@ struct GemmArgs {
     int num_sms;
     unsigned* status;
     uint64_t timeout_ns;
-    bool single_cta;               // dense: use the 1-CTA kernel instead of the CTA pair
+    bool single_cta;               // use the 1-CTA kernel instead of the CTA pair
+    bool grouped_pair;             // grouped: CTA pairs whatever the expert sizes
 };
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st);
 cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st);
+bool gemm_pair_grouped_ok(const GemmArgs& a);
 
 cudaError_t run_timeout_probe(unsigned* status, uint64_t limit_ns, cudaStream_t st);
 

@@ -275,6 +275,95 @@ def test_grouped_gemm_small(bsq):
         assert ok.all(), (g, (~ok).sum())
 
 
+GROUPED_CASES = {
+    # expert sizes with odd band counts, an expert ending mid-band, empty experts
+    "ragged": (np.array([700, 0, 129, 1, 383, 256, 1000, 0, 31], dtype=np.int64), 384, 4160),
+    # every expert starts and ends on a 128-row boundary
+    "aligned": (np.array([256, 128, 512, 0, 384], dtype=np.int64), 512, 256),
+    # one expert holding every row
+    "single": (np.array([1111], dtype=np.int64), 256, 96),
+}
+
+
+_GROUPED_CACHE = {}
+
+
+def _grouped_case_oracle(case):
+    """Oracle codes, scales and exactly dequantized operands of a case (cached
+    across the kernel-path and output-type parametrizations)."""
+    if case not in _GROUPED_CACHE:
+        counts, N, K = GROUPED_CASES[case]
+        off = inputs.group_offsets(counts)
+        xa = inputs.normal_bf16((int(off[-1]), K), 21)
+        xw = inputs.normal_bf16((len(counts) * N, K), 22, std=0.02)
+        ca, sa, _ = _q_oracle(xa, "mxfp8_e4m3")
+        cw, sw, _ = _q_oracle(xw, "mxfp8_e4m3")
+        _GROUPED_CACHE[case] = (off, ca, sa, cw, sw, oracle.dequant_rows(ca, sa, "mxfp8_e4m3"),
+                                oracle.dequant_rows(cw, sw, "mxfp8_e4m3"))
+    return _GROUPED_CACHE[case]
+
+
+@pytest.mark.parametrize("case", sorted(GROUPED_CASES))
+@pytest.mark.parametrize("path", ["pair", "single_cta"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_grouped_gemm_cases(bsq, monkeypatch, case, path, out):
+    """Grouped GEMM on both kernels against the oracle, inside a guarded
+    output buffer: rows before and after C keep their sentinel."""
+    import torch
+    monkeypatch.setenv("BSQ_GEMM_1CTA" if path == "single_cta" else "BSQ_GEMM_GROUPED_PAIR", "1")
+    counts, N, K = GROUPED_CASES[case]
+    G = len(counts)
+    off, ca, sa, cw, sw, Ad, Wd = _grouped_case_oracle(case)
+    M = int(off[-1])
+    A = upload_q(bsq, "mxfp8_e4m3", ca, sa)
+    W = upload_q(bsq, "mxfp8_e4m3", cw, sw)
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    guard = 64
+    buf = torch.full((M + 2 * guard, N), -7.0, dtype=dt, device="cuda")
+    C = buf[guard:guard + M]
+    bsq.grouped_gemm_into(A, torch.from_numpy(off).cuda(), bsq.group_views(W, G), C)
+    bsq.sync_status()
+    host = buf.float().cpu().numpy()
+    assert (host[:guard] == -7.0).all() and (host[guard + M:] == -7.0).all(), "write outside C"
+    Ch = host[guard:guard + M]
+    for g in range(G):
+        lo, hi = off[g], off[g + 1]
+        if hi == lo:
+            continue
+        ref, mag = oracle.gemm_full(Ad[lo:hi], Wd[g * N:(g + 1) * N])
+        ok, err, tol = gemm_tol_ok(Ch[lo:hi], ref, mag, out == "bf16")
+        assert ok.all(), (case, path, g, int((~ok).sum()))
+
+
+def test_grouped_gemm_scattered_scales(bsq):
+    """Experts whose scale buffers are separate allocations (not evenly
+    spaced) take the single-CTA kernel; results match the oracle."""
+    import torch
+    counts = np.array([300, 129, 0, 500], dtype=np.int64)
+    G, N, K = len(counts), 256, 512
+    off = inputs.group_offsets(counts)
+    xa = inputs.normal_bf16((int(off[-1]), K), 31)
+    xw = inputs.normal_bf16((G * N, K), 32, std=0.02)
+    ca, sa, _ = _q_oracle(xa, "mxfp8_e4m3")
+    cw, sw, _ = _q_oracle(xw, "mxfp8_e4m3")
+    A = upload_q(bsq, "mxfp8_e4m3", ca, sa)
+    W = upload_q(bsq, "mxfp8_e4m3", cw, sw)
+    views = bsq.group_views(W, G)
+    # same codes; each expert's scales copied to its own allocation, in reverse order
+    own = [v.scales.clone() for v in views[::-1]][::-1]
+    scattered = [bsq.QTensor(v.fmt, v.rows, v.cols, v.codes, sc, v.tensor_scale) for v, sc in zip(views, own)]
+    C = bsq.grouped_gemm(A, torch.from_numpy(off).cuda(), scattered, torch.float32).cpu().numpy()
+    Ad = oracle.dequant_rows(ca, sa, "mxfp8_e4m3")
+    Wd = oracle.dequant_rows(cw, sw, "mxfp8_e4m3")
+    for g in range(G):
+        lo, hi = off[g], off[g + 1]
+        if hi == lo:
+            continue
+        ref, mag = oracle.gemm_full(Ad[lo:hi], Wd[g * N:(g + 1) * N])
+        ok, err, tol = gemm_tol_ok(C[lo:hi], ref, mag, False)
+        assert ok.all(), (g, int((~ok).sum()))
+
+
 # ----------------------------------------------------------------- failures
 def test_timeout_probe_reports_status(bsq):
     bsq.sync_status()
