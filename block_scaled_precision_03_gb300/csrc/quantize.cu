@@ -222,7 +222,8 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
 // NVFP4 row-wise kernel: one thread = one 16-element block (two 16-byte
 // loads), so the per-block scale work is done once and needs no shuffle.
 // ---------------------------------------------------------------------------
-constexpr int kNvUnroll = 2;
+constexpr int kNvUnroll = 1;
+constexpr int kNvMinBlocks = 4;     // CTAs per SM the register budget must allow
 
 __device__ __forceinline__ uint4 ld_cached(const uint4* p) {
     uint4 r;
@@ -230,7 +231,7 @@ __device__ __forceinline__ uint4 ld_cached(const uint4* p) {
     return r;
 }
 
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kRowThreads, kNvMinBlocks)
 quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row, int64_t s_tiles,
                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const unsigned* __restrict__ nv_amax) {
     const int lane = threadIdx.x & 31;
@@ -541,10 +542,16 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
         case kE5M2: e = launch_rows<kE5M2>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
         case kMXFP4: e = launch_rows<kMXFP4>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
         default: {
+            // persistent grid: as many CTAs as fit on the SMs at once
+            static int resident = 0;
+            if (resident == 0 &&
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, quantize_rows_nv_kernel, kRowThreads, 0) != cudaSuccess)
+                resident = kNvMinBlocks;
+            if (resident < 1) resident = 1;
             const int64_t nblocks = R * C / 16;
             const int64_t per_cta = (int64_t)kRowThreads * kNvUnroll;
             int64_t grid = (nblocks + per_cta - 1) / per_cta;
-            if (grid > (int64_t)a.num_sms * 8) grid = (int64_t)a.num_sms * 8;
+            if (grid > (int64_t)a.num_sms * resident) grid = (int64_t)a.num_sms * resident;
             if (grid < 1) grid = 1;
             const int64_t S = C / 16;
             quantize_rows_nv_kernel<<<(unsigned)grid, kRowThreads, 0, st>>>(
