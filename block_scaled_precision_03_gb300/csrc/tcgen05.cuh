@@ -36,9 +36,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
-// arrive on a barrier of another CTA of the cluster (shared::cluster address)
+// Arrive on a barrier of any CTA of the cluster (shared::cluster address),
+// with the default release semantics at CTA scope.  Used to hand tensor
+// memory back after tcgen05.wait::ld + tcgen05.fence::before_thread_sync:
+// nothing in memory needs publishing, and a cluster-scope release would wait
+// for the thread's outstanding memory traffic (about a microsecond here).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cbar) : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cbar) : "memory");
 }
 // CTA-scope test of a phase (the common case: arrivals from this CTA or
 // from the async proxy: TMA, tcgen05.commit)
