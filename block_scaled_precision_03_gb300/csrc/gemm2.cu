@@ -303,7 +303,9 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 }
             }
             for (int t = cid; t < total && ok; t += ncl, ++iter) {
-                if (!tc::mbar_wait<true>(tempty, (iter & 1) ^ 1, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+                // both CTAs' epilogue warps arrive here after their TMEM loads completed
+                // (tcgen05.wait::ld); a CTA-scope acquire suffices
+                if (!tc::mbar_wait(tempty, (iter & 1) ^ 1, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
                 tc::fence_after();
                 const bool more_tiles = t + ncl < total;
                 for (int kb = 0; kb < p.k_stages; kb++) {
