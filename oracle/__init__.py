@@ -84,6 +84,10 @@ def _load():
     lib.bsqo_mx_quantize_rows.argtypes = [ctypes.c_int, ctypes.c_int, p, c_i64, c_i64, p, p]
     lib.bsqo_nvfp4_tensor_scale.restype = ctypes.c_float
     lib.bsqo_nvfp4_tensor_scale.argtypes = [p, c_i64]
+    lib.bsqo_tensor_amax.restype = ctypes.c_float
+    lib.bsqo_tensor_amax.argtypes = [p, c_i64]
+    lib.bsqo_nvfp4_delayed_tensor_scale.restype = ctypes.c_float
+    lib.bsqo_nvfp4_delayed_tensor_scale.argtypes = [p, c_i64]
     lib.bsqo_nvfp4_quantize_rows.restype = None
     lib.bsqo_nvfp4_quantize_rows.argtypes = [p, c_i64, c_i64, ctypes.c_float, p, p]
     lib.bsqo_mx_dequant_rows.restype = None
@@ -169,6 +173,43 @@ def nvfp4_quantize_rows(x_bits: np.ndarray, s_t: float | None = None):
     scales = np.empty((R, C // 16), dtype=np.uint8)
     _load().bsqo_nvfp4_quantize_rows(_ptr(x), R, C, ctypes.c_float(s_t), _ptr(codes), _ptr(scales))
     return codes, scales, s_t
+
+
+def tensor_amax(x_bits: np.ndarray) -> float:
+    """Largest finite |x| of a BF16 tensor (bit patterns)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    return float(np.float32(_load().bsqo_tensor_amax(_ptr(x), x.size)))
+
+
+def nvfp4_delayed_tensor_scale(history) -> float:
+    """NVFP4 tensor scale under delayed scaling: max(history) / 2688 (FP32),
+    1 when the history holds no positive finite value."""
+    h = np.ascontiguousarray(history, dtype=np.float32)
+    return float(np.float32(_load().bsqo_nvfp4_delayed_tensor_scale(_ptr(h), h.size)))
+
+
+def nvfp4_delayed_quantize(x_bits: np.ndarray, history, axis: str = "row"):
+    """NVFP4 quantize with a delayed tensor scale ("FP8 Training
+    Infrastructure": delayed scaling from the amax history of previous
+    iterations, length 16, algorithm max, margin 0).
+
+    The tensor scale comes from the history as it stands before this step;
+    the blocks are then encoded by the just-in-time NVFP4 steps with that
+    scale (values beyond its range saturate); last, this tensor's amax is
+    pushed to the front of the history and the oldest entry dropped.
+    Returns {"row": (codes, scales), "col": (codes, scales), "s_t": s_t,
+    "history": new_history}, with only the requested orientations."""
+    h = np.asarray(history, dtype=np.float32)
+    s_t = nvfp4_delayed_tensor_scale(h)
+    out = {"s_t": s_t}
+    if axis in ("row", "both"):
+        c, s, _ = nvfp4_quantize_rows(x_bits, s_t)
+        out["row"] = (c, s)
+    if axis in ("col", "both"):
+        c, s, _ = nvfp4_quantize_rows(np.ascontiguousarray(np.asarray(x_bits).T), s_t)
+        out["col"] = (c, s)
+    out["history"] = np.concatenate([np.float32([tensor_amax(x_bits)]), h[:-1]]).astype(np.float32)
+    return out
 
 
 def quantize_rows(x_bits: np.ndarray, fmt_name: str):

@@ -220,6 +220,37 @@ float bsqo_nvfp4_tensor_scale(const uint16_t* x, int64_t n)
     return s_t;
 }
 
+/* Largest finite |x| of a BF16 tensor: the tensor amax of the NVFP4 recipe
+ * (non-finite values are skipped, as in bsqo_nvfp4_tensor_scale). */
+float bsqo_tensor_amax(const uint16_t* x, int64_t n)
+{
+    int64_t i;
+    float amax = 0.0f;
+    for (i = 0; i < n; i++) {
+        float f = bf16_to_float(x[i]);
+        if (isfinite(f) && fabsf(f) > amax) amax = fabsf(f);
+    }
+    return amax;
+}
+
+/* Delayed scaling ("FP8 Training Infrastructure", sections "Transformer
+ * Engine: a fundacao de software" and "Estrategias de escalonamento e
+ * estabilidade": scale factors come from the amax values observed in
+ * previous iterations; history length 16, algorithm "max", margin 0).
+ * For NVFP4 the tensor scale of the current step is
+ *   s_t = max(history) / 2688   (FP32, round to nearest),
+ * and 1 when the history holds no positive finite value (the same rule as
+ * an all-zero tensor in the just-in-time recipe). */
+float bsqo_nvfp4_delayed_tensor_scale(const float* hist, int64_t n)
+{
+    int64_t i;
+    float m = 0.0f;
+    for (i = 0; i < n; i++)
+        if (isfinite(hist[i]) && hist[i] > m) m = hist[i];
+    if (m == 0.0f) return 1.0f;
+    return m / 2688.0f;
+}
+
 void bsqo_nvfp4_quantize_rows(const uint16_t* x, int64_t R, int64_t C, float s_t,
                               uint8_t* codes, uint8_t* scales)
 {

@@ -364,3 +364,59 @@ def test_column_wise_is_transpose():
     np.testing.assert_array_equal(c1, c2)
     np.testing.assert_array_equal(s1, s2)
     assert c1.shape == (96, 64)
+
+
+# ------------------------------------------------------------ delayed scaling
+def _abs_max_numpy(x_bits):
+    """max |x| of finite BF16 values, by numpy on the FP32 widening."""
+    f = (np.asarray(x_bits, np.uint32) << 16).view(np.float32)
+    f = np.abs(f[np.isfinite(f)])
+    return float(f.max()) if f.size else 0.0
+
+
+def test_delayed_equals_just_in_time_when_history_holds_the_amax():
+    # a history whose max is this tensor's own amax reproduces the
+    # just-in-time recipe exactly (tensor scale, block scales, codes)
+    x = inputs.outlier_activations_bf16((96, 256), 5)
+    amax = _abs_max_numpy(x)
+    hist = np.float32([amax / 4, amax, 0.0, amax / 2] + [0.0] * 12)
+    d = oracle.nvfp4_delayed_quantize(x, hist, "both")
+    for key, src in (("row", x), ("col", np.ascontiguousarray(x.T))):
+        c, s, st = oracle.nvfp4_quantize_rows(src)
+        np.testing.assert_array_equal(d[key][0], c)
+        np.testing.assert_array_equal(d[key][1], s)
+        assert d["s_t"] == st
+
+
+def test_delayed_history_update():
+    x = inputs.normal_bf16((32, 64), 6)
+    hist = np.float32(np.arange(1, 17))
+    d = oracle.nvfp4_delayed_quantize(x, hist)
+    assert d["history"].dtype == np.float32 and d["history"].shape == (16,)
+    assert d["history"][0] == np.float32(_abs_max_numpy(x))
+    np.testing.assert_array_equal(d["history"][1:], hist[:-1])
+    assert d["s_t"] == float(np.float32(16.0) / np.float32(2688.0))
+
+
+def test_delayed_saturates_beyond_the_history():
+    # history max = amax / 64: the block holding the amax takes the largest
+    # UE4M3 scale (448) and its largest element the largest E2M1 code (6), so
+    # it dequantizes to 6 * 448 * s_t = max(history) exactly; nothing is larger
+    x = inputs.normal_bf16((16, 128), 7)
+    amax = _abs_max_numpy(x)
+    h = np.float32([amax / 64.0] + [0.0] * 15)
+    d = oracle.nvfp4_delayed_quantize(x, h)
+    c, s = d["row"]
+    v = oracle.dequant_rows(c, s, "nvfp4", d["s_t"])
+    assert np.abs(v).max() == 6.0 * 448.0 * d["s_t"]
+    r, k = np.unravel_index(np.argmax(np.abs((np.asarray(x, np.uint32) << 16).view(np.float32))), x.shape)
+    assert s[r, k // 16] == 0x7E and abs(v[r, k]) == 6.0 * 448.0 * d["s_t"]
+
+
+def test_delayed_empty_history_uses_unit_scale():
+    x = inputs.normal_bf16((16, 64), 8)
+    d = oracle.nvfp4_delayed_quantize(x, np.zeros(16, np.float32))
+    assert d["s_t"] == 1.0
+    c, s, _ = oracle.nvfp4_quantize_rows(x, 1.0)
+    np.testing.assert_array_equal(d["row"][0], c)
+    np.testing.assert_array_equal(d["row"][1], s)
