@@ -181,9 +181,37 @@ class Step:
         part_of = ["fwd"] * 3 + ["bwd"] * 5 + ["nv"] * 6 + ["moe"] * 4
         if part == "bwd":
             want = ("fwd", "bwd")      # the backward quantizes from the forward inputs
-        self.op_part = {op[0]: pt for op, pt in zip(ops, part_of)}
         ops = [op for op, pt in zip(ops, part_of) if pt in want]
         self.ops = ops
+        # Rows beyond the core path, timed on their own after the step (not
+        # part of the step's time or FLOPs).  NEXT-3: NVFP4 with delayed
+        # scaling, one pass (2.5625 B per element), the amax history holding
+        # the tensor's own amax as in steady state.
+        self.extra_ops = []
+        if "nv" in want:
+            B_NV1 = 2 + 0.5 + 1 / 16
+            qd = bsq.quantize_nvfp4_delayed_into
+            self.hist = {}
+            for k in ("X4", "W4", "X42", "W42"):
+                f = (np.asarray(host[k], np.uint32) << 16).view(np.float32)
+                h = torch.zeros(16, dtype=torch.float32, device="cuda")
+                h[0] = float(np.abs(f[np.isfinite(f)]).max())
+                self.hist[k] = h
+            o["X4d"] = E("nvfp4", n["M"], n["K"])
+            o["W4d"] = E("nvfp4", n["N"], n["K"])
+            o["X42d"] = E("nvfp4", n["M"], n["K2"])
+            o["W42d"] = E("nvfp4", n["N"], n["K2"])
+            hs = self.hist
+            self.extra_ops = [
+                ("quant X nvfp4 delayed", "NEXT-3", "quant", lambda: qd(i["X4"], "row", o["X4d"], None, hs["X4"]),
+                 n["M"] * n["K"] * B_NV1, 0, 2),
+                ("quant W nvfp4 delayed", "NEXT-3", "quant", lambda: qd(i["W4"], "row", o["W4d"], None, hs["W4"]),
+                 n["N"] * n["K"] * B_NV1, 0, 2),
+                ("quant X' nvfp4 delayed", "NEXT-3", "quant", lambda: qd(i["X42"], "row", o["X42d"], None, hs["X42"]),
+                 n["M"] * n["K2"] * B_NV1, 0, 2),
+                ("quant W' nvfp4 delayed", "NEXT-3", "quant", lambda: qd(i["W42"], "row", o["W42d"], None, hs["W42"]),
+                 n["N"] * n["K2"] * B_NV1, 0, 2),
+            ]
         self.flops = sum(op[5] for op in ops)
         self.kernels = sum(op[6] for op in ops)
 
@@ -463,6 +491,29 @@ def main():
         a[2] += flops
     for kind in ("quant", "repack", "gemm8", "gemm4"):
         agg.setdefault(kind, [1e-30, 0.0, 0.0])
+
+    # rows beyond the core path: each timed alone, cycling through all of
+    # them so that every input has left L2 before it is read again
+    rows_next = {}
+    if step.extra_ops:
+        reps = 20
+        for _ in range(3):
+            for op in step.extra_ops:
+                op[3]()
+        xev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in step.extra_ops] for _ in range(reps)]
+        torch.cuda.synchronize()
+        for r in range(reps):
+            for j, op in enumerate(step.extra_ops):
+                xev[r][j][0].record()
+                op[3]()
+                xev[r][j][1].record()
+        torch.cuda.synchronize()
+        for j, (name, row, kind, _, nbytes, flops, nk) in enumerate(step.extra_ops):
+            ms = statistics.mean(xev[r][j][0].elapsed_time(xev[r][j][1]) for r in range(reps))
+            ach = nbytes / (ms * 1e-3) / 1e9
+            rows_next[name] = {"row": row, "ms": round(ms, 4), "gbs": round(ach, 1),
+                               "frac": round(ach / pk["hbm_gbs"], 4), "frac_spec_8tbs": round(ach / 8000.0, 4)}
     q_ms, q_bytes = agg["quant"][0] + agg["repack"][0], agg["quant"][1] + agg["repack"][1]
     g8_ms, g8_fl = agg["gemm8"][0], agg["gemm8"][2]
     g4_ms, g4_fl = agg["gemm4"][0], agg["gemm4"][2]
@@ -527,7 +578,7 @@ def main():
             "quantize_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
             "quantize_frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "gemm_fp8_tflops": round(g8, 1), "gemm_nvfp4_tflops": round(g4_fl / (g4_ms * 1e-3) / 1e12, 1),
-            "roofline": roofline, "rows": rows, "gpu_launches": step.kernels * args.steps,
+            "roofline": roofline, "rows": rows, "rows_next": rows_next, "gpu_launches": step.kernels * args.steps,
             "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "peaks": {k: pk[k] for k in ("hbm_gbs", "fp8_tflops", "fp4_tflops", "source")},
         }

@@ -61,6 +61,7 @@ def lib():
         "bsq_codes_bytes": (sz, [i32, i64, i64]),
         "bsq_scales_bytes": (sz, [i32, i64, i64]),
         "bsq_quantize": (i32, [vp, i64, i64, i32, i32, PT, PT, vp]),
+        "bsq_quantize_nvfp4_delayed": (i32, [vp, i64, i64, i32, PT, PT, vp, i32, vp]),
         "bsq_dequantize": (i32, [PT, vp, i32, vp]),
         "bsq_gemm": (i32, [PT, PT, vp, i32, vp]),
         "bsq_grouped_gemm": (i32, [PT, vp, i32, PT, vp, i32, vp]),
@@ -148,6 +149,35 @@ def quantize(x, fmt, axis="row", stream=None):
     row = empty(fmt, R, C, x.device) if a & ROWWISE else None
     col = empty(fmt, C, R, x.device) if a & COLWISE else None
     quantize_into(x, fmt, a, row, col, stream)
+    return row, col
+
+
+def quantize_nvfp4_delayed_into(x, axis, out_row: QTensor | None, out_col: QTensor | None, history, stream=None):
+    """NVFP4 quantize with delayed scaling into given tensors; `history` is a
+    float32 CUDA tensor of past amax values, updated in place."""
+    import torch
+    assert history.dtype == torch.float32 and history.is_cuda and history.is_contiguous()
+    a = AXES[axis] if isinstance(axis, str) else int(axis)
+    R, C = x.shape
+    cr = out_row.c() if out_row is not None else None
+    cc = out_col.c() if out_col is not None else None
+    st = lib().bsq_quantize_nvfp4_delayed(ctypes.c_void_p(x.data_ptr()), R, C, a,
+                                          ctypes.byref(cr) if cr is not None else None,
+                                          ctypes.byref(cc) if cc is not None else None,
+                                          ctypes.c_void_p(history.data_ptr()), history.numel(), _stream(stream))
+    _check(st, "bsq_quantize_nvfp4_delayed")
+
+
+def quantize_nvfp4_delayed(x, history, axis="row", stream=None):
+    """NVFP4 quantize of a contiguous BF16 CUDA matrix with the tensor scale
+    taken from `history` (see bsq_quantize_nvfp4_delayed); returns (row, col)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.is_cuda and x.is_contiguous()
+    a = AXES[axis] if isinstance(axis, str) else int(axis)
+    R, C = x.shape
+    row = empty("nvfp4", R, C, x.device) if a & ROWWISE else None
+    col = empty("nvfp4", C, R, x.device) if a & COLWISE else None
+    quantize_nvfp4_delayed_into(x, a, row, col, history, stream)
     return row, col
 
 

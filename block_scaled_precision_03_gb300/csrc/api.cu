@@ -74,23 +74,11 @@ bool env_grouped_pair() {
 
 const uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
 
-}  // namespace
-
-extern "C" {
-
-size_t bsq_codes_bytes(int32_t fmt, int64_t rows, int64_t cols) {
-    if (!valid_fmt(fmt) || rows < 0 || cols < 0) return 0;
-    if (fp4(fmt) && (cols % 2)) return 0;
-    return codes_bytes(fmt, rows, cols);
-}
-
-size_t bsq_scales_bytes(int32_t fmt, int64_t rows, int64_t cols) {
-    if (!valid_fmt(fmt) || rows < 0 || cols < 0 || (cols % blk(fmt)) != 0) return 0;
-    return scales_bytes(fmt, rows, cols);
-}
-
-bsq_status bsq_quantize(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
-                        bsq_tensor* out_row, bsq_tensor* out_col, void* stream) {
+// bsq_quantize and bsq_quantize_nvfp4_delayed: argument checks and launch;
+// `history` (NVFP4 only) selects delayed scaling.
+bsq_status quantize_common(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
+                           bsq_tensor* out_row, bsq_tensor* out_col, float* history, int32_t hist_len,
+                           void* stream) {
     if (!src_bf16 || !valid_fmt(fmt) || axis < BSQ_ROWWISE || axis > BSQ_BOTH) return BSQ_ERR_INVALID_ARG;
     if (rows < 1 || cols < 1) return BSQ_ERR_INVALID_ARG;
     if (!al16(src_bf16) || (cols % 8) != 0) return BSQ_ERR_ALIGNMENT;
@@ -132,7 +120,40 @@ bsq_status bsq_quantize(const void* src_bf16, int64_t rows, int64_t cols, int32_
         a.col_scales_pad = scales_padded(fmt, cols, rows);
     }
     a.num_sms = num_sms();
+    a.history = history;
+    a.hist_len = hist_len;
     return from_cuda(bsq::run_quantize(a, static_cast<cudaStream_t>(stream)));
+}
+
+
+}  // namespace
+
+extern "C" {
+
+size_t bsq_codes_bytes(int32_t fmt, int64_t rows, int64_t cols) {
+    if (!valid_fmt(fmt) || rows < 0 || cols < 0) return 0;
+    if (fp4(fmt) && (cols % 2)) return 0;
+    return codes_bytes(fmt, rows, cols);
+}
+
+size_t bsq_scales_bytes(int32_t fmt, int64_t rows, int64_t cols) {
+    if (!valid_fmt(fmt) || rows < 0 || cols < 0 || (cols % blk(fmt)) != 0) return 0;
+    return scales_bytes(fmt, rows, cols);
+}
+
+bsq_status bsq_quantize(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
+                        bsq_tensor* out_row, bsq_tensor* out_col, void* stream) {
+    return quantize_common(src_bf16, rows, cols, fmt, axis, out_row, out_col, nullptr, 0, stream);
+}
+
+bsq_status bsq_quantize_nvfp4_delayed(const void* src_bf16, int64_t rows, int64_t cols, int32_t axis,
+                                      bsq_tensor* out_row, bsq_tensor* out_col, float* amax_history,
+                                      int32_t history_len, void* stream) {
+    if (!amax_history || history_len < 1 || history_len > 4096) return BSQ_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(amax_history) & 3) return BSQ_ERR_ALIGNMENT;
+    // same argument rules as bsq_quantize with NVFP4; the scale then comes from the history
+    return quantize_common(src_bf16, rows, cols, BSQ_NVFP4_E2M1, axis, out_row, out_col, amax_history, history_len,
+                           stream);
 }
 
 bsq_status bsq_dequantize(const bsq_tensor* in, void* dst, int32_t dst_type, void* stream) {

@@ -14,6 +14,8 @@ struct QuantizeArgs {
     size_t row_scales_bytes, col_scales_bytes;
     bool row_scales_pad, col_scales_pad;     // buffer has padding to zero
     int num_sms;
+    float* history;                // NVFP4 delayed scaling: amax history (nullptr: just in time)
+    int hist_len;
 };
 cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st);
 

@@ -119,6 +119,54 @@ __device__ __forceinline__ float nv_tensor_scale(const unsigned* amax_bits) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
 }
 
+// Where a kernel takes the NVFP4 tensor scale from: the amax of this tensor
+// (just in time, after the amax pass) or, with delayed scaling ("FP8 Training
+// Infrastructure", "Estrategias de escalonamento": scale factors from the
+// amax of previous iterations, history length 16, algorithm max), the
+// largest positive finite entry of the amax history; then this tensor's
+// amax is accumulated in the same pass for the history update.
+struct NvScale {
+    const unsigned* amax_bits;     // just in time: tensor amax (FP32 bits)
+    const float* history;          // delayed: amax history (nullptr: just in time)
+    int32_t hist_len;
+    unsigned* amax_acc;            // delayed: this tensor's amax accumulates here (FP32 bits)
+};
+
+__device__ __forceinline__ float nv_history_scale(const float* h, int n) {
+    float m = 0.0f;
+    for (int i = 0; i < n; i++) {
+        const float v = h[i];
+        if (isfinite(v) && v > m) m = v;
+    }
+    return m == 0.0f ? 1.0f : __fdiv_rn(m, 2688.0f);
+}
+
+__device__ __forceinline__ float nv_scale_of(const NvScale& ns) {
+    return ns.history ? nv_history_scale(ns.history, ns.hist_len) : nv_tensor_scale(ns.amax_bits);
+}
+
+// Running max of finite |x| (BF16 bit patterns without sign): `am` is the
+// max over a group of values given as packed words `w`; a group holding a
+// non-finite value is rescanned for its finite ones.
+__device__ __forceinline__ void nv_acc_group(uint32_t& acc, uint32_t am, const uint32_t* w, int nw) {
+    if (am < 0x7F80u) {
+        acc = max(acc, am);
+        return;
+    }
+    for (int q = 0; q < nw; q++) {
+        const uint32_t lo = w[q] & 0x7FFFu, hi = (w[q] >> 16) & 0x7FFFu;
+        if (lo < 0x7F80u) acc = max(acc, lo);
+        if (hi < 0x7F80u) acc = max(acc, hi);
+    }
+}
+
+// Warp-wide max of `acc`, one atomic per warp (all lanes of the warp call it).
+__device__ __forceinline__ void nv_acc_flush(const NvScale& ns, uint32_t acc) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) acc = max(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
+    if ((threadIdx.x & 31) == 0 && acc) atomicMax(ns.amax_acc, acc << 16);
+}
+
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
     uint4 r;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -150,7 +198,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kRowThreads)
 quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t blocks_per_row,
                      int64_t s_tiles, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                     const unsigned* __restrict__ nv_amax) {
+                     const NvScale nv) {
     constexpr int BLK = block_of(FMT);
     constexpr int LPB = BLK / 8;            // lanes per block: 4 (MX) or 2 (NV)
     const int lane = threadIdx.x & 31;
@@ -159,7 +207,7 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
     const bool vec_sf = (blocks_per_row & 3u) == 0;
     float s_t = 1.0f, inv_st = 1.0f;
     if (FMT == kNVFP4) {
-        s_t = nv_tensor_scale(nv_amax);
+        s_t = nv_scale_of(nv);
         inv_st = __frcp_rn(s_t);
     }
 
@@ -231,15 +279,17 @@ __device__ __forceinline__ uint4 ld_cached(const uint4* p) {
     return r;
 }
 
+template <bool DELAYED>
 __global__ void __launch_bounds__(kRowThreads, kNvMinBlocks)
 quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row, int64_t s_tiles,
-                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const unsigned* __restrict__ nv_amax) {
+                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const NvScale nv) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
     const bool vec_sf = (blocks_per_row & 3u) == 0;
-    const float s_t = nv_tensor_scale(nv_amax);
+    const float s_t = nv_scale_of(nv);
     const float inv_st = __frcp_rn(s_t);
+    uint32_t acc = 0;                 // delayed scaling: running amax of this tensor
     const int64_t step = nwarps * 32 * kNvUnroll;
     uint4 w[kNvUnroll][2];
     int64_t base = warp * 32 * kNvUnroll;
@@ -261,6 +311,11 @@ quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t
         for (int u = 0; u < kNvUnroll; u++) {
             const int64_t b = base + u * 32 + lane;
             const uint32_t am = max(absmax8(w[u][0]), absmax8(w[u][1]));
+            if (DELAYED && b < nblocks) {
+                const uint32_t ws[8] = {w[u][0].x, w[u][0].y, w[u][0].z, w[u][0].w,
+                                        w[u][1].x, w[u][1].y, w[u][1].z, w[u][1].w};
+                nv_acc_group(acc, am, ws, 8);
+            }
             const uint32_t sb = nv_scale_byte(am, s_t, inv_st);
             float f[16];
             unpack8(w[u][0], f);
@@ -285,6 +340,7 @@ quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t
 #pragma unroll
         for (int u = 0; u < kNvUnroll; u++) { w[u][0] = wn[u][0]; w[u][1] = wn[u][1]; }
     }
+    if (DELAYED) nv_acc_flush(nv, acc);
 }
 
 // ---------------------------------------------------------------------------
@@ -299,7 +355,7 @@ __global__ void __launch_bounds__(kTileThreads)
 quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
                      uint8_t* __restrict__ codes_r, uint8_t* __restrict__ scales_r, int64_t s_tiles_r,
                      uint8_t* __restrict__ codes_c, uint8_t* __restrict__ scales_c, int64_t s_tiles_c,
-                     const unsigned* __restrict__ nv_amax) {
+                     const NvScale nv) {
     constexpr int BLK = block_of(FMT);
     constexpr int NB = kTile / BLK;                 // blocks per tile edge: 4 or 8
     __shared__ __align__(16) uint32_t tile[kTile * kPitchW];
@@ -311,7 +367,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
     const int64_t c0 = (int64_t)blockIdx.x * kTile;
     float s_t = 1.0f, inv_st = 1.0f;
     if (FMT == kNVFP4) {
-        s_t = nv_tensor_scale(nv_amax);
+        s_t = nv_scale_of(nv);
         inv_st = __frcp_rn(s_t);
     }
 
@@ -327,6 +383,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
     }
     __syncthreads();
 
+    uint32_t acc = 0;
     if (COL) {
         // task = (row-block rb, column pair cp): two columns x BLK rows
         constexpr int TASKS = NB * (kTile / 2);
@@ -341,6 +398,8 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
                 am_lo = max(am_lo, w[r] & 0x7FFFu);
                 am_hi = max(am_hi, (w[r] >> 16) & 0x7FFFu);
             }
+            // delayed scaling: this tile's finite amax (zero-filled padding adds nothing)
+            if (FMT == kNVFP4 && nv.amax_acc) nv_acc_group(acc, max(am_lo, am_hi), w, BLK);
 #pragma unroll
             for (int half = 0; half < 2; half++) {
                 const uint32_t am = half ? am_hi : am_lo;
@@ -368,6 +427,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
             }
         }
     }
+    if (FMT == kNVFP4 && nv.amax_acc) nv_acc_flush(nv, acc);
     if (ROW) {
         // task = (row rr, column block cb): BLK contiguous elements
         constexpr int TASKS = kTile * NB;
@@ -483,12 +543,24 @@ __global__ void nv_finalize_kernel(float* ts0, float* ts1) {
     if (ts1) *ts1 = s;
 }
 
+// Delayed scaling, after the quantize pass: the outputs get the tensor scale
+// the pass used (from the history as it stood), and the history takes this
+// tensor's amax at the front, dropping its oldest entry.
+__global__ void nv_delayed_finalize_kernel(float* hist, int n, float* ts0, float* ts1) {
+    const float s = nv_history_scale(hist, n);
+    const float amax = __uint_as_float(*reinterpret_cast<const unsigned*>(ts0));
+    for (int i = n - 1; i > 0; i--) hist[i] = hist[i - 1];
+    hist[0] = amax;
+    *ts0 = s;
+    if (ts1) *ts1 = s;
+}
+
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
 template <int FMT>
 static cudaError_t launch_rows(const void* src, int64_t R, int64_t C, uint8_t* codes, uint8_t* scales,
-                               const unsigned* nv_amax, cudaStream_t st, int num_sms) {
+                               const NvScale& nv, cudaStream_t st, int num_sms) {
     const int64_t nchunks = R * C / 8;
     const int64_t per_cta = (int64_t)kRowThreads * kRowUnroll;
     int64_t grid = (nchunks + per_cta - 1) / per_cta;
@@ -496,22 +568,22 @@ static cudaError_t launch_rows(const void* src, int64_t R, int64_t C, uint8_t* c
     if (grid < 1) grid = 1;
     const int64_t S = C / block_of(FMT);
     quantize_rows_kernel<FMT><<<(unsigned)grid, kRowThreads, 0, st>>>(
-        reinterpret_cast<const uint4*>(src), nchunks, (uint32_t)S, (S + 3) / 4, codes, scales, nv_amax);
+        reinterpret_cast<const uint4*>(src), nchunks, (uint32_t)S, (S + 3) / 4, codes, scales, nv);
     return cudaGetLastError();
 }
 
 template <int FMT>
 static cudaError_t launch_tile(const void* src, int64_t R, int64_t C, int axis,
                                uint8_t* cr, uint8_t* sr, uint8_t* cc, uint8_t* sc,
-                               const unsigned* nv_amax, cudaStream_t st) {
+                               const NvScale& nv, cudaStream_t st) {
     dim3 grid((unsigned)((C + kTile - 1) / kTile), (unsigned)((R + kTile - 1) / kTile));
     const int BLK = block_of(FMT);
     const int64_t str = (C / BLK + 3) / 4, stc = (R / BLK + 3) / 4;
     const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
     if (axis == 3)
-        quantize_tile_kernel<FMT, true, true><<<grid, kTileThreads, 0, st>>>(s, R, C, cr, sr, str, cc, sc, stc, nv_amax);
+        quantize_tile_kernel<FMT, true, true><<<grid, kTileThreads, 0, st>>>(s, R, C, cr, sr, str, cc, sc, stc, nv);
     else
-        quantize_tile_kernel<FMT, false, true><<<grid, kTileThreads, 0, st>>>(s, R, C, cr, sr, str, cc, sc, stc, nv_amax);
+        quantize_tile_kernel<FMT, false, true><<<grid, kTileThreads, 0, st>>>(s, R, C, cr, sr, str, cc, sc, stc, nv);
     return cudaGetLastError();
 }
 
@@ -526,9 +598,19 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
         if ((e = cudaMemsetAsync(a.col_scales, 0, a.col_scales_bytes, st)) != cudaSuccess) return e;
     }
     unsigned* amax = nullptr;
+    NvScale nv{};
     if (a.fmt == kNVFP4) {
+        // the tensor-scale output first holds the amax (FP32 bits)
         amax = reinterpret_cast<unsigned*>(a.axis & 1 ? a.row_ts : a.col_ts);
         if ((e = cudaMemsetAsync(amax, 0, sizeof(float), st)) != cudaSuccess) return e;
+    }
+    if (a.fmt == kNVFP4 && a.history) {
+        // delayed scaling: no amax pass; the quantize pass accumulates the amax
+        nv.history = a.history;
+        nv.hist_len = a.hist_len;
+        nv.amax_acc = amax;
+    } else if (a.fmt == kNVFP4) {
+        nv.amax_bits = amax;
         int64_t nchunks = R * C / 8;
         int64_t grid = (nchunks + 256 * 4 - 1) / (256 * 4);
         if (grid > (int64_t)a.num_sms * 8) grid = (int64_t)a.num_sms * 8;
@@ -538,14 +620,15 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
     }
     if (a.axis == 1) {
         switch (a.fmt) {
-        case kE4M3: e = launch_rows<kE4M3>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
-        case kE5M2: e = launch_rows<kE5M2>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
-        case kMXFP4: e = launch_rows<kMXFP4>(a.src, R, C, a.row_codes, a.row_scales, amax, st, a.num_sms); break;
+        case kE4M3: e = launch_rows<kE4M3>(a.src, R, C, a.row_codes, a.row_scales, nv, st, a.num_sms); break;
+        case kE5M2: e = launch_rows<kE5M2>(a.src, R, C, a.row_codes, a.row_scales, nv, st, a.num_sms); break;
+        case kMXFP4: e = launch_rows<kMXFP4>(a.src, R, C, a.row_codes, a.row_scales, nv, st, a.num_sms); break;
         default: {
             // persistent grid: as many CTAs as fit on the SMs at once
             static int resident = 0;
             if (resident == 0 &&
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, quantize_rows_nv_kernel, kRowThreads, 0) != cudaSuccess)
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, quantize_rows_nv_kernel<false>, kRowThreads, 0) !=
+                    cudaSuccess)
                 resident = kNvMinBlocks;
             if (resident < 1) resident = 1;
             const int64_t nblocks = R * C / 16;
@@ -554,24 +637,31 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
             if (grid > (int64_t)a.num_sms * resident) grid = (int64_t)a.num_sms * resident;
             if (grid < 1) grid = 1;
             const int64_t S = C / 16;
-            quantize_rows_nv_kernel<<<(unsigned)grid, kRowThreads, 0, st>>>(
-                reinterpret_cast<const uint4*>(a.src), nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, amax);
+            if (nv.amax_acc)
+                quantize_rows_nv_kernel<true><<<(unsigned)grid, kRowThreads, 0, st>>>(
+                    reinterpret_cast<const uint4*>(a.src), nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, nv);
+            else
+                quantize_rows_nv_kernel<false><<<(unsigned)grid, kRowThreads, 0, st>>>(
+                    reinterpret_cast<const uint4*>(a.src), nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, nv);
             e = cudaGetLastError();
             break;
         }
         }
     } else {
         switch (a.fmt) {
-        case kE4M3: e = launch_tile<kE4M3>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, amax, st); break;
-        case kE5M2: e = launch_tile<kE5M2>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, amax, st); break;
-        case kMXFP4: e = launch_tile<kMXFP4>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, amax, st); break;
-        default: e = launch_tile<kNVFP4>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, amax, st); break;
+        case kE4M3: e = launch_tile<kE4M3>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, nv, st); break;
+        case kE5M2: e = launch_tile<kE5M2>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, nv, st); break;
+        case kMXFP4: e = launch_tile<kMXFP4>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, nv, st); break;
+        default: e = launch_tile<kNVFP4>(a.src, R, C, a.axis, a.row_codes, a.row_scales, a.col_codes, a.col_scales, nv, st); break;
         }
     }
     if (e != cudaSuccess) return e;
     if (a.fmt == kNVFP4) {
         float* other = (a.axis == 3) ? a.col_ts : nullptr;
-        nv_finalize_kernel<<<1, 1, 0, st>>>(reinterpret_cast<float*>(amax), other);
+        if (a.history)
+            nv_delayed_finalize_kernel<<<1, 1, 0, st>>>(a.history, a.hist_len, reinterpret_cast<float*>(amax), other);
+        else
+            nv_finalize_kernel<<<1, 1, 0, st>>>(reinterpret_cast<float*>(amax), other);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

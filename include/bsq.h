@@ -122,6 +122,27 @@ size_t bsq_scales_bytes(int32_t fmt, int64_t rows, int64_t cols);
 bsq_status bsq_quantize(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
                         bsq_tensor* out_row, bsq_tensor* out_col, void* stream);
 
+/* NVFP4 quantize with delayed scaling: one pass instead of two.  The tensor
+ * scale is taken from the amax of previous steps instead of this tensor:
+ *   s_t = max(amax_history) / 2688 (FP32; positive finite entries only;
+ *         1 when there is none),
+ * the blocks are then encoded as by bsq_quantize with that s_t (values
+ * beyond its range saturate to the largest block scale and code), each
+ * written tensor_scale receives s_t, and last this tensor's amax (largest
+ * finite |x|) is pushed to the front of amax_history and its oldest entry
+ * dropped.  amax_history: DEVICE float[history_len], 4-byte aligned, owned
+ * by the caller, read and updated in stream order (zero-filled before the
+ * first step); 1 <= history_len <= 4096.  Arguments and outputs otherwise
+ * as bsq_quantize with fmt = BSQ_NVFP4_E2M1; on an argument error nothing
+ * is launched and the history is unchanged.  Citation: FP8 page,
+ * "Transformer Engine: a fundacao de software" (DelayedScaling recipe:
+ * amax_history_len = 16, amax_compute_algo = "max", margin = 0) and
+ * "Estrategias de escalonamento e estabilidade" (scale factors from the
+ * statistics of previous iterations). */
+bsq_status bsq_quantize_nvfp4_delayed(const void* src_bf16, int64_t rows, int64_t cols, int32_t axis,
+                                      bsq_tensor* out_row, bsq_tensor* out_col, float* amax_history,
+                                      int32_t history_len, void* stream);
+
 /* Exact dequantization dst[rows, cols] = code * scale (* tensor scale),
  * rounded once to FP32 or BF16 (nearest-even).  dst is device memory,
  * 16-byte aligned.  Citation: MoE FP4 page section 2 (the dequantization

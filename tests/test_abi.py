@@ -70,3 +70,11 @@ def test_host_argument_checks_launch_nothing(lib):
     # repack needs MXFP4 in, E4M3 out
     assert lib.bsq_mxfp4_to_mxfp8(ctypes.byref(a), ctypes.byref(a), null) == 2
     assert lib.bsq_status_string(5) == b"device wait timed out"
+    # delayed NVFP4: history pointer and length are checked before anything else
+    t4 = bsq.BsqTensorC(3, 0, 128, 128, 256, 512, 1024)
+    assert lib.bsq_quantize_nvfp4_delayed(ctypes.c_void_p(256), 128, 128, 1, ctypes.byref(t4), None, None, 16, null) == 1
+    assert lib.bsq_quantize_nvfp4_delayed(ctypes.c_void_p(256), 128, 128, 1, ctypes.byref(t4), None,
+                                          ctypes.c_void_p(4096), 0, null) == 1
+    assert lib.bsq_quantize_nvfp4_delayed(ctypes.c_void_p(256), 128, 128, 1, ctypes.byref(t4), None,
+                                          ctypes.c_void_p(4098), 16, null) == 3
+    assert lib.bsq_quantize_nvfp4_delayed(None, 128, 128, 1, ctypes.byref(t4), None, ctypes.c_void_p(4096), 16, null) == 1

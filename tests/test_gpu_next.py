@@ -1,0 +1,106 @@
+"""Parity of the rows beyond the core path, against the oracle.
+
+NVFP4 with delayed scaling: the tensor scale comes from an amax history of
+previous steps ("FP8 Training Infrastructure", DelayedScaling recipe with
+amax_history_len = 16, algorithm max); codes, scales, the tensor scale and
+the updated history must equal the oracle's byte for byte."""
+import numpy as np
+import pytest
+
+import oracle
+from block_scaled_precision_03_gb300 import inputs
+from _util import dev_bf16, host_u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bsq():
+    import block_scaled_precision_03_gb300 as b
+    b.lib()
+    return b
+
+
+def _abs_max(x_bits):
+    f = (np.asarray(x_bits, np.uint32) << 16).view(np.float32)
+    return float(np.abs(f[np.isfinite(f)]).max())
+
+
+def _check_delayed(q, codes, scales, s_t, what):
+    exp_c = oracle.storage_codes(codes, "nvfp4")
+    got_c = host_u8(q.codes).reshape(exp_c.shape)
+    assert np.array_equal(got_c, exp_c), f"{what}: {(got_c != exp_c).sum()} code bytes differ"
+    got_s = host_u8(q.scales)
+    assert np.array_equal(got_s, oracle.swizzle_scales(scales)), f"{what}: scales differ"
+    assert np.float32(q.tensor_scale.cpu().numpy()[0]) == np.float32(s_t), what
+
+
+@pytest.mark.parametrize("shape", [(256, 512), (304, 1040), (16, 16), (1008, 96)])
+@pytest.mark.parametrize("axis", ["row", "col", "both"])
+def test_delayed_nvfp4_matches_oracle(bsq, shape, axis):
+    import torch
+    R, C = shape
+    x = inputs.outlier_activations_bf16(shape, 11)
+    hist0 = np.float32([3.0, 0.0, 7.5, 1.0] + [0.0] * 12)
+    h = torch.from_numpy(hist0.copy()).cuda()
+    row, col = bsq.quantize_nvfp4_delayed(dev_bf16(x), h, axis)
+    exp = oracle.nvfp4_delayed_quantize(x, hist0, axis)
+    if row is not None:
+        _check_delayed(row, *exp["row"], exp["s_t"], f"row {shape}")
+    if col is not None:
+        _check_delayed(col, *exp["col"], exp["s_t"], f"col {shape}")
+    np.testing.assert_array_equal(h.cpu().numpy(), exp["history"])
+    bsq.sync_status()
+
+
+def test_delayed_nvfp4_consecutive_steps(bsq):
+    # three steps on different tensors share one history in stream order
+    import torch
+    hist = np.zeros(16, np.float32)
+    h = torch.from_numpy(hist.copy()).cuda()
+    for step, scale in enumerate((1.0, 8.0, 0.25)):
+        x = inputs.normal_bf16((128, 256), 20 + step, std=scale)
+        row, _ = bsq.quantize_nvfp4_delayed(dev_bf16(x), h, "row")
+        exp = oracle.nvfp4_delayed_quantize(x, hist, "row")
+        _check_delayed(row, *exp["row"], exp["s_t"], f"step {step}")
+        hist = exp["history"]
+        np.testing.assert_array_equal(h.cpu().numpy(), hist)
+    assert hist[0] == np.float32(_abs_max(x))
+
+
+def test_delayed_nvfp4_saturates(bsq):
+    import torch
+    x = inputs.normal_bf16((64, 256), 30)
+    hist0 = np.float32([_abs_max(x) / 64.0] + [0.0] * 15)
+    h = torch.from_numpy(hist0.copy()).cuda()
+    row, _ = bsq.quantize_nvfp4_delayed(dev_bf16(x), h, "row")
+    exp = oracle.nvfp4_delayed_quantize(x, hist0, "row")
+    _check_delayed(row, *exp["row"], exp["s_t"], "saturating")
+    v = bsq.dequantize(row, torch.float32).cpu().numpy()
+    assert np.abs(v).max() == np.float32(6.0 * 448.0 * exp["s_t"])
+
+
+def test_delayed_nvfp4_full_size_equals_just_in_time(bsq):
+    # config 4's X (8192 x 4096): with its own amax in the history the one-pass
+    # delayed path gives the two-pass result exactly
+    import torch
+    X = inputs.nvfp4_forward()["X"]
+    xd = dev_bf16(X)
+    jit, _ = bsq.quantize(xd, "nvfp4", "row")
+    h = torch.zeros(16, dtype=torch.float32, device="cuda")
+    h[3] = oracle.tensor_amax(X)
+    dl, _ = bsq.quantize_nvfp4_delayed(xd, h, "row")
+    assert torch.equal(jit.codes, dl.codes) and torch.equal(jit.scales, dl.scales)
+    assert torch.equal(jit.tensor_scale, dl.tensor_scale)
+    assert float(h[0]) == oracle.tensor_amax(X) and float(h[4]) == oracle.tensor_amax(X) and float(h[3]) == 0.0
+    bsq.sync_status()
+
+
+def test_delayed_nvfp4_empty_history_unit_scale(bsq):
+    import torch
+    x = inputs.normal_bf16((32, 64), 31)
+    h = torch.zeros(16, dtype=torch.float32, device="cuda")
+    row, _ = bsq.quantize_nvfp4_delayed(dev_bf16(x), h, "row")
+    assert float(row.tensor_scale.cpu()[0]) == 1.0
+    c, s, _ = oracle.nvfp4_quantize_rows(x, 1.0)
+    _check_delayed(row, c, s, 1.0, "unit scale")
