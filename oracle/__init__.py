@@ -96,6 +96,8 @@ def _load():
     lib.bsqo_nvfp4_dequant_rows.argtypes = [p, p, ctypes.c_float, c_i64, c_i64, p]
     lib.bsqo_mxfp4_to_mxfp8_rows.restype = None
     lib.bsqo_mxfp4_to_mxfp8_rows.argtypes = [p, p, c_i64, c_i64, p, p]
+    lib.bsqo_mxfp4_row_to_mxfp8_col.restype = None
+    lib.bsqo_mxfp4_row_to_mxfp8_col.argtypes = [p, p, c_i64, c_i64, p, p]
     lib.bsqo_gemm_pairs.restype = None
     lib.bsqo_gemm_pairs.argtypes = [p, p, c_i64, p, p, c_i64, p, p]
     lib.bsqo_gemm_full.restype = None
@@ -322,6 +324,20 @@ def mxfp4_to_mxfp8_rows(codes4: np.ndarray, scales4: np.ndarray):
 
 
 # ------------------------------------------------------------------- GEMM
+def mxfp4_row_to_mxfp8_col(codes4: np.ndarray, scales4: np.ndarray):
+    """FP4RowToFP8Col: MXFP8 E4M3 column-wise quantization of the exactly
+    dequantized MXFP4 matrix (codes [R, C] unpacked, scales [R, C/32]).
+    Returns (codes [C, R], scales [C, R/32]) of the transpose."""
+    c4 = np.ascontiguousarray(codes4, dtype=np.uint8)
+    s4 = np.ascontiguousarray(scales4, dtype=np.uint8)
+    R, C = c4.shape
+    assert R % 32 == 0 and C % 32 == 0 and s4.shape == (R, C // 32)
+    codes8 = np.empty((C, R), dtype=np.uint8)
+    scales8 = np.empty((C, R // 32), dtype=np.uint8)
+    _load().bsqo_mxfp4_row_to_mxfp8_col(_ptr(c4), _ptr(s4), R, C, _ptr(codes8), _ptr(scales8))
+    return codes8, scales8
+
+
 def gemm_pairs(A: np.ndarray, B: np.ndarray, ms, ns):
     """ref, mag for C[m, n] = sum_k A[m, k] B[n, k] at the given (m, n)."""
     A = np.ascontiguousarray(A, dtype=np.float64)

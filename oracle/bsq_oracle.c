@@ -339,6 +339,29 @@ void bsqo_mxfp4_to_mxfp8_rows(const uint8_t* codes4, const uint8_t* scales4, int
  * [M][K] and [N][K].  For each requested (m, n) pair it returns
  * ref = sum_k a*b and mag = sum_k |a*b| in FP64.
  * ------------------------------------------------------------------- */
+/* FP4RowToFP8Col ("Practical FP4 Training for Large-Scale MoE Models on
+ * Hopper GPUs", section 2, "Kernels": dequantize, transpose and
+ * re-quantize column-wise in one step, for the weight gradient).  Reading:
+ * the MXFP8 E4M3 quantization, blocks of 32 along the rows, of the exactly
+ * dequantized MXFP4 matrix, stored transposed.
+ *   in:  codes4 [R, C] (one E2M1 code per byte), scales4 [R, C/32] (E8M0)
+ *   out: codes8 [C, R] (E4M3), scales8 [C, R/32] (E8M0); R % 32 == 0. */
+void bsqo_mxfp4_row_to_mxfp8_col(const uint8_t* codes4, const uint8_t* scales4, int64_t R, int64_t C,
+                                 uint8_t* codes8, uint8_t* scales8)
+{
+    int64_t c, j;
+    int i;
+    double v[32];
+    for (c = 0; c < C; c++)
+        for (j = 0; j < R / 32; j++) {
+            for (i = 0; i < 32; i++) {
+                const int64_t r = j * 32 + i;
+                v[i] = bsqo_decode(O_E2M1, codes4[r * C + c]) * bsqo_decode_e8m0(scales4[r * (C / 32) + c / 32]);
+            }
+            bsqo_mx_block(O_E4M3, v, 32, codes8 + c * R + j * 32, scales8 + c * (R / 32) + j);
+        }
+}
+
 void bsqo_gemm_pairs(const double* A, const double* B, int64_t K,
                      const int64_t* ms, const int64_t* ns, int64_t npairs,
                      double* ref, double* mag)

@@ -420,3 +420,51 @@ def test_delayed_empty_history_uses_unit_scale():
     c, s, _ = oracle.nvfp4_quantize_rows(x, 1.0)
     np.testing.assert_array_equal(d["row"][0], c)
     np.testing.assert_array_equal(d["row"][1], s)
+
+
+# ------------------------------------------------------------ FP4RowToFP8Col
+def _bf16_bits_of_exact(v):
+    """Exact doubles that BF16 represents -> BF16 bit patterns (asserts exactness)."""
+    f = np.asarray(v, np.float64).astype(np.float32)
+    assert np.array_equal(f.astype(np.float64), v)
+    bits = (f.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(((bits.astype(np.uint32) << 16).view(np.float32)).astype(np.float64), v)
+    return bits
+
+
+def test_fp4_row_to_fp8_col_equals_column_quantize_of_dequant():
+    # MXFP4 made from BF16 data dequantizes to values BF16 holds exactly, so the
+    # fused step must equal the (separately pinned) column-wise E4M3 quantize of
+    # those values
+    for seed, shape in ((40, (64, 96)), (41, (128, 64)), (42, (96, 256))):
+        x = inputs.outlier_activations_bf16(shape, seed)
+        c4, s4 = oracle.mx_quantize_rows(x, "mxfp4")
+        v = oracle.dequant_rows(c4, s4, "mxfp4")
+        cc, sc, _ = oracle.quantize_cols(_bf16_bits_of_exact(v), "mxfp8_e4m3")
+        c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
+        np.testing.assert_array_equal(c8, cc)
+        np.testing.assert_array_equal(s8, sc)
+
+
+def test_fp4_row_to_fp8_col_lossless_with_uniform_row_scales():
+    # one E8M0 scale for every row of a column block: every value is an E2M1
+    # value times that scale, which E4M3 holds exactly after the re-scale
+    rng = np.random.default_rng(43)
+    R, C = 64, 64
+    c4 = rng.integers(0, 16, (R, C)).astype(np.uint8)
+    s4 = np.full((R, C // 32), 120, np.uint8)
+    c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
+    v4 = oracle.dequant_rows(c4, s4, "mxfp4")
+    v8 = oracle.dequant_rows(c8, s8, "mxfp8_e4m3")
+    np.testing.assert_array_equal(v8, v4.T)
+
+
+def test_fp4_row_to_fp8_col_nan_scale_and_zero_block():
+    c4 = np.zeros((64, 32), np.uint8)
+    c4[40, 5] = 0x7                       # 6.0 in the second row block
+    s4 = np.full((64, 1), 127, np.uint8)
+    s4[3, 0] = 0xFF                       # NaN scale on row 3: first row block of every column
+    c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
+    assert (s8[:, 0] == 0xFF).all() and (c8[:, :32] == 0x7F).all()
+    assert (s8[:, 1][np.arange(32) != 5] == 0).all()      # all-zero blocks: scale 2^-127
+    assert s8[5, 1] == 127 + 2 - 8 and c8[5, 40] == oracle.encode(E4M3, 6.0 * 2.0 ** 6)
