@@ -188,6 +188,12 @@ class Step:
         # scaling, one pass (2.5625 B per element), the amax history holding
         # the tensor's own amax as in steady state.
         self.extra_ops = []
+        if "moe" in want:
+            # NEXT-1: FP4RowToFP8Col of the MoE activations (the wgrad operand),
+            # from the MXFP4 rows the step produced; read 0.53125 + write 1.03125 B
+            o["A8c"] = E("mxfp8_e4m3", m["K"], m["rows"])
+            self.extra_ops.append(("fp4row->fp8col A_moe", "NEXT-1", "repack",
+                                   lambda: bsq.mxfp4_to_mxfp8_col_into(o["A4"], o["A8c"]), mn * B_REPACK, 0, 1))
         if "nv" in want:
             B_NV1 = 2 + 0.5 + 1 / 16
             qd = bsq.quantize_nvfp4_delayed_into
@@ -202,7 +208,7 @@ class Step:
             o["X42d"] = E("nvfp4", n["M"], n["K2"])
             o["W42d"] = E("nvfp4", n["N"], n["K2"])
             hs = self.hist
-            self.extra_ops = [
+            self.extra_ops += [
                 ("quant X nvfp4 delayed", "NEXT-3", "quant", lambda: qd(i["X4"], "row", o["X4d"], None, hs["X4"]),
                  n["M"] * n["K"] * B_NV1, 0, 2),
                 ("quant W nvfp4 delayed", "NEXT-3", "quant", lambda: qd(i["W4"], "row", o["W4d"], None, hs["W4"]),

@@ -66,6 +66,7 @@ def lib():
         "bsq_gemm": (i32, [PT, PT, vp, i32, vp]),
         "bsq_grouped_gemm": (i32, [PT, vp, i32, PT, vp, i32, vp]),
         "bsq_mxfp4_to_mxfp8": (i32, [PT, PT, vp]),
+        "bsq_mxfp4_to_mxfp8_col": (i32, [PT, PT, vp]),
         "bsq_sync_status": (i32, [vp]),
         "bsq_debug_timeout_probe": (i32, [ctypes.c_uint64, vp]),
         "bsq_status_string": (ctypes.c_char_p, [i32]),
@@ -247,6 +248,18 @@ def mxfp4_to_mxfp8_into(q: QTensor, out: QTensor, stream=None):
 def mxfp4_to_mxfp8(q: QTensor, stream=None) -> QTensor:
     out = empty(MXFP8_E4M3, q.rows, q.cols, q.codes.device)
     return mxfp4_to_mxfp8_into(q, out, stream)
+
+
+def mxfp4_to_mxfp8_col_into(q: QTensor, out: QTensor, stream=None):
+    ci, co = q.c(), out.c()
+    _check(lib().bsq_mxfp4_to_mxfp8_col(ctypes.byref(ci), ctypes.byref(co), _stream(stream)), "bsq_mxfp4_to_mxfp8_col")
+
+
+def mxfp4_to_mxfp8_col(q: QTensor, stream=None) -> QTensor:
+    """FP4RowToFP8Col: [R, C] MXFP4 (row-wise) -> [C, R] MXFP8 E4M3 of the transpose."""
+    out = empty("mxfp8_e4m3", q.cols, q.rows, q.codes.device)
+    mxfp4_to_mxfp8_col_into(q, out, stream)
+    return out
 
 
 def sync_status(stream=None):

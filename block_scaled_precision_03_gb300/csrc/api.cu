@@ -282,6 +282,26 @@ bsq_status bsq_mxfp4_to_mxfp8(const bsq_tensor* in, bsq_tensor* out, void* strea
     return from_cuda(bsq::run_repack(a, static_cast<cudaStream_t>(stream)));
 }
 
+bsq_status bsq_mxfp4_to_mxfp8_col(const bsq_tensor* in, bsq_tensor* out, void* stream) {
+    bsq_status s = check_tensor(in, false);
+    if (s != BSQ_OK) return s;
+    if ((s = check_tensor(out, false)) != BSQ_OK) return s;
+    if (in->fmt != BSQ_MXFP4_E2M1 || out->fmt != BSQ_MXFP8_E4M3) return BSQ_ERR_UNSUPPORTED;
+    if (out->rows != in->cols || out->cols != in->rows) return BSQ_ERR_INVALID_ARG;
+    if (in->rows % 32 || in->cols % 32) return BSQ_ERR_INVALID_ARG;
+    bsq::RepackArgs a{};
+    a.in_codes = static_cast<const uint8_t*>(in->codes);
+    a.in_scales = in->scales;
+    a.out_codes = static_cast<uint8_t*>(out->codes);
+    a.out_scales = out->scales;
+    a.rows = in->rows;
+    a.cols = in->cols;
+    a.scales_bytes = scales_bytes(BSQ_MXFP8_E4M3, out->rows, out->cols);
+    a.scales_pad = scales_padded(BSQ_MXFP8_E4M3, out->rows, out->cols);
+    a.num_sms = num_sms();
+    return from_cuda(bsq::run_repack_col(a, static_cast<cudaStream_t>(stream)));
+}
+
 bsq_status bsq_sync_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return BSQ_ERR_CUDA;

@@ -100,6 +100,118 @@ cudaError_t run_repack(const RepackArgs& a, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------------------
+// FP4RowToFP8Col (same page and section, kernel FP4RowToFP8Col): dequantize,
+// transpose and re-quantize column-wise to MXFP8 E4M3 in one pass, without a
+// BF16 intermediate.  An E2M1 magnitude index m = 1..7 is a * 2^b with
+// (a, b) = (1,-1) (1,0) (3,-1) (1,1) (3,0) (1,2) (3,1); under the row scale
+// byte s its value is a * 2^(b + s - 127), whose floor(log2) is
+// b + [a == 3] + s - 127.  A 32-row block of one column takes the E8M0
+// exponent e = clamp(max floor(log2) - 8, -127, 127) (the MX rule with
+// E4M3's largest exponent 8; -127 for an all-zero block), each element
+// a * 2^(b + s - 127 - e) is built as an exact FP32 value and rounded once
+// by the hardware E4M3 conversion; a NaN row scale (0xFF) in the block
+// makes the block NaN.  Tiles of 128 input rows x 128 input columns: the
+// codes (8 KB) and the one 512-byte scale tile that covers them are staged
+// in shared memory; a thread encodes two (column, 32-row block) pairs.
+// ---------------------------------------------------------------------------
+constexpr int kColTile = 128;
+constexpr int kColThreads = 256;
+
+// (log2 floor + 1) and b of the E2M1 magnitudes, 4 bits each (index m)
+constexpr uint32_t kLg1 = 0x33221100u;      // m: 0..7 -> 0,0,1,1,2,2,3,3
+constexpr uint32_t kBexp = 0x23120100u;     // b + 1: m 1..7 -> 0,1,0,2,1,3,2 (m = 0 unused)
+
+__device__ __forceinline__ float e2m1_scaled(uint32_t n, int s_minus_e) {
+    const uint32_t m = n & 7u;
+    float v = 0.0f;
+    if (m) {
+        const int t = (int)((kBexp >> (4 * m)) & 0xFu) - 1 + s_minus_e;     // value = a * 2^t
+        const bool three = (m & 1u) && m > 1;                              // m = 3, 5, 7: a = 3
+        const int ex = three ? t + 1 : t;                                  // 3 * 2^t = 1.5 * 2^(t+1)
+        if (ex >= -126) v = __uint_as_float(((uint32_t)(ex + 127) << 23) | (three ? 0x400000u : 0u));
+    }
+    return (n & 8u) ? -v : v;
+}
+
+__global__ void __launch_bounds__(kColThreads)
+repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ sin, int64_t R, int64_t C,
+                  int64_t s_tiles_in, uint8_t* __restrict__ out, uint8_t* __restrict__ sout, int64_t s_tiles_out) {
+    __shared__ __align__(16) uint32_t codes[kColTile * 16];     // 128 rows x 64 bytes
+    __shared__ __align__(16) uint8_t sf[512];                   // row scales: the 128x4 tile
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.y * kColTile, c0 = (int64_t)blockIdx.x * kColTile;
+    // codes: 128 rows x 4 chunks of 16 bytes (32 columns each)
+#pragma unroll
+    for (int k = 0; k < 2; k++) {
+        const int idx = tid + k * kColThreads, rr = idx >> 2, ch = idx & 3;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r0 + rr < R && c0 + 32 * ch < C)
+            v = *reinterpret_cast<const uint4*>(in + (r0 + rr) * (C / 2) + c0 / 2 + 16 * ch);
+        *reinterpret_cast<uint4*>(&codes[rr * 16 + ch * 4]) = v;
+    }
+    if (tid < 32)
+        *reinterpret_cast<uint4*>(&sf[tid * 16]) =
+            *reinterpret_cast<const uint4*>(sin + ((r0 / 128) * s_tiles_in + c0 / 128) * 512 + tid * 16);
+    __syncthreads();
+#pragma unroll 1
+    for (int id = tid; id < kColTile * 4; id += kColThreads) {
+        const int c = id & (kColTile - 1), j = id >> 7, cb = c >> 5;
+        if (c0 + c >= C || r0 + 32 * j >= R) continue;
+        const int sh = (c & 7) * 4;
+        // pass 1: block exponent (largest floor(log2)) and NaN
+        int emax = -1;
+        bool nan = false;
+#pragma unroll 8
+        for (int i = 0; i < 32; i++) {
+            const uint32_t n = (codes[(32 * j + i) * 16 + (c >> 3)] >> sh) & 0xFu;
+            const uint32_t sr = sf[i * 16 + j * 4 + cb];
+            nan |= sr == 0xFFu;
+            if (n & 7u) emax = max(emax, (int)((kLg1 >> (4 * (n & 7u))) & 0xFu) + (int)sr);
+        }
+        uint32_t w[8];
+        uint32_t sbyte;
+        if (nan) {
+            sbyte = 0xFF;
+#pragma unroll
+            for (int q = 0; q < 8; q++) w[q] = 0x7F7F7F7Fu;
+        } else {
+            // floor(log2 amax) = emax - 1 - 127; e = that - 8, clamped; no nonzero: -127
+            const int e = emax < 0 ? -127 : min(max(emax - 136, -127), 127);
+            sbyte = (uint32_t)(e + 127);
+            // pass 2: encode a * 2^(b + s - 127 - e)
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                uint32_t pk[2];
+#pragma unroll
+                for (int h = 0; h < 2; h++) {
+                    const int i0 = 4 * q + 2 * h;
+                    const uint32_t n0 = (codes[(32 * j + i0) * 16 + (c >> 3)] >> sh) & 0xFu;
+                    const uint32_t n1 = (codes[(32 * j + i0 + 1) * 16 + (c >> 3)] >> sh) & 0xFu;
+                    const int s0 = (int)sf[i0 * 16 + j * 4 + cb] - 127 - e;
+                    const int s1 = (int)sf[(i0 + 1) * 16 + j * 4 + cb] - 127 - e;
+                    pk[h] = cvt_e4m3x2(e2m1_scaled(n0, s0), e2m1_scaled(n1, s1));
+                }
+                w[q] = pk[0] | (pk[1] << 16);
+            }
+        }
+        uint8_t* dst = out + (c0 + c) * R + r0 + 32 * j;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        sout[sf_offset(c0 + c, r0 / 32 + j, s_tiles_out)] = (uint8_t)sbyte;
+    }
+}
+
+cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st) {
+    cudaError_t e;
+    if (a.scales_pad && (e = cudaMemsetAsync(a.out_scales, 0, a.scales_bytes, st)) != cudaSuccess) return e;
+    const int64_t R = a.rows, C = a.cols;
+    dim3 grid((unsigned)((C + kColTile - 1) / kColTile), (unsigned)((R + kColTile - 1) / kColTile));
+    repack_col_kernel<<<grid, kColThreads, 0, st>>>(a.in_codes, a.in_scales, R, C, (C / 32 + 3) / 4, a.out_codes,
+                                                   a.out_scales, (R / 32 + 3) / 4);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Dequantize: value = code * scale (* tensor scale), rounded once.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float e5m2_to_float(uint32_t b) {

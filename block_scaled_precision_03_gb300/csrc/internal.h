@@ -30,6 +30,8 @@ struct RepackArgs {
     int num_sms;
 };
 cudaError_t run_repack(const RepackArgs& a, cudaStream_t st);
+// FP4RowToFP8Col: rows, cols = the MXFP4 input's; the output is [cols, rows]
+cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st);
 
 struct DequantArgs {
     int fmt;

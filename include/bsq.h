@@ -180,6 +180,19 @@ bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_de
  * FP4RowToFP8Row. */
 bsq_status bsq_mxfp4_to_mxfp8(const bsq_tensor* in_mxfp4, bsq_tensor* out_e4m3, void* stream);
 
+/* FP4RowToFP8Col: dequantize a row-wise MXFP4 tensor in[R, C], transpose and
+ * re-quantize column-wise to MXFP8 E4M3: out[C, R] holds the K-major codes
+ * of the transpose with E8M0 scales over 32-row blocks of each column.  The
+ * result equals the column-wise E4M3 MX quantization of the exactly
+ * dequantized input (computed in the integer domain, no BF16 or FP32
+ * intermediate that could round); a NaN row scale makes its blocks NaN.
+ * R % 32 == 0 and C % 32 == 0; out->rows == C, out->cols == R; buffers as
+ * for bsq_mxfp4_to_mxfp8 (device, caller-owned, 16-byte aligned).
+ * Citation: MoE FP4 page section 2, "Kernels" (FP4RowToFP8Col: fused
+ * dequantization, transposition and requantization for the weight
+ * gradient). */
+bsq_status bsq_mxfp4_to_mxfp8_col(const bsq_tensor* in_mxfp4, bsq_tensor* out_e4m3, void* stream);
+
 /* Synchronize `stream`, read and clear the device status word, and return
  * BSQ_ERR_TIMEOUT if any kernel recorded a timed-out wait since the last
  * call, BSQ_ERR_CUDA if the stream reported an error, else BSQ_OK. */

@@ -104,3 +104,62 @@ def test_delayed_nvfp4_empty_history_unit_scale(bsq):
     assert float(row.tensor_scale.cpu()[0]) == 1.0
     c, s, _ = oracle.nvfp4_quantize_rows(x, 1.0)
     _check_delayed(row, c, s, 1.0, "unit scale")
+
+
+# ------------------------------------------------------------ FP4RowToFP8Col
+def _check_fp8col(out, codes8, scales8, what):
+    got_c = host_u8(out.codes).reshape(codes8.shape)
+    bad = np.argwhere(got_c != codes8)
+    assert len(bad) == 0, f"{what}: {len(bad)} code bytes differ, first at {tuple(bad[0])}"
+    assert np.array_equal(host_u8(out.scales), oracle.swizzle_scales(scales8)), f"{what}: scales differ"
+
+
+@pytest.mark.parametrize("shape", [(128, 128), (96, 160), (32, 32), (416, 4160), (4128, 96)])
+def test_fp4_row_to_fp8_col_random_codes_and_scales(bsq, shape):
+    # every nibble, scale bytes over the whole range including 0, 254 and NaN
+    from _util import upload_q
+    R, C = shape
+    rng = np.random.default_rng(R * 7 + C)
+    c4 = rng.integers(0, 16, (R, C)).astype(np.uint8)
+    s4 = rng.integers(0, 255, (R, C // 32)).astype(np.uint8)
+    s4[rng.random(s4.shape) < 0.01] = 0xFF
+    s4[0, 0], s4[-1, -1] = 0, 254
+    q4 = upload_q(bsq, "mxfp4", c4, s4)
+    out = bsq.mxfp4_to_mxfp8_col(q4)
+    c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
+    _check_fp8col(out, c8, s8, f"random {shape}")
+    bsq.sync_status()
+
+
+def test_fp4_row_to_fp8_col_from_bf16(bsq):
+    # the MoE path: BF16 activations -> MXFP4 rows (GPU) -> FP8 columns (GPU)
+    x = inputs.normal_bf16((1024, 7168), 50)
+    q4, _ = bsq.quantize(dev_bf16(x), "mxfp4", "row")
+    c4, s4 = oracle.mx_quantize_rows(x, "mxfp4")
+    out = bsq.mxfp4_to_mxfp8_col(q4)
+    c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
+    _check_fp8col(out, c8, s8, "from bf16")
+
+
+def test_fp4_row_to_fp8_col_full_size_sampled(bsq):
+    # config 5's activations (32768 x 7168); the oracle checks four whole
+    # 32-column groups (every row, every scale block of those columns)
+    d = inputs.moe_grouped()
+    A = d["A"]
+    q4, _ = bsq.quantize(dev_bf16(A), "mxfp4", "row")
+    out = bsq.mxfp4_to_mxfp8_col(q4)
+    rng = np.random.default_rng(51)
+    groups = np.sort(rng.choice(7168 // 32, size=4, replace=False))
+    S_out = 32768 // 32
+    codes_all = host_u8(out.codes).reshape(7168, 32768)
+    sc_buf = host_u8(out.scales)
+    for g in groups:
+        cols = np.arange(32 * g, 32 * g + 32)
+        c4, s4 = oracle.mx_quantize_rows(np.ascontiguousarray(A[:, cols]), "mxfp4")
+        c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
+        assert np.array_equal(codes_all[cols], c8), f"group {g}: codes differ"
+        r = cols[:, None]
+        cc = np.arange(S_out)[None, :]
+        off = ((r // 128) * (S_out // 4) + cc // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + cc % 4
+        assert np.array_equal(sc_buf[off], s8), f"group {g}: scales differ"
+    bsq.sync_status()
