@@ -114,98 +114,127 @@ cudaError_t run_repack(const RepackArgs& a, cudaStream_t st) {
 // codes (8 KB) and the one 512-byte scale tile that covers them are staged
 // in shared memory; a thread encodes two (column, 32-row block) pairs.
 // ---------------------------------------------------------------------------
-constexpr int kColTile = 128;
-constexpr int kColThreads = 256;
+constexpr int kColRows = 256;       // tile: 256 input rows x 128 input columns
+constexpr int kColCols = 128;
+constexpr int kColThreads = 256;    // one thread = 4 columns x one 32-row block
 
-// (log2 floor + 1) and b of the E2M1 magnitudes, 4 bits each (index m)
-constexpr uint32_t kLg1 = 0x33221100u;      // m: 0..7 -> 0,0,1,1,2,2,3,3
-constexpr uint32_t kBexp = 0x23120100u;     // b + 1: m 1..7 -> 0,1,0,2,1,3,2 (m = 0 unused)
+// b + 1 of the E2M1 magnitudes, 4 bits each (index m), for the exact path
+constexpr uint32_t kBexp = 0x23120100u;     // m 1..7 -> 0,1,0,2,1,3,2 (m = 0 unused)
 
+// Exact FP32 value a * 2^t of magnitude index m (sign from the nibble) with
+// t = b + s_minus_e; values below 2^-126 become 0 (E4M3 rounds them to 0).
 __device__ __forceinline__ float e2m1_scaled(uint32_t n, int s_minus_e) {
     const uint32_t m = n & 7u;
     float v = 0.0f;
     if (m) {
-        const int t = (int)((kBexp >> (4 * m)) & 0xFu) - 1 + s_minus_e;     // value = a * 2^t
-        const bool three = (m & 1u) && m > 1;                              // m = 3, 5, 7: a = 3
-        const int ex = three ? t + 1 : t;                                  // 3 * 2^t = 1.5 * 2^(t+1)
+        const int t = (int)((kBexp >> (4 * m)) & 0xFu) - 1 + s_minus_e;
+        const bool three = (m & 1u) && m > 1;                              // a = 3: 1.5 * 2^(t+1)
+        const int ex = three ? t + 1 : t;
         if (ex >= -126) v = __uint_as_float(((uint32_t)(ex + 127) << 23) | (three ? 0x400000u : 0u));
     }
     return (n & 8u) ? -v : v;
 }
 
+// E4M3 byte of nibble n with row scale byte sr in a block of scale byte sb.
+// For m = 1..7, floor(log2 |value|) + 1 = (m >> 1) + sr - 127, so the E4M3
+// exponent field is key - sb + 6 with key = (m >> 1) + sr, and the mantissa
+// field is 4 for m = 3, 5, 7 (a = 3) and 0 otherwise; a field below 1 means
+// E4M3's subnormal range, which the exact conversion handles.
+// the rare subnormal case, out of line to keep the unrolled loops small
+__device__ __noinline__ uint32_t fp8_of_nibble_exact(uint32_t n, int s_minus_e) {
+    return cvt_e4m3x2(e2m1_scaled(n, s_minus_e), 0.0f) & 0xFFu;
+}
+__device__ __forceinline__ uint32_t fp8_of_nibble(uint32_t n, uint32_t sr, uint32_t sb) {
+    const uint32_t m = n & 7u, sign = (n & 8u) << 4;
+    const int E = (int)(m >> 1) + (int)sr - (int)sb + 6;
+    const uint32_t normal = sign | ((uint32_t)E << 3) | (((m & 1u) && m > 1) ? 4u : 0u);
+    if (m == 0) return sign;
+    if (E >= 1) return normal;
+    return fp8_of_nibble_exact(n, (int)sr - (int)sb);
+}
+
 __global__ void __launch_bounds__(kColThreads)
 repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ sin, int64_t R, int64_t C,
                   int64_t s_tiles_in, uint8_t* __restrict__ out, uint8_t* __restrict__ sout, int64_t s_tiles_out) {
-    __shared__ __align__(16) uint32_t codes[kColTile * 16];     // 128 rows x 64 bytes
-    __shared__ __align__(16) uint8_t sf[512];                   // row scales: the 128x4 tile
+    __shared__ __align__(16) uint32_t codes[kColRows * 16];    // 256 rows x 64 bytes
+    __shared__ __align__(16) uint8_t sf[2 * 512];              // row scales: two 128x4 tiles
     const int tid = threadIdx.x;
-    const int64_t r0 = (int64_t)blockIdx.y * kColTile, c0 = (int64_t)blockIdx.x * kColTile;
-    // codes: 128 rows x 4 chunks of 16 bytes (32 columns each)
+    const int64_t r0 = (int64_t)blockIdx.y * kColRows, c0 = (int64_t)blockIdx.x * kColCols;
+    // codes: 256 rows x 4 chunks of 16 bytes (32 columns each)
 #pragma unroll
-    for (int k = 0; k < 2; k++) {
+    for (int k = 0; k < 4; k++) {
         const int idx = tid + k * kColThreads, rr = idx >> 2, ch = idx & 3;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (r0 + rr < R && c0 + 32 * ch < C)
             v = *reinterpret_cast<const uint4*>(in + (r0 + rr) * (C / 2) + c0 / 2 + 16 * ch);
         *reinterpret_cast<uint4*>(&codes[rr * 16 + ch * 4]) = v;
     }
-    if (tid < 32)
-        *reinterpret_cast<uint4*>(&sf[tid * 16]) =
-            *reinterpret_cast<const uint4*>(sin + ((r0 / 128) * s_tiles_in + c0 / 128) * 512 + tid * 16);
+    if (tid < 64) {
+        const int band = tid >> 5;          // 128-row band of the tile
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r0 + 128 * band < R)
+            v = *reinterpret_cast<const uint4*>(sin + ((r0 / 128 + band) * s_tiles_in + c0 / 128) * 512 + (tid & 31) * 16);
+        *reinterpret_cast<uint4*>(&sf[band * 512 + (tid & 31) * 16]) = v;
+    }
     __syncthreads();
-#pragma unroll 1
-    for (int id = tid; id < kColTile * 4; id += kColThreads) {
-        const int c = id & (kColTile - 1), j = id >> 7, cb = c >> 5;
-        if (c0 + c >= C || r0 + 32 * j >= R) continue;
-        const int sh = (c & 7) * 4;
-        // pass 1: block exponent (largest floor(log2)) and NaN
-        int emax = -1;
-        bool nan = false;
+    const int quad = tid & 31, rb = tid >> 5;           // columns 4 quad .. 4 quad + 3, rows 32 rb .. 32 rb + 31
+    const int c = 4 * quad, cb = c >> 5;
+    if (c0 + c >= C || r0 + 32 * rb >= R) return;
+    const int wi = c >> 3, sh = (c & 7) * 4;            // the word and bit offset of the 4 nibbles
+    const uint8_t* srow = sf + (rb >> 2) * 512 + (rb & 3) * 4 + cb;   // + i * 16 for row i of the block
+    // pass 1: per column the largest key (m >> 1) + sr over nonzero codes, and NaN rows
+    uint32_t kmax[4] = {0, 0, 0, 0};
+    bool nan = false;
 #pragma unroll 8
-        for (int i = 0; i < 32; i++) {
-            const uint32_t n = (codes[(32 * j + i) * 16 + (c >> 3)] >> sh) & 0xFu;
-            const uint32_t sr = sf[i * 16 + j * 4 + cb];
-            nan |= sr == 0xFFu;
-            if (n & 7u) emax = max(emax, (int)((kLg1 >> (4 * (n & 7u))) & 0xFu) + (int)sr);
+    for (int i = 0; i < 32; i++) {
+        const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
+        const uint32_t sr = srow[i * 16];
+        nan |= sr == 0xFFu;
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint32_t m = (nb >> (4 * k)) & 7u;
+            if (m) kmax[k] = max(kmax[k], (m >> 1) + sr);
         }
-        uint32_t w[8];
-        uint32_t sbyte;
-        if (nan) {
-            sbyte = 0xFF;
+    }
+    // scale bytes: floor(log2 amax) = key - 128, e = that - 8 clamped to [-127, 127]
+    uint32_t sb[4];
 #pragma unroll
-            for (int q = 0; q < 8; q++) w[q] = 0x7F7F7F7Fu;
-        } else {
-            // floor(log2 amax) = emax - 1 - 127; e = that - 8, clamped; no nonzero: -127
-            const int e = emax < 0 ? -127 : min(max(emax - 136, -127), 127);
-            sbyte = (uint32_t)(e + 127);
-            // pass 2: encode a * 2^(b + s - 127 - e)
+    for (int k = 0; k < 4; k++)
+        sb[k] = nan ? 0xFFu : (kmax[k] == 0 ? 0u : (uint32_t)min(max((int)kmax[k] - 9, 0), 254));
+    // pass 2: encode 8 rows at a time, 8 bytes per column per step
+    const int ncols = C - (c0 + c) < 4 ? (int)(C - (c0 + c)) : 4;
+    uint8_t* dst0 = out + (c0 + c) * R + r0 + 32 * rb;
+#pragma unroll 1
+    for (int q = 0; q < 4; q++) {
+        uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                uint32_t pk[2];
+        for (int h = 0; h < 8; h++) {
+            const int i = 8 * q + h;
+            const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
+            const uint32_t sr = srow[i * 16];
 #pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int i0 = 4 * q + 2 * h;
-                    const uint32_t n0 = (codes[(32 * j + i0) * 16 + (c >> 3)] >> sh) & 0xFu;
-                    const uint32_t n1 = (codes[(32 * j + i0 + 1) * 16 + (c >> 3)] >> sh) & 0xFu;
-                    const int s0 = (int)sf[i0 * 16 + j * 4 + cb] - 127 - e;
-                    const int s1 = (int)sf[(i0 + 1) * 16 + j * 4 + cb] - 127 - e;
-                    pk[h] = cvt_e4m3x2(e2m1_scaled(n0, s0), e2m1_scaled(n1, s1));
-                }
-                w[q] = pk[0] | (pk[1] << 16);
+            for (int k = 0; k < 4; k++) {
+                const uint32_t b = fp8_of_nibble((nb >> (4 * k)) & 0xFu, sr, sb[k]) << (8 * (h & 3));
+                if (h < 4) lo[k] |= b;
+                else hi[k] |= b;
             }
         }
-        uint8_t* dst = out + (c0 + c) * R + r0 + 32 * j;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-        sout[sf_offset(c0 + c, r0 / 32 + j, s_tiles_out)] = (uint8_t)sbyte;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            if (k < ncols)
+                *reinterpret_cast<uint2*>(dst0 + (int64_t)k * R + 8 * q) =
+                    nan ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu) : make_uint2(lo[k], hi[k]);
     }
+#pragma unroll
+    for (int k = 0; k < 4; k++)
+        if (k < ncols) sout[sf_offset(c0 + c + k, r0 / 32 + rb, s_tiles_out)] = (uint8_t)sb[k];
 }
 
 cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st) {
     cudaError_t e;
     if (a.scales_pad && (e = cudaMemsetAsync(a.out_scales, 0, a.scales_bytes, st)) != cudaSuccess) return e;
     const int64_t R = a.rows, C = a.cols;
-    dim3 grid((unsigned)((C + kColTile - 1) / kColTile), (unsigned)((R + kColTile - 1) / kColTile));
+    dim3 grid((unsigned)((C + kColCols - 1) / kColCols), (unsigned)((R + kColRows - 1) / kColRows));
     repack_col_kernel<<<grid, kColThreads, 0, st>>>(a.in_codes, a.in_scales, R, C, (C / 32 + 3) / 4, a.out_codes,
                                                    a.out_scales, (R / 32 + 3) / 4);
     return cudaGetLastError();
