@@ -194,6 +194,18 @@ class Step:
             o["A8c"] = E("mxfp8_e4m3", m["K"], m["rows"])
             self.extra_ops.append(("fp4row->fp8col A_moe", "NEXT-1", "repack",
                                    lambda: bsq.mxfp4_to_mxfp8_col_into(o["A4"], o["A8c"]), mn * B_REPACK, 0, 1))
+            # NEXT-4: the MoE GEMM on MXFP4 x MXFP4 natively (weights quantized to
+            # MXFP4 as well), against the step's repack + MXFP8 grouped GEMM
+            o["Wm4"] = E("mxfp4", m["experts"] * m["N"], m["K"])
+            o["Ym4"] = torch.empty((m["rows"], m["N"]), dtype=torch.bfloat16, device="cuda")
+            self.wm4_groups = bsq.group_views(o["Wm4"], m["experts"])
+            self.extra_ops += [
+                ("quant W_moe mxfp4 row", "NEXT-4", "quant", lambda: q(i["W_moe"], "mxfp4", "row", o["Wm4"], None),
+                 m["experts"] * m["N"] * m["K"] * B_ROW4, 0, 1),
+                ("grouped gemm moe mxfp4", "NEXT-4", "gemm4", lambda: bsq.grouped_gemm_into(o["A4"], self.offsets,
+                                                                                           self.wm4_groups, o["Ym4"]),
+                 0, 2 * m["rows"] * m["N"] * m["K"], 1),
+            ]
         if "nv" in want:
             B_NV1 = 2 + 0.5 + 1 / 16
             qd = bsq.quantize_nvfp4_delayed_into
@@ -517,9 +529,14 @@ def main():
         torch.cuda.synchronize()
         for j, (name, row, kind, _, nbytes, flops, nk) in enumerate(step.extra_ops):
             ms = statistics.mean(xev[r][j][0].elapsed_time(xev[r][j][1]) for r in range(reps))
-            ach = nbytes / (ms * 1e-3) / 1e9
-            rows_next[name] = {"row": row, "ms": round(ms, 4), "gbs": round(ach, 1),
-                               "frac": round(ach / pk["hbm_gbs"], 4), "frac_spec_8tbs": round(ach / 8000.0, 4)}
+            if flops:
+                ach = flops / (ms * 1e-3) / 1e12
+                peak = pk["fp4_tflops"] if kind == "gemm4" else pk["fp8_tflops"]
+                rows_next[name] = {"row": row, "ms": round(ms, 4), "tflops": round(ach, 1), "frac": round(ach / peak, 4)}
+            else:
+                ach = nbytes / (ms * 1e-3) / 1e9
+                rows_next[name] = {"row": row, "ms": round(ms, 4), "gbs": round(ach, 1),
+                                   "frac": round(ach / pk["hbm_gbs"], 4), "frac_spec_8tbs": round(ach / 8000.0, 4)}
     q_ms, q_bytes = agg["quant"][0] + agg["repack"][0], agg["quant"][1] + agg["repack"][1]
     g8_ms, g8_fl = agg["gemm8"][0], agg["gemm8"][2]
     g4_ms, g4_fl = agg["gemm4"][0], agg["gemm4"][2]

@@ -184,6 +184,7 @@ static bsq_status check_gemm_pair(const bsq_tensor* A, const bsq_tensor* B) {
     const bool b8 = B->fmt == BSQ_MXFP8_E4M3 || B->fmt == BSQ_MXFP8_E5M2;
     if (a8 && b8) return BSQ_OK;
     if (A->fmt == BSQ_NVFP4_E2M1 && B->fmt == BSQ_NVFP4_E2M1) return BSQ_OK;
+    if (A->fmt == BSQ_MXFP4_E2M1 && B->fmt == BSQ_MXFP4_E2M1) return BSQ_OK;
     return BSQ_ERR_UNSUPPORTED;
 }
 
@@ -228,7 +229,7 @@ bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_de
     if (!al16(C)) return BSQ_ERR_ALIGNMENT;
     const bsq_tensor& b0 = B_groups[0];
     const size_t gbytes = codes_bytes(b0.fmt, b0.rows, b0.cols);
-    static const uint8_t* sf[bsq::kMaxGroups];
+    const uint8_t* sf[bsq::kMaxGroups];
     for (int g = 0; g < num_groups; g++) {
         const bsq_tensor& bg = B_groups[g];
         if ((s = check_tensor(&bg, false)) != BSQ_OK) return s;
@@ -260,6 +261,9 @@ bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_de
     a.num_sms = num_sms();
     a.status = st;
     a.timeout_ns = kDefaultTimeoutNs;
+    // MXFP4 runs on the CTA-pair kernel only, which spans the experts' scales
+    // with one tensor map: they must be evenly spaced (as group views are)
+    if (A->fmt == BSQ_MXFP4_E2M1 && !bsq::gemm_pair_grouped_ok(a)) return BSQ_ERR_UNSUPPORTED;
     return from_cuda(bsq::run_gemm(a, static_cast<cudaStream_t>(stream)));
 }
 

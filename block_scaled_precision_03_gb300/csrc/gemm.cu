@@ -252,8 +252,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
                 const uint64_t ad = ad_base + (uint64_t)((st * A_BYTES) >> 4) + 2 * m;
                 const uint64_t bd = bd_base + (uint64_t)((st * B_BYTES) >> 4) + 2 * m;
-                if (FP4) mma<1, true>(tmem, ad, bd, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
-                else mma<1, false>(tmem, ad, bd, p.idesc | ((uint32_t)m << 4) | ((uint32_t)m << 29), sfa_t, sfb_t, acc);
+                if (FP4) mma<1, kMmaNV>(tmem, ad, bd, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
+                else mma<1, kMmaFP8>(tmem, ad, bd, p.idesc | ((uint32_t)m << 4) | ((uint32_t)m << 29), sfa_t, sfb_t, acc);
             };
             int stage = 0;
             uint32_t phase = 0;
@@ -394,6 +394,8 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st) {
     // tile idle per expert, against a quarter of a 256-row span for the
     // 128-row tiles of the single-CTA kernel.
     constexpr int64_t kPairRowsPerGroup = 1024;
+    // MXFP4 x MXFP4 exists only on the CTA-pair kernel (kind::mxf4)
+    if (a.fmt_a == kMXFP4) return run_gemm_pair(a, st);
     if (!a.single_cta) {
         if (a.num_groups == 0) return run_gemm_pair(a, st);
         if (gemm_pair_grouped_ok(a) && (a.grouped_pair || a.M >= kPairRowsPerGroup * a.num_groups))

@@ -57,14 +57,22 @@ struct GroupTable2 {
 };
 constexpr int kGroupTableBytes = (int)sizeof(GroupTable2);
 
-template <bool FP4>
+// Operand kinds: MXFP8 (E4M3 / E5M2), NVFP4, MXFP4 (E2M1 with UE8M0 scales
+// per 32, the MoE page's activation format, multiplied natively).
+constexpr int kKindFP8 = tc::kMmaFP8, kKindNV = tc::kMmaNV, kKindMX4 = tc::kMmaMX4;
+
+template <int KIND>
 struct Cfg2 {
-    // KSUB 128-byte K sub-steps per stage: more MMAs per barrier handshake
+    static constexpr bool FP4 = KIND != kKindFP8;
+    // KSUB 128-byte K sub-steps per stage: more MMAs per barrier handshake.
+    // FP4 stages stay at 128 bytes: the scales of a 256-byte MXFP4 stage
+    // (6 KB) would not leave room for three stages and the epilogue.
     static constexpr int KSUB = FP4 ? 1 : 2;
     static constexpr int STAGES = FP4 ? 5 : 3;
     static constexpr int MPS = 4 * KSUB;                  // MMAs per stage
     static constexpr int OP_BYTES = KSUB * HALF;          // one CTA's A (or B) bytes per stage
-    static constexpr int SF_ATOMS = KSUB * (FP4 ? 4 : 1); // 512-byte scale atoms per 128 rows per stage
+    // 512-byte scale atoms (4 scale columns x 128 rows) per 128 rows per stage
+    static constexpr int SF_ATOMS = KSUB * (KIND == kKindNV ? 4 : (KIND == kKindMX4 ? 2 : 1));
     static constexpr int SFA_BYTES = SF_ATOMS * 512;
     static constexpr int SFB_BYTES = 2 * SF_ATOMS * 512;
     static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
@@ -155,12 +163,12 @@ __device__ __forceinline__ Tile2 tile2(const Params2& p, int t, const GroupTable
     return ti;
 }
 
-template <bool FP4>
+template <int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params2 p) {
-    using CF = Cfg2<FP4>;
+    using CF = Cfg2<KIND>;
     constexpr int S = CF::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -290,6 +298,22 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                 else tc::cp_sf<2>(sfb_t + 8 * a + 4 * (part - 1),
                                   sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + a) * 512) >> 4));
             };
+            // MMA m of a stage: FP8 takes scale byte k of the sub-step's atom
+            // (1X), NVFP4 one atom per MMA (4X), MXFP4 the byte pair 2 (m & 1)
+            // of atom m >> 1 (2X)
+            auto issue_mma = [&](int m, uint64_t adm, uint64_t bdm, uint32_t sfa_t, uint32_t sfb_t, uint32_t acc) {
+                const int sub = m >> 2, k = m & 3;
+                if (KIND == kKindNV) {
+                    tc::mma<2, tc::kMmaNV>(tmem, adm, bdm, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
+                } else if (KIND == kKindMX4) {
+                    const uint32_t id = (uint32_t)(m & 1) * 2u;
+                    tc::mma<2, tc::kMmaMX4>(tmem, adm, bdm, p.idesc | (id << 4) | (id << 29), sfa_t + 4 * (m >> 1),
+                                            sfb_t + 8 * (m >> 1), acc);
+                } else {
+                    tc::mma<2, tc::kMmaFP8>(tmem, adm, bdm, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29),
+                                            sfa_t + 4 * sub, sfb_t + 8 * sub, acc);
+                }
+            };
             int stage = 0;
             uint32_t phase = 0;
             int iter = 0;
@@ -324,11 +348,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                             const int sub = m >> 2, k = m & 3;
                             const uint64_t adm = ad + sub * SUB_STEP + 2 * k, bdm = bd + sub * SUB_STEP + 2 * k;
                             const uint32_t acc = m == 0 ? (uint32_t)(kb != 0) : 1u;
-                            if (FP4)
-                                tc::mma<2, true>(tmem, adm, bdm, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
-                            else
-                                tc::mma<2, false>(tmem, adm, bdm, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29),
-                                                  sfa_t + 4 * sub, sfb_t + 8 * sub, acc);
+                            issue_mma(m, adm, bdm, sfa_t, sfb_t, acc);
                             if (m == 0) {
                                 ready = tc::mbar_test(full0 + 8 * nstage, nphase);
                             } else {
@@ -349,11 +369,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                             // +32 bytes along K inside a 128-byte swizzle row = +2 in the address field
                             const uint64_t adm = ad + sub * SUB_STEP + 2 * k, bdm = bd + sub * SUB_STEP + 2 * k;
                             const uint32_t acc = (kb | m) != 0;
-                            if (FP4)
-                                tc::mma<2, true>(tmem, adm, bdm, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
-                            else
-                                tc::mma<2, false>(tmem, adm, bdm, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29),
-                                                  sfa_t + 4 * sub, sfb_t + 8 * sub, acc);
+                            issue_mma(m, adm, bdm, sfa_t, sfb_t, acc);
                         }
                         if (!has_next) continue;
                         if (m == 0) {
@@ -389,7 +405,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         const int h = (warp - 2) >> 2;
         const uint32_t tempty_c0 = tc::mapa(tempty, 0);
         float alpha = 1.0f;
-        if (FP4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+        if (KIND == kKindNV) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
         int iter = 0, gcur = 0;
         for (int t = cid; t < total; t += ncl, ++iter) {
             const Tile2 ti = tile2(p, t, gt, gcur, rank);
@@ -433,16 +449,16 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     }
 }
 
-template <bool FP4>
+template <int KIND>
 cudaError_t launch2(const Params2& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tsa,
                     const CUtensorMap& tsb, const CUtensorMap& tc_, int grid, cudaStream_t st) {
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(gemm2_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<FP4>::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(gemm2_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<KIND>::SMEM);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    gemm2_kernel<FP4><<<grid, kThreads, Cfg2<FP4>::SMEM, st>>>(ta, tb, tsa, tsb, tc_, p);
+    gemm2_kernel<KIND><<<grid, kThreads, Cfg2<KIND>::SMEM, st>>>(ta, tb, tsa, tsb, tc_, p);
     return cudaGetLastError();
 }
 
@@ -452,7 +468,7 @@ cudaError_t launch2(const Params2& p, const CUtensorMap& ta, const CUtensorMap& 
 // bands per expert and the experts' scale buffers evenly spaced (one tensor
 // map then spans all of them).
 bool gemm_pair_grouped_ok(const GemmArgs& a) {
-    if (a.num_groups < 1 || a.fmt_a == kNVFP4 || a.N % 128 != 0) return false;
+    if (a.num_groups < 1 || a.fmt_a == kNVFP4 || a.N % 128 != 0) return false;     // MXFP8 or MXFP4
     const int64_t n_atoms = (a.K / 32 + 3) / 4;
     const int64_t stride = (a.N / 128) * n_atoms * 512;
     for (int g = 0; g < a.num_groups; g++)
@@ -463,14 +479,15 @@ bool gemm_pair_grouped_ok(const GemmArgs& a) {
 // Block-scaled GEMM on CTA pairs: dense, or grouped over experts when
 // gemm_pair_grouped_ok() holds.
 cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
-    const bool fp4 = a.fmt_a == kNVFP4;
+    const int kind = a.fmt_a == kNVFP4 ? kKindNV : (a.fmt_a == kMXFP4 ? kKindMX4 : kKindFP8);
+    const bool fp4 = kind != kKindFP8;
     const int64_t kbytes = fp4 ? a.K / 2 : a.K;
-    const int64_t S = a.K / (fp4 ? 16 : 32);
+    const int64_t S = a.K / (kind == kKindNV ? 16 : 32);
     const int64_t n_atoms = (S + 3) / 4;
     Params2 p{};
     p.M = (int32_t)a.M;
     p.N = (int32_t)a.N;
-    const int64_t stage_kb = (int64_t)BKB * (fp4 ? Cfg2<true>::KSUB : Cfg2<false>::KSUB);
+    const int64_t stage_kb = (int64_t)BKB * (fp4 ? Cfg2<kKindNV>::KSUB : Cfg2<kKindFP8>::KSUB);
     p.k_stages = (int32_t)((kbytes + stage_kb - 1) / stage_kb);
     p.mma_last = (int32_t)((kbytes - (int64_t)(p.k_stages - 1) * stage_kb + 31) / 32);
     p.m_tiles = (int32_t)((a.M + 255) / 256);
@@ -483,7 +500,8 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     p.vec_ok = ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0) && ((a.N * esz) % 16 == 0);
     p.ts_a = a.ts_a;
     p.ts_b = a.ts_b;
-    p.idesc = fp4 ? make_idesc(1, 1, false, 256, BN)
+    // E2M1 operands are type 1 in the FP4 kinds; UE8M0 scales except NVFP4's UE4M3
+    p.idesc = fp4 ? make_idesc(1, 1, kind == kKindMX4, 256, BN)
                   : make_idesc(a.fmt_a == kE5M2 ? 1 : 0, a.fmt_b == kE5M2 ? 1 : 0, true, 256, BN);
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
@@ -503,7 +521,8 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
         }
     }
 
-    const int sf_atoms = fp4 ? Cfg2<true>::SF_ATOMS : Cfg2<false>::SF_ATOMS;
+    const int sf_atoms = kind == kKindNV ? Cfg2<kKindNV>::SF_ATOMS
+                       : (kind == kKindMX4 ? Cfg2<kKindMX4>::SF_ATOMS : Cfg2<kKindFP8>::SF_ATOMS);
     CUtensorMap ta, tb, tsa, tsb;
     if (!tmap::codes_2d(&ta, a.a_codes, a.M, kbytes, 128)) return cudaErrorInvalidValue;
     const int64_t b_rows = grouped ? a.N * a.num_groups : a.N;
@@ -518,7 +537,9 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     int pairs = a.num_sms / 2;
     if (!grouped && p.total_tiles < pairs) pairs = p.total_tiles;
     if (pairs < 1) pairs = 1;
-    return fp4 ? launch2<true>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st) : launch2<false>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st);
+    if (kind == kKindNV) return launch2<kKindNV>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st);
+    if (kind == kKindMX4) return launch2<kKindMX4>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st);
+    return launch2<kKindFP8>(p, ta, tb, tsa, tsb, tcm, 2 * pairs, st);
 }
 
 }  // namespace bsq

@@ -152,7 +152,8 @@ bsq_status bsq_dequantize(const bsq_tensor* in, void* dst, int32_t dst_type, voi
 /* C[M,N] = A[M,K] * B[N,K]^T with FP32 accumulation on tcgen05 block-scaled
  * tensor-core MMAs; C row-major with leading dimension N, FP32 or BF16.
  * Supported pairs: any of MXFP8 E4M3 / E5M2 with each other; NVFP4 with
- * NVFP4 (the result is multiplied by both tensor scales).  K = A.cols =
+ * NVFP4 (the result is multiplied by both tensor scales); MXFP4 with MXFP4
+ * (native FP4 MMA with UE8M0 scales, no re-encode).  K = A.cols =
  * B.cols; K % 32 == 0.  M, N >= 1 of any size.  Citation: MoE FP4 page
  * section 2 ("Calculo Intenso": GEMMs stay on native FP8 tensor cores);
  * FP8 page "MXFP8 e NVFP4 do Blackwell" (hardware block scaling). */
@@ -165,7 +166,9 @@ bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t o
  * tensors of identical shape [N, K] and format; their code buffers must be
  * consecutive slices of one allocation (B_g.codes = B_0.codes + g * codes
  * bytes); scale buffers may be anywhere.  A's scales use the plain tiled
- * layout of the whole [A.rows, K] matrix.  num_groups <= 256; MXFP8 only.
+ * layout of the whole [A.rows, K] matrix.  num_groups <= 256; MXFP8
+ * (any mix of E4M3 / E5M2) or MXFP4 x MXFP4; for MXFP4 the experts' scale
+ * buffers must also be evenly spaced (BSQ_ERR_UNSUPPORTED otherwise).
  * Citation: MoE FP4 page section 2, ragged tensors whose per-expert token
  * counts vary. */
 bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_dev, int32_t num_groups,

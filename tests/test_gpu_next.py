@@ -163,3 +163,68 @@ def test_fp4_row_to_fp8_col_full_size_sampled(bsq):
         off = ((r // 128) * (S_out // 4) + cc // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + cc % 4
         assert np.array_equal(sc_buf[off], s8), f"group {g}: scales differ"
     bsq.sync_status()
+
+
+# ------------------------------------------------------- native MXFP4 GEMM
+def _mx4_gemm_check(bsq, xa, xb, out, groups=None):
+    """Oracle-quantized MXFP4 operands uploaded, GEMM on the device, compared
+    with the FP64 product of the exactly dequantized operands."""
+    import torch
+    from _util import upload_q, gemm_tol_ok
+    ca, sa = oracle.mx_quantize_rows(xa, "mxfp4")
+    cb, sb = oracle.mx_quantize_rows(xb, "mxfp4")
+    A = upload_q(bsq, "mxfp4", ca, sa)
+    B = upload_q(bsq, "mxfp4", cb, sb)
+    dt = torch.float32 if out == "f32" else torch.bfloat16
+    Ad = oracle.dequant_rows(ca, sa, "mxfp4")
+    Bd = oracle.dequant_rows(cb, sb, "mxfp4")
+    if groups is None:
+        C = bsq.gemm(A, B, dt).float().cpu().numpy()
+        pairs = [(slice(0, xa.shape[0]), slice(0, xb.shape[0]))]
+    else:
+        off = inputs.group_offsets(groups)
+        N = xb.shape[0] // len(groups)
+        C = bsq.grouped_gemm(A, torch.from_numpy(off).cuda(), bsq.group_views(B, len(groups)), dt)
+        C = C.float().cpu().numpy()
+        pairs = [(slice(off[g], off[g + 1]), slice(g * N, (g + 1) * N)) for g in range(len(groups)) if off[g + 1] > off[g]]
+    for rows, brows in pairs:
+        ref, mag = oracle.gemm_full(Ad[rows], Bd[brows])
+        ok, err, tol = gemm_tol_ok(C[rows], ref, mag, out == "bf16")
+        assert ok.all(), f"{(~ok).sum()} of {ok.size} outside the bound (max err/tol {np.max(err / tol):.3g})"
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (1, 1, 32), (200, 300, 96), (257, 513, 4160), (64, 640, 1024),
+                                   (300, 256, 7168)])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_gemm_mxfp4_shapes(bsq, M, N, K, out):
+    xa = inputs.outlier_activations_bf16((M, K), 60)
+    xb = inputs.normal_bf16((N, K), 61, std=0.02)
+    _mx4_gemm_check(bsq, xa, xb, out)
+    bsq.sync_status()
+
+
+def test_grouped_gemm_mxfp4(bsq):
+    counts = np.array([700, 0, 129, 1, 383, 256, 1000, 0, 31], dtype=np.int64)
+    N, K = 256, 4160
+    xa = inputs.normal_bf16((int(counts.sum()), K), 62)
+    xb = inputs.normal_bf16((len(counts) * N, K), 63, std=0.02)
+    _mx4_gemm_check(bsq, xa, xb, "f32", groups=counts)
+    bsq.sync_status()
+
+
+def test_gemm_mxfp4_single_scale_probe(bsq):
+    """Codes all 1.0, one scale per (row, 32-block) drawn near 2^0: every
+    scale byte must reach the MMA for the row and K-block it belongs to
+    (each MMA reads a byte pair of a 4-byte scale word)."""
+    import torch
+    from _util import upload_q
+    M, N, K = 128, 256, 512
+    one = oracle.encode(oracle.E2M1, 1.0)
+    ca = np.full((M, K), one, np.uint8)
+    cb = np.full((N, K), one, np.uint8)
+    rng = np.random.default_rng(64)
+    sa = (127 + rng.integers(-3, 4, (M, K // 32))).astype(np.uint8)
+    sb = (127 + rng.integers(-3, 4, (N, K // 32))).astype(np.uint8)
+    C = bsq.gemm(upload_q(bsq, "mxfp4", ca, sa), upload_q(bsq, "mxfp4", cb, sb), torch.float32).cpu().numpy()
+    ref = 32.0 * (np.exp2(sa.astype(np.float64) - 127) @ np.exp2(sb.astype(np.float64) - 127).T)
+    np.testing.assert_array_equal(C, ref.astype(np.float32))
