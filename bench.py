@@ -188,6 +188,15 @@ class Step:
         # scaling, one pass (2.5625 B per element), the amax history holding
         # the tensor's own amax as in steady state.
         self.extra_ops = []
+        if "fwd" in want:
+            # NEXT-4, dense: the forward GEMM on MXFP4 x MXFP4 operands
+            # (quantized once here; the timed op is the GEMM alone)
+            o["Xq4"] = E("mxfp4", M, K)
+            o["Wq4"] = E("mxfp4", N, K)
+            q(i["X"], "mxfp4", "row", o["Xq4"], None)
+            q(i["W"], "mxfp4", "row", o["Wq4"], None)
+            self.extra_ops.append(("gemm fwd mxfp4 Y=XW^T", "NEXT-4", "gemm4",
+                                   lambda: bsq.gemm_into(o["Xq4"], o["Wq4"], o["Y"]), 0, 2 * M * N * K, 1))
         if "moe" in want:
             # NEXT-1: FP4RowToFP8Col of the MoE activations (the wgrad operand),
             # from the MXFP4 rows the step produced; read 0.53125 + write 1.03125 B
