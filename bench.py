@@ -120,6 +120,8 @@ class Step:
         self.inp = {k: dev(host[k]) for k in ("X", "W", "dY", "X4", "W4", "X42", "W42", "A_moe", "W_moe")
                     if k in host}
         self.offsets = torch.from_numpy(host["offsets"]).cuda() if "offsets" in host else None
+        self.moe_counts = np.diff(host["offsets"]).tolist() if "offsets" in host else None
+        self.moe_kn = (sh["moe"]["K"], sh["moe"]["N"])
         want = {"all": ("fwd", "bwd", "nv", "moe")}.get(part, (part,))
         f, n, m = sh["fwd"], sh["nv"], sh["moe"]
         M, N, K = f["M"], f["N"], f["K"]
@@ -511,6 +513,22 @@ def main():
             ach = nbytes / (ms * 1e-3) / 1e9
             rec = {"ms": round(ms, 4), "gbs": round(ach, 1), "frac": round(ach / pk["hbm_gbs"], 4),
                    "frac_spec_8tbs": round(ach / 8000.0, 4)}
+        if kind == "quant" and row == "a3":
+            # the NVFP4 bytes above count the amax pass; also the one-read minimum
+            one = nbytes * (2 + 0.5 + 1 / 16) / (2 + 2 + 0.5 + 1 / 16)
+            rec["frac_one_read"] = round(one / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)
+        if name == "grouped gemm moe" and step.moe_counts is not None:
+            # attainable time: per expert the larger of its compute time at the
+            # FP8 peak and the time to stream its weights, activations and
+            # output at the HBM rate (small experts are bound by their weights)
+            K_, N_ = step.moe_kn
+            t_bound = 0.0
+            for cnt in step.moe_counts:
+                fl = 2.0 * cnt * N_ * K_
+                by = N_ * K_ * (1 + 1 / 32) + cnt * K_ * (1 + 1 / 32) + cnt * N_ * 2
+                t_bound += max(fl / (pk["fp8_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
+            rec["attainable_ms"] = round(t_bound * 1e3, 4)
+            rec["frac_attainable"] = round(t_bound * 1e3 / ms, 4)
         rows[name] = dict(row=row, **rec)
         a = agg.setdefault(kind, [0.0, 0.0, 0.0])
         a[0] += ms

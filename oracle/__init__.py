@@ -281,6 +281,34 @@ def unswizzle_scales(buf: np.ndarray, R: int, S: int) -> np.ndarray:
     return buf[off]
 
 
+def grouped_scale_starts(offsets) -> tuple[np.ndarray, int]:
+    """Per-expert padded scale layout: expert g's scale rows start at
+    P_g = sum over earlier experts of their row counts rounded up to 128, so
+    no 128-row scale tile holds two experts.  Returns (P [G], total rows)."""
+    o = np.asarray(offsets, dtype=np.int64)
+    padded = (np.diff(o) + 127) // 128 * 128
+    P = np.concatenate([[0], np.cumsum(padded)[:-1]]).astype(np.int64)
+    return P, int(padded.sum())
+
+
+def swizzle_scales_grouped(s: np.ndarray, offsets, capacity_rows: int | None = None) -> np.ndarray:
+    """Row-major [R, S] scales of rows grouped by `offsets` -> the tiled byte
+    stream of the [P_total, S] matrix in which data row r of expert g sits at
+    scale row P_g + (r - offsets[g]); every other byte is zero.  The buffer
+    may be longer (capacity_rows, a multiple of 128)."""
+    s = np.asarray(s, dtype=np.uint8)
+    R, S = s.shape
+    o = np.asarray(offsets, dtype=np.int64)
+    P, total = grouped_scale_starts(o)
+    rows = total if capacity_rows is None else capacity_rows
+    assert rows >= total and rows % 128 == 0
+    padded = np.zeros((rows, S), dtype=np.uint8)
+    for g in range(len(o) - 1):
+        n = o[g + 1] - o[g]
+        padded[P[g]:P[g] + n] = s[o[g]:o[g + 1]]
+    return swizzle_scales(padded)
+
+
 def scale_pad_mask(R: int, S: int) -> np.ndarray:
     """Boolean mask over the tiled buffer: True where a byte is padding."""
     m = np.ones(scales_nbytes(R, S), dtype=bool)

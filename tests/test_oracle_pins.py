@@ -468,3 +468,34 @@ def test_fp4_row_to_fp8_col_nan_scale_and_zero_block():
     assert (s8[:, 0] == 0xFF).all() and (c8[:, :32] == 0x7F).all()
     assert (s8[:, 1][np.arange(32) != 5] == 0).all()      # all-zero blocks: scale 2^-127
     assert s8[5, 1] == 127 + 2 - 8 and c8[5, 40] == oracle.encode(E4M3, 6.0 * 2.0 ** 6)
+
+
+# ------------------------------------------------ per-expert padded scales
+def test_grouped_scale_layout_reduces_to_plain():
+    rng = np.random.default_rng(70)
+    s = rng.integers(1, 255, (300, 9)).astype(np.uint8)
+    # one expert, or experts whose sizes are multiples of 128: the plain layout
+    np.testing.assert_array_equal(oracle.swizzle_scales_grouped(s, [0, 300]), oracle.swizzle_scales(s))
+    s2 = rng.integers(1, 255, (384, 5)).astype(np.uint8)
+    np.testing.assert_array_equal(oracle.swizzle_scales_grouped(s2, [0, 128, 128, 384]), oracle.swizzle_scales(s2))
+
+
+def test_grouped_scale_layout_rows_and_padding():
+    # each expert's rows start on a 128-row tile boundary of the padded
+    # matrix; read back through the plain (independently pinned) layout
+    rng = np.random.default_rng(71)
+    counts = np.array([100, 0, 300, 1, 129, 70])
+    off = np.concatenate([[0], np.cumsum(counts)])
+    R, S = int(off[-1]), 7
+    s = rng.integers(1, 255, (R, S)).astype(np.uint8)
+    P, total = oracle.grouped_scale_starts(off)
+    assert list(P) == [0, 128, 128, 512, 640, 896] and total == 1024
+    buf = oracle.swizzle_scales_grouped(s, off, capacity_rows=1152)
+    m = oracle.unswizzle_scales(buf, 1152, S)
+    used = np.zeros(1152, bool)
+    for g in range(len(counts)):
+        np.testing.assert_array_equal(m[P[g]:P[g] + counts[g]], s[off[g]:off[g + 1]])
+        used[P[g]:P[g] + counts[g]] = True
+        assert P[g] % 128 == 0
+    assert not m[~used].any()
+    assert buf.size == 1152 * 8 and not buf[oracle.scale_pad_mask(1152, S)].any()
