@@ -147,7 +147,9 @@ class Step:
             o["Y42"] = torch.empty((n["M"], n["N"]), dtype=torch.bfloat16, device="cuda")
         if "moe" in want:
             o["A4"] = E("mxfp4", m["rows"], m["K"])
-            o["A8"] = E("mxfp8_e4m3", m["rows"], m["K"])
+            # the re-encoded activations carry their scales in the per-expert
+            # padded layout, so the grouped GEMM's tiles start at expert boundaries
+            o["A8"] = bsq.empty_grouped("mxfp8_e4m3", m["rows"], m["K"], m["experts"])
             o["Wm"] = E("mxfp8_e4m3", m["experts"] * m["N"], m["K"])
             o["Ym"] = torch.empty((m["rows"], m["N"]), dtype=torch.bfloat16, device="cuda")
         self.out = o
@@ -174,10 +176,12 @@ class Step:
             ("gemm nvfp4 Y=XW^T", "a4", "gemm4", lambda: bsq.gemm_into(o["X4q"], o["W4q"], o["Y4"]), 0, 2 * n["M"] * n["N"] * n["K"], 1),
             ("gemm nvfp4 Y'=X'W'^T", "a4", "gemm4", lambda: bsq.gemm_into(o["X42q"], o["W42q"], o["Y42"]), 0, 2 * n["M"] * n["N"] * n["K2"], 1),
             ("quant A_moe mxfp4 row", "a1", "quant", lambda: q(i["A_moe"], "mxfp4", "row", o["A4"], None), mn * B_ROW4, 0, 1),
-            ("repack mxfp4->mxfp8", "a5", "repack", lambda: bsq.mxfp4_to_mxfp8_into(o["A4"], o["A8"]), mn * B_REPACK, 0, 1),
+            ("repack mxfp4->mxfp8", "a5", "repack",
+             lambda: bsq.mxfp4_to_mxfp8_grouped_into(o["A4"], o["A8"], self.offsets, m["experts"]), mn * B_REPACK, 0, 1),
             ("quant W_moe e4m3 row", "a1", "quant", lambda: q(i["W_moe"], "mxfp8_e4m3", "row", o["Wm"], None),
              m["experts"] * m["N"] * m["K"] * B_ROW8, 0, 1),
-            ("grouped gemm moe", "a6", "gemm8", lambda: bsq.grouped_gemm_into(o["A8"], self.offsets, self.wm_groups, o["Ym"]),
+            ("grouped gemm moe", "a6", "gemm8", lambda: bsq.grouped_gemm_into(o["A8"], self.offsets, self.wm_groups, o["Ym"],
+                                                                               padded_scales=True),
              0, 2 * m["rows"] * m["N"] * m["K"], 1),
         ]
         part_of = ["fwd"] * 3 + ["bwd"] * 5 + ["nv"] * 6 + ["moe"] * 4

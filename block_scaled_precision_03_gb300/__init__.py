@@ -65,6 +65,9 @@ def lib():
         "bsq_dequantize": (i32, [PT, vp, i32, vp]),
         "bsq_gemm": (i32, [PT, PT, vp, i32, vp]),
         "bsq_grouped_gemm": (i32, [PT, vp, i32, PT, vp, i32, vp]),
+        "bsq_grouped_gemm_padded": (i32, [PT, vp, i32, PT, vp, i32, vp]),
+        "bsq_grouped_scales_bytes": (sz, [i32, i64, i64, i32]),
+        "bsq_mxfp4_to_mxfp8_grouped": (i32, [PT, PT, vp, i32, vp]),
         "bsq_mxfp4_to_mxfp8": (i32, [PT, PT, vp]),
         "bsq_mxfp4_to_mxfp8_col": (i32, [PT, PT, vp]),
         "bsq_sync_status": (i32, [vp]),
@@ -221,22 +224,24 @@ def group_views(B: QTensor, groups: int) -> list[QTensor]:
             for g in range(groups)]
 
 
-def grouped_gemm_into(A: QTensor, offsets_dev, B_groups: list[QTensor], C, stream=None):
+def grouped_gemm_into(A: QTensor, offsets_dev, B_groups: list[QTensor], C, stream=None, padded_scales=False):
+    """Grouped GEMM into C; padded_scales: A's scales are in the per-expert
+    padded layout (from mxfp4_to_mxfp8_grouped)."""
     import torch
     ca = A.c()
     arr = (BsqTensorC * len(B_groups))(*[b.c() for b in B_groups])
-    st = lib().bsq_grouped_gemm(ctypes.byref(ca), ctypes.c_void_p(offsets_dev.data_ptr()), len(B_groups), arr,
-                                ctypes.c_void_p(C.data_ptr()),
-                                OUT_BF16 if C.dtype == torch.bfloat16 else OUT_F32, _stream(stream))
+    f = lib().bsq_grouped_gemm_padded if padded_scales else lib().bsq_grouped_gemm
+    st = f(ctypes.byref(ca), ctypes.c_void_p(offsets_dev.data_ptr()), len(B_groups), arr, ctypes.c_void_p(C.data_ptr()),
+           OUT_BF16 if C.dtype == torch.bfloat16 else OUT_F32, _stream(stream))
     _check(st, "bsq_grouped_gemm")
     return C
 
 
-def grouped_gemm(A: QTensor, offsets_dev, B_groups: list[QTensor], dtype=None, stream=None):
+def grouped_gemm(A: QTensor, offsets_dev, B_groups: list[QTensor], dtype=None, stream=None, padded_scales=False):
     import torch
     dtype = dtype or torch.float32
     C = torch.empty((A.rows, B_groups[0].rows), dtype=dtype, device=A.codes.device)
-    return grouped_gemm_into(A, offsets_dev, B_groups, C, stream)
+    return grouped_gemm_into(A, offsets_dev, B_groups, C, stream, padded_scales)
 
 
 def mxfp4_to_mxfp8_into(q: QTensor, out: QTensor, stream=None):
@@ -248,6 +253,31 @@ def mxfp4_to_mxfp8_into(q: QTensor, out: QTensor, stream=None):
 def mxfp4_to_mxfp8(q: QTensor, stream=None) -> QTensor:
     out = empty(MXFP8_E4M3, q.rows, q.cols, q.codes.device)
     return mxfp4_to_mxfp8_into(q, out, stream)
+
+
+def grouped_scales_bytes(fmt, rows: int, cols: int, groups: int) -> int:
+    return int(lib().bsq_grouped_scales_bytes(_fmt(fmt), rows, cols, groups))
+
+
+def empty_grouped(fmt, rows: int, cols: int, groups: int, device="cuda") -> QTensor:
+    """Uninitialized tensor whose scale buffer holds the per-expert padded layout."""
+    import torch
+    q = empty(fmt, rows, cols, device)
+    q.scales = torch.empty(grouped_scales_bytes(fmt, rows, cols, groups), dtype=torch.uint8, device=device)
+    return q
+
+
+def mxfp4_to_mxfp8_grouped_into(q: QTensor, out: QTensor, offsets_dev, groups: int, stream=None):
+    ci, co = q.c(), out.c()
+    _check(lib().bsq_mxfp4_to_mxfp8_grouped(ctypes.byref(ci), ctypes.byref(co), ctypes.c_void_p(offsets_dev.data_ptr()),
+                                            groups, _stream(stream)), "bsq_mxfp4_to_mxfp8_grouped")
+
+
+def mxfp4_to_mxfp8_grouped(q: QTensor, offsets_dev, groups: int, stream=None) -> QTensor:
+    """MXFP4 -> MXFP8 E4M3 with the scales in the per-expert padded layout."""
+    out = empty_grouped("mxfp8_e4m3", q.rows, q.cols, groups, q.codes.device)
+    mxfp4_to_mxfp8_grouped_into(q, out, offsets_dev, groups, stream)
+    return out
 
 
 def mxfp4_to_mxfp8_col_into(q: QTensor, out: QTensor, stream=None):

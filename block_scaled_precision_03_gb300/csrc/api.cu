@@ -74,6 +74,8 @@ bool env_grouped_pair() {
 
 const uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
 
+
+
 // bsq_quantize and bsq_quantize_nvfp4_delayed: argument checks and launch;
 // `history` (NVFP4 only) selects delayed scaling.
 bsq_status quantize_common(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
@@ -218,8 +220,10 @@ bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t o
     return from_cuda(bsq::run_gemm(a, static_cast<cudaStream_t>(stream)));
 }
 
-bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_dev, int32_t num_groups,
-                            const bsq_tensor* B_groups, void* C, int32_t out_type, void* stream) {
+// bsq_grouped_gemm and bsq_grouped_gemm_padded: checks and launch; `padded`
+// says A's scales are in the per-expert padded layout.
+static bsq_status grouped_gemm_common(const bsq_tensor* A, const int64_t* group_offsets_dev, int32_t num_groups,
+                               const bsq_tensor* B_groups, void* C, int32_t out_type, bool padded, void* stream) {
     if (!B_groups || !group_offsets_dev || num_groups < 1) return BSQ_ERR_INVALID_ARG;
     if (num_groups > bsq::kMaxGroups) return BSQ_ERR_UNSUPPORTED;
     bsq_status s = check_gemm_pair(A, &B_groups[0]);
@@ -256,6 +260,7 @@ bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_de
     a.num_groups = num_groups;
     a.offsets = group_offsets_dev;
     a.b_group_scales = sf;
+    a.a_grouped_sf = padded;
     a.single_cta = env_single_cta();
     a.grouped_pair = env_grouped_pair();
     a.num_sms = num_sms();
@@ -265,6 +270,49 @@ bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_de
     // with one tensor map: they must be evenly spaced (as group views are)
     if (A->fmt == BSQ_MXFP4_E2M1 && !bsq::gemm_pair_grouped_ok(a)) return BSQ_ERR_UNSUPPORTED;
     return from_cuda(bsq::run_gemm(a, static_cast<cudaStream_t>(stream)));
+}
+
+bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_dev, int32_t num_groups,
+                            const bsq_tensor* B_groups, void* C, int32_t out_type, void* stream) {
+    return grouped_gemm_common(A, group_offsets_dev, num_groups, B_groups, C, out_type, false, stream);
+}
+
+bsq_status bsq_grouped_gemm_padded(const bsq_tensor* A, const int64_t* group_offsets_dev, int32_t num_groups,
+                                   const bsq_tensor* B_groups, void* C, int32_t out_type, void* stream) {
+    return grouped_gemm_common(A, group_offsets_dev, num_groups, B_groups, C, out_type, true, stream);
+}
+
+size_t bsq_grouped_scales_bytes(int32_t fmt, int64_t rows, int64_t cols, int32_t num_groups) {
+    if (num_groups < 1 || num_groups > bsq::kMaxGroups || rows < 0) return 0;
+    const size_t plain = scales_bytes(fmt, rows, cols);
+    if (plain == 0 && rows > 0) return 0;
+    const int64_t s_pad = rows > 0 ? (int64_t)plain / ((rows + 127) / 128 * 128) : 0;
+    return (size_t)(((rows + 127) / 128 * 128) + 128 * (int64_t)num_groups) * (size_t)s_pad;
+}
+
+bsq_status bsq_mxfp4_to_mxfp8_grouped(const bsq_tensor* in, bsq_tensor* out, const int64_t* group_offsets_dev,
+                                      int32_t num_groups, void* stream) {
+    if (!group_offsets_dev || num_groups < 1) return BSQ_ERR_INVALID_ARG;
+    if (num_groups > bsq::kMaxGroups) return BSQ_ERR_UNSUPPORTED;
+    bsq_status s = check_tensor(in, false);
+    if (s != BSQ_OK) return s;
+    if ((s = check_tensor(out, false)) != BSQ_OK) return s;
+    if (in->fmt != BSQ_MXFP4_E2M1 || out->fmt != BSQ_MXFP8_E4M3) return BSQ_ERR_UNSUPPORTED;
+    if (in->rows != out->rows || in->cols != out->cols) return BSQ_ERR_INVALID_ARG;
+    if (in->rows > 0x7FFFFF00LL) return BSQ_ERR_UNSUPPORTED;
+    bsq::RepackArgs a{};
+    a.in_codes = static_cast<const uint8_t*>(in->codes);
+    a.in_scales = in->scales;
+    a.out_codes = static_cast<uint8_t*>(out->codes);
+    a.out_scales = out->scales;
+    a.rows = in->rows;
+    a.cols = in->cols;
+    a.scales_bytes = bsq_grouped_scales_bytes(BSQ_MXFP8_E4M3, in->rows, in->cols, num_groups);
+    a.scales_pad = false;              // the kernel writes every byte of the capacity
+    a.num_sms = num_sms();
+    a.offsets = group_offsets_dev;
+    a.num_groups = num_groups;
+    return from_cuda(bsq::run_repack(a, static_cast<cudaStream_t>(stream)));
 }
 
 bsq_status bsq_mxfp4_to_mxfp8(const bsq_tensor* in, bsq_tensor* out, void* stream) {

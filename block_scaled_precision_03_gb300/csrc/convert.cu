@@ -8,6 +8,8 @@
 // nibble keeps its sign and mantissa bit and its exponent moves by the
 // shift between the two scales, so every value is carried over exactly.
 // There is no BF16 or FP32 intermediate.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -19,69 +21,213 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-// 4 nibbles (low 16 bits of x) -> one byte each, nibble k in byte k.
-__device__ __forceinline__ uint32_t spread_nibbles(uint32_t x) {
-    x &= 0xFFFFu;
-    x = (x | (x << 8)) & 0x00FF00FFu;
-    x = (x | (x << 4)) & 0x0F0F0F0Fu;
-    return x;
-}
-
 // 8 E2M1 nibbles of w -> 8 E4M3 bytes given the magnitude table (lut_lo =
-// bytes for magnitudes 0..3, lut_hi = 4..7).
+// bytes for magnitudes 0..3, lut_hi = 4..7).  The magnitudes index the table
+// directly (a byte permute reads its 4 selector nibbles from the low 16
+// bits); the sign bits are moved to bit 7 of their bytes in place (odd
+// nibbles' signs already sit at bit 7 of a byte, even nibbles' after a
+// 4-bit shift) and interleaved with two more byte permutes.
 __device__ __forceinline__ uint2 remap8(uint32_t w, uint32_t lut_lo, uint32_t lut_hi) {
     const uint32_t m = w & 0x77777777u;
-    uint32_t lo = prmt(lut_lo, lut_hi, m & 0xFFFFu);
-    uint32_t hi = prmt(lut_lo, lut_hi, m >> 16);
-    lo |= (spread_nibbles(w) & 0x08080808u) << 4;
-    hi |= (spread_nibbles(w >> 16) & 0x08080808u) << 4;
+    const uint32_t s_even = (w << 4) & 0x80808080u;      // nibbles 0, 2, 4, 6
+    const uint32_t s_odd = w & 0x80808080u;              // nibbles 1, 3, 5, 7
+    const uint32_t lo = prmt(lut_lo, lut_hi, m) | prmt(s_even, s_odd, 0x5140u);
+    const uint32_t hi = prmt(lut_lo, lut_hi, m >> 16) | prmt(s_even, s_odd, 0x7362u);
     return make_uint2(lo, hi);
 }
 
-__global__ void __launch_bounds__(256)
+// Expert offsets for the per-expert padded scale layout of the output: expert
+// g's scale rows start at P_g = sum over earlier experts of their row counts
+// rounded up to 128 (clamped offsets, as in the grouped GEMM).
+struct ExpertRows {
+    const int64_t* offsets;        // device, num_groups + 1 (nullptr: plain layout)
+    int32_t num_groups;
+};
+constexpr int kMaxExperts = kMaxGroups;
+
+// One 32-block: 16 code bytes in, 32 code bytes and the new scale byte out.
+__device__ __forceinline__ void repack_block(const uint4 w, const uint32_t s, uint4& o0, uint4& o1, uint32_t& ns) {
+    if (s == 0xFF) {
+        ns = 0xFF;
+        o0 = o1 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        return;
+    }
+    // largest magnitude index over the 32 nibbles (value order = code order)
+    uint32_t mx = __vmaxu4(__vmaxu4(w.x & 0x07070707u, (w.x >> 4) & 0x07070707u),
+                           __vmaxu4(w.y & 0x07070707u, (w.y >> 4) & 0x07070707u));
+    mx = __vmaxu4(mx, __vmaxu4(__vmaxu4(w.z & 0x07070707u, (w.z >> 4) & 0x07070707u),
+                               __vmaxu4(w.w & 0x07070707u, (w.w >> 4) & 0x07070707u)));
+    mx = max(max(mx & 0xFF, (mx >> 8) & 0xFF), max((mx >> 16) & 0xFF, mx >> 24));
+    uint32_t lut_lo = 0, lut_hi = 0;
+    if (mx == 0) {
+        ns = 0;                                  // all-zero block: e = -127
+    } else {
+        // exponent of the largest magnitude: 0.5 -> -1, 1|1.5 -> 0, 2|3 -> 1, 4|6 -> 2
+        const int e_c = mx == 1 ? -1 : (int)(mx >> 1) - 1;
+        int nb = (int)s + e_c - 8;
+        if (nb < 0) nb = 0;
+        ns = (uint32_t)nb;
+        const uint32_t E = (uint32_t)((int)s - nb + 7);   // biased E4M3 exponent of magnitude 1.0
+        // E4M3 bytes of magnitudes 0, 0.5, 1, 1.5 | 2, 3, 4, 6 scaled by 2^(s - nb)
+        lut_lo = ((E - 1) << 11) | ((E << 3) << 16) | (((E << 3) | 4u) << 24);
+        lut_hi = ((E + 1) << 3) | ((((E + 1) << 3) | 4u) << 8) | (((E + 2) << 3) << 16) |
+                 ((((E + 2) << 3) | 4u) << 24);
+    }
+    const uint2 a = remap8(w.x, lut_lo, lut_hi), bb = remap8(w.y, lut_lo, lut_hi);
+    const uint2 c = remap8(w.z, lut_lo, lut_hi), d = remap8(w.w, lut_lo, lut_hi);
+    o0 = make_uint4(a.x, a.y, bb.x, bb.y);
+    o1 = make_uint4(c.x, c.y, d.x, d.y);
+}
+
+// One 32-byte store (both halves of a converted block): a warp then writes
+// 1 KB of whole sectors per instruction instead of two half-filled passes.
+// The address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32B(uint4* p, const uint4 a, const uint4 b) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+                 "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
+constexpr int kRepackThreads = 256;
+constexpr int kRepackUnroll = 4;     // 32-blocks in flight per thread
+
+// Each CTA converts one contiguous range of 32-blocks (row-major order), a
+// thread taking every 256th block, four per iteration so that four 16-byte
+// loads are in flight (the kernel is bound by memory latency times the loads
+// in flight per SM).  Rows grow along a thread's walk, so in the grouped
+// form its expert only moves forward (o_s / p_s: expert row starts and
+// padded scale row starts, built per CTA from the clamped offsets).  The
+// grouped form also writes every other byte of the scale buffer (cap_bytes)
+// as zero, each byte by exactly one thread: the pad columns of live rows,
+// the rows between an expert's last row and its next 128-row boundary, and
+// the whole tiles past the last expert.  Rows past the last offset belong to
+// no expert: their codes are converted, their scales have no slot.  WIDE:
+// the output codes are 32-byte aligned and each block is one 32-byte store.
+template <bool GROUPED, bool WIDE>
+__global__ void __launch_bounds__(kRepackThreads)
 repack_kernel(const uint4* __restrict__ in, const uint8_t* __restrict__ sin, uint4* __restrict__ out,
-              uint8_t* __restrict__ sout, int64_t nblocks, uint32_t bpr, int64_t s_tiles) {
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
-        const uint4 w = in[b];
-        const uint32_t r = (uint32_t)(b / bpr), j = (uint32_t)(b - (int64_t)r * bpr);
-        const int64_t off = sf_offset(r, j, s_tiles);
-        const uint32_t s = sin[off];
-        uint4 o0, o1;
-        uint32_t ns;
-        if (s == 0xFF) {
-            ns = 0xFF;
-            o0 = o1 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-        } else {
-            // largest magnitude index over the 32 nibbles (value order = code order)
-            uint32_t mx = __vmaxu4(__vmaxu4(w.x & 0x07070707u, (w.x >> 4) & 0x07070707u),
-                                   __vmaxu4(w.y & 0x07070707u, (w.y >> 4) & 0x07070707u));
-            mx = __vmaxu4(mx, __vmaxu4(__vmaxu4(w.z & 0x07070707u, (w.z >> 4) & 0x07070707u),
-                                       __vmaxu4(w.w & 0x07070707u, (w.w >> 4) & 0x07070707u)));
-            mx = max(max(mx & 0xFF, (mx >> 8) & 0xFF), max((mx >> 16) & 0xFF, mx >> 24));
-            uint32_t lut_lo = 0, lut_hi = 0;
-            if (mx == 0) {
-                ns = 0;                                  // all-zero block: e = -127
-            } else {
-                // exponent of the largest magnitude: 0.5 -> -1, 1|1.5 -> 0, 2|3 -> 1, 4|6 -> 2
-                const int e_c = mx == 1 ? -1 : (int)(mx >> 1) - 1;
-                int nb = (int)s + e_c - 8;
-                if (nb < 0) nb = 0;
-                ns = (uint32_t)nb;
-                const uint32_t E = (uint32_t)((int)s - nb + 7);   // biased E4M3 exponent of magnitude 1.0
-                // E4M3 bytes of magnitudes 0, 0.5, 1, 1.5 | 2, 3, 4, 6 scaled by 2^(s - nb)
-                lut_lo = ((E - 1) << 11) | ((E << 3) << 16) | (((E << 3) | 4u) << 24);
-                lut_hi = ((E + 1) << 3) | ((((E + 1) << 3) | 4u) << 8) | (((E + 2) << 3) << 16) |
-                         ((((E + 2) << 3) | 4u) << 24);
+              uint8_t* __restrict__ sout, int64_t nblocks, int64_t per_cta, uint32_t bpr, int64_t s_tiles, int64_t R,
+              const ExpertRows er, int64_t cap_bytes) {
+    __shared__ int32_t o_s[kMaxExperts + 1], p_s[kMaxExperts + 1];
+    const int64_t b_lo = (int64_t)blockIdx.x * per_cta;
+    const int64_t b_hi = min(nblocks, b_lo + per_cta);
+    int g = 0;
+    if (GROUPED) {
+        if (threadIdx.x < 32) {
+            int carry = 0, prev = 0;
+            for (int g0 = 0; g0 <= er.num_groups; g0 += 32) {
+                const int gi = g0 + (int)threadIdx.x;
+                int o = 0;
+                if (gi <= er.num_groups) o = gi == 0 ? 0 : clamp_rows(er.offsets[gi], 0, R);
+                // offsets are non-decreasing after a running max
+                int om = o;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int u = __shfl_up_sync(0xffffffffu, om, d);
+                    if ((int)threadIdx.x >= d) om = max(om, u);
+                }
+                om = max(om, prev);
+                const int lo = __shfl_up_sync(0xffffffffu, om, 1);
+                const int lo_g = threadIdx.x == 0 ? prev : lo;          // start of expert gi - 1
+                int padded = (gi >= 1 && gi <= er.num_groups) ? (om - lo_g + 127) / 128 * 128 : 0;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int u = __shfl_up_sync(0xffffffffu, padded, d);
+                    if ((int)threadIdx.x >= d) padded += u;
+                }
+                if (gi <= er.num_groups) { o_s[gi] = om; p_s[gi] = carry + padded; }
+                carry += __shfl_sync(0xffffffffu, padded, 31);
+                prev = __shfl_sync(0xffffffffu, om, 31);
             }
-            const uint2 a = remap8(w.x, lut_lo, lut_hi), bb = remap8(w.y, lut_lo, lut_hi);
-            const uint2 c = remap8(w.z, lut_lo, lut_hi), d = remap8(w.w, lut_lo, lut_hi);
-            o0 = make_uint4(a.x, a.y, bb.x, bb.y);
-            o1 = make_uint4(c.x, c.y, d.x, d.y);
         }
-        out[2 * b] = o0;
-        out[2 * b + 1] = o1;
-        sout[off] = (uint8_t)ns;
+        __syncthreads();
+        // expert of this CTA's first row: the last g < num_groups with o_s[g] <= row
+        // (rows at or past o_s[num_groups] stay with the last expert)
+        const int r0 = (int)(b_lo / bpr);
+        int lo = 0, hi = er.num_groups;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (o_s[mid] <= r0) lo = mid;
+            else hi = mid;
+        }
+        g = lo;
+    }
+    const int o_end = GROUPED ? o_s[er.num_groups] : 0;
+    // expert cursor: first row of the next expert, scale row shift of this one
+    int next_row = 0, shift = 0;
+    if (GROUPED) {
+        next_row = g + 1 < er.num_groups ? o_s[g + 1] : INT_MAX;
+        shift = p_s[g] - o_s[g];
+    }
+    // block coordinates (row r, block column j) advance by kRepackThreads
+    // blocks per step without a division
+    const int64_t b_first = b_lo + threadIdx.x;
+    uint32_t r = (uint32_t)(b_first / bpr);
+    uint32_t j = (uint32_t)(b_first - (int64_t)r * bpr);
+    const uint32_t dq = (uint32_t)kRepackThreads / bpr, dr = (uint32_t)kRepackThreads % bpr;
+    for (int64_t b0 = b_first; b0 < b_hi; b0 += kRepackUnroll * kRepackThreads) {
+        uint4 w[kRepackUnroll];
+        uint32_t s[kRepackUnroll], rr[kRepackUnroll], jj[kRepackUnroll];
+#pragma unroll
+        for (int u = 0; u < kRepackUnroll; ++u) {
+            const int64_t b = b0 + u * kRepackThreads;
+            rr[u] = r;
+            jj[u] = j;
+            if (b < b_hi) {
+                w[u] = in[b];
+                s[u] = sin[sf_offset(r, j, s_tiles)];
+            }
+            j += dr;
+            r += dq;
+            if (j >= bpr) { j -= bpr; ++r; }
+        }
+#pragma unroll
+        for (int u = 0; u < kRepackUnroll; ++u) {
+            const int64_t b = b0 + u * kRepackThreads;
+            if (b >= b_hi) break;
+            uint4 o0, o1;
+            uint32_t ns;
+            repack_block(w[u], s[u], o0, o1, ns);
+            if (WIDE) {
+                st_global_32B(out + 2 * b, o0, o1);
+            } else {
+                out[2 * b] = o0;
+                out[2 * b + 1] = o1;
+            }
+            if (GROUPED) {
+                while ((int)rr[u] >= next_row) {
+                    ++g;
+                    next_row = g + 1 < er.num_groups ? o_s[g + 1] : INT_MAX;
+                    shift = p_s[g] - o_s[g];
+                }
+                if ((int)rr[u] < o_end) {
+                    const int64_t off_out = sf_offset((int64_t)rr[u] + shift, jj[u], s_tiles);
+                    sout[off_out] = (uint8_t)ns;
+                    if (jj[u] == bpr - 1)      // pad columns of the row's last 4-column group
+                        for (int c = 1; c < (int)(4 * s_tiles - bpr) + 1; ++c) sout[off_out + c] = 0;
+                }
+            } else {
+                sout[sf_offset(rr[u], jj[u], s_tiles)] = (uint8_t)ns;
+            }
+        }
+    }
+    if (GROUPED) {
+        // rows from an expert's last row up to its next 128-row boundary
+        for (int gg = (int)blockIdx.x; gg < er.num_groups; gg += (int)gridDim.x) {
+            const int first = p_s[gg] + (o_s[gg + 1] - o_s[gg]);
+            const int units = (p_s[gg + 1] - first) * (int)s_tiles;
+            for (int t = (int)threadIdx.x; t < units; t += kRepackThreads) {
+                const int row = first + t / (int)s_tiles, cg = t % (int)s_tiles;
+                *reinterpret_cast<uint32_t*>(sout + sf_offset(row, 4 * cg, s_tiles)) = 0u;
+            }
+        }
+        // whole tiles past the last expert (p_s[num_groups] is a multiple of 128)
+        const int64_t tail_lo = (int64_t)(p_s[er.num_groups] >> 7) * s_tiles * 512;
+        const int64_t n16 = (cap_bytes - tail_lo) / 16;
+        uint4* tail = reinterpret_cast<uint4*>(sout + tail_lo);
+        for (int64_t i = (int64_t)blockIdx.x * kRepackThreads + threadIdx.x; i < n16;
+             i += (int64_t)gridDim.x * kRepackThreads)
+            tail[i] = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
@@ -89,13 +235,40 @@ cudaError_t run_repack(const RepackArgs& a, cudaStream_t st) {
     cudaError_t e;
     if (a.scales_pad && (e = cudaMemsetAsync(a.out_scales, 0, a.scales_bytes, st)) != cudaSuccess) return e;
     const int64_t nblocks = a.rows * (a.cols / 32);
-    int64_t grid = (nblocks + 255) / 256;
-    if (grid > (int64_t)a.num_sms * 16) grid = (int64_t)a.num_sms * 16;
+    // one wave: as many CTAs as are resident on the SMs at once, each a
+    // contiguous range of whole warps' worth of blocks
+    const bool wide = (reinterpret_cast<uintptr_t>(a.out_codes) & 31) == 0;
+    const int variant = (a.num_groups > 0 ? 2 : 0) + (wide ? 1 : 0);
+    static int resident[4] = {0, 0, 0, 0};
+    int& res = resident[variant];
+    if (res == 0) {
+        cudaError_t oe;
+        switch (variant) {
+            case 0: oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&res, repack_kernel<false, false>, kRepackThreads, 0); break;
+            case 1: oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&res, repack_kernel<false, true>, kRepackThreads, 0); break;
+            case 2: oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&res, repack_kernel<true, false>, kRepackThreads, 0); break;
+            default: oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&res, repack_kernel<true, true>, kRepackThreads, 0); break;
+        }
+        if (oe != cudaSuccess || res < 1) res = 1;
+    }
+    int64_t grid = (int64_t)a.num_sms * res;
+    const int64_t per_min = kRepackThreads;
+    if (grid * per_min > nblocks) grid = (nblocks + per_min - 1) / per_min;
     if (grid < 1) grid = 1;
+    int64_t per_cta = (nblocks + grid - 1) / grid;
+    per_cta = (per_cta + 31) / 32 * 32;
     const uint32_t bpr = (uint32_t)(a.cols / 32);
-    repack_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(a.in_codes), a.in_scales,
-                                                 reinterpret_cast<uint4*>(a.out_codes), a.out_scales, nblocks,
-                                                 bpr, (bpr + 3) / 4);
+    const ExpertRows er{a.offsets, a.num_groups};
+    const uint4* in = reinterpret_cast<const uint4*>(a.in_codes);
+    uint4* out = reinterpret_cast<uint4*>(a.out_codes);
+    const int64_t st_ = (bpr + 3) / 4, cap = (int64_t)a.scales_bytes;
+    const dim3 g((unsigned)grid), b(kRepackThreads);
+    switch (variant) {
+        case 0: repack_kernel<false, false><<<g, b, 0, st>>>(in, a.in_scales, out, a.out_scales, nblocks, per_cta, bpr, st_, a.rows, er, 0); break;
+        case 1: repack_kernel<false, true><<<g, b, 0, st>>>(in, a.in_scales, out, a.out_scales, nblocks, per_cta, bpr, st_, a.rows, er, 0); break;
+        case 2: repack_kernel<true, false><<<g, b, 0, st>>>(in, a.in_scales, out, a.out_scales, nblocks, per_cta, bpr, st_, a.rows, er, cap); break;
+        default: repack_kernel<true, true><<<g, b, 0, st>>>(in, a.in_scales, out, a.out_scales, nblocks, per_cta, bpr, st_, a.rows, er, cap); break;
+    }
     return cudaGetLastError();
 }
 

@@ -77,6 +77,7 @@ struct Params {
     const float* ts_b;
     uint32_t idesc;
     int32_t num_groups;
+    int32_t gsf;                   // grouped: A's scales in the per-expert padded layout
     const int64_t* offsets;
     unsigned* status;
     uint64_t timeout_ns;
@@ -117,8 +118,9 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int t, const Grou
         const int cnt = (gt->prefix[g + 1] - gt->prefix[g]) / p.n_tiles;
         const int local = t - gt->prefix[g];
         const int nt = local / cnt, band = gt->band0[g] + local % cnt;
-        ti.a_row0 = band * BM; ti.band = band; ti.b_row0 = g * p.N + nt * BN; ti.n0 = nt * BN;
-        ti.row_lo = max(gt->lo[g], band * BM); ti.row_hi = min(gt->hi[g], band * BM + BM);
+        ti.a_row0 = p.gsf ? gt->lo[g] + (local % cnt) * BM : band * BM;
+        ti.band = band; ti.b_row0 = g * p.N + nt * BN; ti.n0 = nt * BN;
+        ti.row_lo = max(gt->lo[g], ti.a_row0); ti.row_hi = min(gt->hi[g], ti.a_row0 + BM);
         ti.group = g;
     }
     return ti;
@@ -164,13 +166,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
     int total = p.total_tiles;
     if (p.num_groups > 0 && warp == 2 && lane == 0) {
-        int acc = 0;
+        // boundaries clamped to [0, M] and non-decreasing (expert 0 starts at 0)
+        int acc = 0, prev = 0, pband = 0;
         gt->prefix[0] = 0;
         for (int g = 0; g < p.num_groups; g++) {
-            const int lo = clamp_rows(p.offsets[g], 0, p.M);
-            const int hi = clamp_rows(p.offsets[g + 1], lo, p.M);
-            const int b0 = lo / BM, b1 = (hi + BM - 1) / BM;
-            const int cnt = hi > lo ? b1 - b0 : 0;
+            const int lo = prev;
+            const int hi = max(lo, clamp_rows(p.offsets[g + 1], 0, p.M));
+            prev = hi;
+            int b0, cnt;
+            if (p.gsf) {
+                // per-expert padded scale layout: tiles start at the expert's first row
+                cnt = (hi - lo + BM - 1) / BM;
+                b0 = pband;
+                pband += cnt;
+            } else {
+                b0 = lo / BM;
+                cnt = hi > lo ? (hi + BM - 1) / BM - b0 : 0;
+            }
             gt->band0[g] = b0; gt->lo[g] = lo; gt->hi[g] = hi;
             acc += cnt * p.n_tiles;
             gt->prefix[g + 1] = acc;
@@ -429,6 +441,7 @@ cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st) {
     if (fp4) p.idesc = make_idesc(1, 1, false, BM, BN);
     else p.idesc = make_idesc(a.fmt_a == kE5M2 ? 1 : 0, a.fmt_b == kE5M2 ? 1 : 0, true, BM, BN);
     p.num_groups = a.num_groups;
+    p.gsf = a.num_groups > 0 && a.a_grouped_sf;
     p.offsets = a.offsets;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;

@@ -96,6 +96,7 @@ struct Params2 {
     uint32_t idesc;
     int32_t raster, raster_n;
     int32_t num_groups;            // 0 = dense
+    int32_t gsf;                   // grouped: A's scales in the per-expert padded layout
     int32_t group_bands;           // 128-row bands of one expert's B
     const int64_t* offsets;        // grouped: device row offsets, num_groups + 1
     unsigned* status;
@@ -129,7 +130,8 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 // mixes experts and at most half a tile is idle when an expert covers an odd
 // number of bands.
 struct Tile2 {
-    int32_t a_band;        // this CTA's 128-row band of A (also its scale band)
+    int32_t a_row;         // this CTA's first row of A (and of C)
+    int32_t a_band;        // its 128-row band of A's scale tiles
     int32_t nt;            // 256-column tile of C
     int32_t b_row;         // this CTA's first B row
     int32_t sfb_band;      // first of the tile's two B scale bands
@@ -142,6 +144,7 @@ __device__ __forceinline__ Tile2 tile2(const Params2& p, int t, const GroupTable
         int mt, nt;
         tile_mn(p, t, mt, nt);
         ti.a_band = mt * 2 + (int)rank;
+        ti.a_row = ti.a_band * 128;
         ti.nt = nt;
         ti.b_row = nt * BN + (int)rank * 128;
         ti.sfb_band = nt * 2;
@@ -155,10 +158,13 @@ __device__ __forceinline__ Tile2 tile2(const Params2& p, int t, const GroupTable
         const int pi = local % pairs;
         ti.nt = local / pairs;
         ti.a_band = gt->band0[g] + 2 * pi + (int)rank;
+        // plain scale layout: tiles sit on A's own 128-row bands; per-expert
+        // padded layout: tiles start at the expert's first row
+        ti.a_row = p.gsf ? gt->lo[g] + 128 * (2 * pi + (int)rank) : ti.a_band * 128;
         ti.b_row = g * p.N + ti.nt * BN + (int)rank * 128;
         ti.sfb_band = g * p.group_bands + ti.nt * 2;
-        ti.row_lo = max(gt->lo[g], ti.a_band * 128);
-        ti.row_hi = min(gt->hi[g], ti.a_band * 128 + 128);
+        ti.row_lo = max(gt->lo[g], ti.a_row);
+        ti.row_hi = min(gt->hi[g], ti.a_row + 128);
     }
     return ti;
 }
@@ -207,29 +213,45 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     }
     if (warp == 1) tc::tmem_alloc<2>(tc::smem_u32(tmem_slot), kTmemCols);
     if (p.num_groups > 0 && warp == 2) {
-        // expert table, 32 experts per pass; offsets are clamped to [0, M]
-        int carry = 0;
-        for (int g0 = 0; g0 < p.num_groups; g0 += 32) {
+        // Expert table, 32 boundaries per pass.  Boundaries are clamped to
+        // [0, M] and made non-decreasing (running max; expert 0 starts at 0),
+        // so the experts never hold more than M rows in total.  Entry g of a
+        // pass is boundary g; expert g - 1 is [boundary g - 1, boundary g).
+        int carry = 0, bcarry = 0, prev = 0;
+        for (int g0 = 0; g0 <= p.num_groups; g0 += 32) {
             const int g = g0 + lane;
-            int pairs = 0;
-            if (g < p.num_groups) {
-                const int lo = clamp_rows(p.offsets[g], 0, p.M);
-                const int hi = clamp_rows(p.offsets[g + 1], lo, p.M);
-                const int b0 = lo / 128;
-                if (hi > lo) pairs = ((hi - 1) / 128 - b0 + 2) / 2;
-                gt->band0[g] = b0;
-                gt->pairs[g] = pairs;
-                gt->lo[g] = lo;
-                gt->hi[g] = hi;
-            }
-            int v = pairs * p.n_tiles;
+            int om = (g >= 1 && g <= p.num_groups) ? clamp_rows(p.offsets[g], 0, p.M) : 0;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, v, d);
-                if (lane >= d) v += u;
+                const int u = __shfl_up_sync(0xffffffffu, om, d);
+                if (lane >= d) om = max(om, u);
             }
-            if (g < p.num_groups) gt->prefix[g + 1] = carry + v;
-            carry += __shfl_sync(0xffffffffu, v, 31);
+            om = max(om, prev);
+            const int up = __shfl_up_sync(0xffffffffu, om, 1);
+            const int lo = lane == 0 ? prev : up;
+            const bool expert = g >= 1 && g <= p.num_groups;
+            int nb = 0, pairs = 0;
+            if (expert && om > lo) {
+                nb = (om - lo + 127) / 128;                                  // 128-row tiles of the expert
+                pairs = p.gsf ? (nb + 1) / 2 : ((om - 1) / 128 - lo / 128 + 2) / 2;
+            }
+            int vt = pairs * p.n_tiles, vb = nb;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int ut = __shfl_up_sync(0xffffffffu, vt, d), ub = __shfl_up_sync(0xffffffffu, vb, d);
+                if (lane >= d) { vt += ut; vb += ub; }
+            }
+            if (expert) {
+                const int e = g - 1;
+                gt->lo[e] = lo;
+                gt->hi[e] = om;
+                gt->pairs[e] = pairs;
+                gt->band0[e] = p.gsf ? bcarry + vb - nb : lo / 128;     // padded layout: 128-row tiles per expert
+                gt->prefix[e + 1] = carry + vt;
+            }
+            carry += __shfl_sync(0xffffffffu, vt, 31);
+            bcarry += __shfl_sync(0xffffffffu, vb, 31);
+            prev = __shfl_sync(0xffffffffu, om, 31);
         }
         if (lane == 0) gt->prefix[0] = 0;
     }
@@ -251,7 +273,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             int gcur = 0;
             for (int t = cid; t < total && ok; t += ncl) {
                 const Tile2 ti = tile2(p, t, gt, gcur, rank);
-                const int arow = ti.a_band * 128, brow = ti.b_row;
+                const int arow = ti.a_row, brow = ti.b_row;
                 for (int kb = 0; kb < p.k_stages; kb++) {
                     if (!tc::mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, p.timeout_ns)) {
                         ok = false;
@@ -422,7 +444,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) tc::mbar_arrive_cluster(tempty_c0);
             // this warp's 32 rows, clipped to the rows the CTA may write
-            const int row0 = ti.a_band * 128 + q * 32;
+            const int row0 = ti.a_row + q * 32;
             const int col0 = ti.nt * BN + h * 128;
             const int lo = max(row0, ti.row_lo), hi = min(row0 + 32, ti.row_hi);
             if (lo >= hi || col0 >= p.N) continue;
@@ -507,6 +529,7 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     p.timeout_ns = a.timeout_ns;
     const bool grouped = a.num_groups > 0;
     p.num_groups = a.num_groups;
+    p.gsf = grouped && a.a_grouped_sf;
     p.offsets = a.offsets;
     p.group_bands = (int32_t)(a.N / 128);
     // raster order: sweep the larger operand past the whole of the smaller one
@@ -528,7 +551,9 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     const int64_t b_rows = grouped ? a.N * a.num_groups : a.N;
     const uint8_t* b_sf = grouped ? a.b_group_scales[0] : a.b_scales;
     if (!tmap::codes_2d(&tb, a.b_codes, b_rows, kbytes, 128)) return cudaErrorInvalidValue;
-    if (!tmap::scales_3d(&tsa, a.a_scales, (a.M + 127) / 128, n_atoms, sf_atoms, 1)) return cudaErrorInvalidValue;
+    // the per-expert padded scale layout spans up to one extra 128-row tile per expert
+    const int64_t a_bands = (a.M + 127) / 128 + (p.gsf ? a.num_groups : 0);
+    if (!tmap::scales_3d(&tsa, a.a_scales, a_bands, n_atoms, sf_atoms, 1)) return cudaErrorInvalidValue;
     if (!tmap::scales_3d(&tsb, b_sf, (b_rows + 127) / 128, n_atoms, sf_atoms, 2)) return cudaErrorInvalidValue;
     // TMA stores of the output when its base and row pitch allow them
     CUtensorMap tcm = ta;

@@ -28,6 +28,9 @@ struct RepackArgs {
     size_t scales_bytes;
     bool scales_pad;
     int num_sms;
+    // per-expert padded scale layout of the output (num_groups = 0: plain)
+    const int64_t* offsets;
+    int num_groups;
 };
 cudaError_t run_repack(const RepackArgs& a, cudaStream_t st);
 // FP4RowToFP8Col: rows, cols = the MXFP4 input's; the output is [cols, rows]
@@ -62,6 +65,7 @@ struct GemmArgs {
     int num_groups;                // 0 = dense
     const int64_t* offsets;        // device
     const uint8_t* const* b_group_scales;   // host array [num_groups]
+    bool a_grouped_sf;             // grouped: A's scales in the per-expert padded layout
     int num_sms;
     unsigned* status;
     uint64_t timeout_ns;

@@ -174,6 +174,36 @@ bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t o
 bsq_status bsq_grouped_gemm(const bsq_tensor* A, const int64_t* group_offsets_dev, int32_t num_groups,
                             const bsq_tensor* B_groups, void* C, int32_t out_type, void* stream);
 
+/* Per-expert padded scale layout of a grouped activation tensor A[rows, cols]
+ * with expert row offsets o (o_0 = 0, non-decreasing, o_G = rows): the scales
+ * of expert g's rows start at scale row P_g = sum over earlier experts of
+ * their row counts rounded up to 128, so no 128x4 scale tile holds two
+ * experts (the tile layout itself is the plain one, over P_G rows; bytes
+ * between experts are zero).  Codes keep their plain row-major layout.
+ * This returns the buffer size that holds it for any offsets:
+ * (ceil(rows/128)*128 + 128*num_groups) * ceil(S/4)*4, S = cols / block;
+ * 0 on a bad format, shape or group count (1..256). */
+size_t bsq_grouped_scales_bytes(int32_t fmt, int64_t rows, int64_t cols, int32_t num_groups);
+
+/* MXFP4 -> MXFP8 re-encode (as bsq_mxfp4_to_mxfp8) whose output scales are
+ * written in the per-expert padded layout for the given DEVICE offsets
+ * (int64[num_groups+1]); out->scales must hold
+ * bsq_grouped_scales_bytes(BSQ_MXFP8_E4M3, rows, cols, num_groups) bytes
+ * (zero-filled by the call).  Offsets are clamped to [0, rows] and made
+ * non-decreasing on the device.  Citation: MoE FP4 page section 2
+ * (FP4RowToFP8Row feeding the per-expert FP8 GEMM). */
+bsq_status bsq_mxfp4_to_mxfp8_grouped(const bsq_tensor* in_mxfp4, bsq_tensor* out_e4m3,
+                                      const int64_t* group_offsets_dev, int32_t num_groups, void* stream);
+
+/* Grouped GEMM as bsq_grouped_gemm, with A's scales in the per-expert padded
+ * layout (as written by bsq_mxfp4_to_mxfp8_grouped).  Output tiles then start
+ * at each expert's first row, so only the last tile of an expert is partly
+ * idle (with the plain layout a 128-row scale tile shared by two experts is
+ * computed for both).  Same formats, limits and errors as
+ * bsq_grouped_gemm. */
+bsq_status bsq_grouped_gemm_padded(const bsq_tensor* A, const int64_t* group_offsets_dev, int32_t num_groups,
+                                   const bsq_tensor* B_groups, void* C, int32_t out_type, void* stream);
+
 /* Direct MXFP4 -> MXFP8 (E4M3) re-encode in the integer domain, same shape
  * and block grid.  Per 32-block with scale exponent e and largest code
  * magnitude exponent e_c: new scale e + e_c - 8 (clamped at -127), every

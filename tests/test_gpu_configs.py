@@ -162,15 +162,22 @@ def test_config5_moe_grouped(bsq):
     c8, s8 = oracle.mxfp4_to_mxfp8_rows(c4, s4)
     assert np.array_equal(_gpu_rows_codes(q8, mr, "mxfp8_e4m3"), c8)
     assert np.array_equal(_gpu_rows_scales(q8, mr, "mxfp8_e4m3"), s8)
-    Y = bsq.grouped_gemm(q8, torch.from_numpy(off).cuda(), bsq.group_views(qw, G), torch.bfloat16)
+    offd = torch.from_numpy(off).cuda()
+    Y = bsq.grouped_gemm(q8, offd, bsq.group_views(qw, G), torch.bfloat16)
+    # the benchmark's path: re-encode with per-expert padded scales, grouped GEMM reading them
+    q8p = bsq.mxfp4_to_mxfp8_grouped(q4, offd, G)
+    assert torch.equal(q8p.codes, q8.codes)
+    Yp = bsq.grouped_gemm(q8p, offd, bsq.group_views(qw, G), torch.bfloat16, padded_scales=True)
     # for each sampled A row, its expert's weights on sampled output columns
     nr = _rows(N, 24)
     groups = np.searchsorted(off, mr, side="right") - 1
-    Yn = Y.index_select(1, torch.from_numpy(nr).cuda())
-    for g in np.unique(groups):
-        sel = np.flatnonzero(groups == g)
-        wr = g * N + nr
-        cw, sw = _check_rows(qw, W[wr], wr, "mxfp8_e4m3", what=f"W_{g}")
-        _check_gemm_samples(Yn, c8[sel], s8[sel], "mxfp8_e4m3", cw, sw, "mxfp8_e4m3", mr[sel], np.arange(len(nr)),
-                            True, f"expert {g}")
+    ncols = torch.from_numpy(nr).cuda()
+    for name, out in (("plain", Y), ("padded", Yp)):
+        Yn = out.index_select(1, ncols)
+        for g in np.unique(groups):
+            sel = np.flatnonzero(groups == g)
+            wr = g * N + nr
+            cw, sw = _check_rows(qw, W[wr], wr, "mxfp8_e4m3", what=f"W_{g}")
+            _check_gemm_samples(Yn, c8[sel], s8[sel], "mxfp8_e4m3", cw, sw, "mxfp8_e4m3", mr[sel],
+                                np.arange(len(nr)), True, f"{name} expert {g}")
     bsq.sync_status()

@@ -135,13 +135,26 @@ def _random_mxfp4(R, C, seed, scale_lo=0, scale_hi=256):
     return codes, scales
 
 
+def _codes_at(out, align):
+    """Give out a code buffer whose address is `align` (16 or 32) modulo 32."""
+    import torch
+    if align == 16:
+        buf = torch.empty(out.codes.numel() + 16, dtype=torch.uint8, device=out.codes.device)
+        out.codes = buf[16:]
+        assert out.codes.data_ptr() % 32 == 16
+    return out
+
+
 @pytest.mark.parametrize("shape", [(64, 256), (130, 96), (1, 32), (300, 7168)])
-def test_repack_bitexact(bsq, shape):
+@pytest.mark.parametrize("align", [32, 16])
+def test_repack_bitexact(bsq, shape, align):
+    """Both store paths: 32-byte stores (aligned output) and 16-byte halves."""
     R, C = shape
     codes, scales = _random_mxfp4(R, C, R + C)
     scales.ravel()[:12] = [0, 1, 2, 5, 6, 7, 8, 9, 250, 253, 254, 255][:scales.size]
     q = upload_q(bsq, "mxfp4", codes, scales)
-    out = bsq.mxfp4_to_mxfp8(q)
+    out = _codes_at(bsq.empty("mxfp8_e4m3", R, C), align)
+    bsq.mxfp4_to_mxfp8_into(q, out)
     c8, s8 = oracle.mxfp4_to_mxfp8_rows(codes, scales)
     assert_qtensor_equal(out, (c8, oracle.swizzle_scales(s8), None), f"repack {shape}")
 
@@ -413,3 +426,64 @@ def test_gemm_pair_tile_tails(bsq):
         xb = inputs.normal_bf16((N, K), 9, std=0.02)
         _check_gemm(bsq, xa, "mxfp8_e4m3", xb, "mxfp8_e4m3", "f32")
         _check_gemm(bsq, xa, "nvfp4", xb, "nvfp4", "bf16")
+
+
+# ------------------------------------------------ per-expert padded scales
+def _padded_capacity(R, G):
+    return (R + 127) // 128 * 128 + 128 * G
+
+
+@pytest.mark.parametrize("case", sorted(GROUPED_CASES))
+@pytest.mark.parametrize("align", [32, 16])
+def test_repack_grouped_scale_layout(bsq, case, align):
+    import torch
+    counts, N, K = GROUPED_CASES[case]
+    off = inputs.group_offsets(counts)
+    R = int(off[-1])
+    x = inputs.normal_bf16((R, K), 23)
+    c4, s4 = oracle.mx_quantize_rows(x, "mxfp4")
+    q4 = upload_q(bsq, "mxfp4", c4, s4)
+    # stale bytes in the whole buffer: every byte of the capacity is written by the call
+    q8 = _codes_at(bsq.empty_grouped("mxfp8_e4m3", R, K, len(counts)), align)
+    q8.scales.fill_(0xAB)
+    q8.codes.fill_(0xAB)
+    bsq.mxfp4_to_mxfp8_grouped_into(q4, q8, torch.from_numpy(off).cuda(), len(counts))
+    c8, s8 = oracle.mxfp4_to_mxfp8_rows(c4, s4)
+    assert np.array_equal(host_u8(q8.codes).reshape(R, K), c8)
+    exp = oracle.swizzle_scales_grouped(s8, off, _padded_capacity(R, len(counts)))
+    assert q8.scales.numel() == exp.size
+    got = host_u8(q8.scales)
+    assert np.array_equal(got, exp), f"{(got != exp).sum()} scale bytes differ"
+
+
+@pytest.mark.parametrize("case", sorted(GROUPED_CASES))
+@pytest.mark.parametrize("path", ["pair", "single_cta"])
+def test_grouped_gemm_padded_scales(bsq, monkeypatch, case, path):
+    """Grouped GEMM reading A's scales in the per-expert padded layout: tiles
+    start at each expert's first row; results as the oracle, nothing written
+    outside C."""
+    import torch
+    monkeypatch.setenv("BSQ_GEMM_1CTA" if path == "single_cta" else "BSQ_GEMM_GROUPED_PAIR", "1")
+    counts, N, K = GROUPED_CASES[case]
+    G = len(counts)
+    off, ca, sa, cw, sw, Ad, Wd = _grouped_case_oracle(case)
+    R = int(off[-1])
+    A = bsq.empty("mxfp8_e4m3", R, K)
+    A.codes.copy_(dev_u8(ca.ravel()))
+    A.scales = dev_u8(oracle.swizzle_scales_grouped(sa, off, _padded_capacity(R, G)))
+    W = upload_q(bsq, "mxfp8_e4m3", cw, sw)
+    guard = 64
+    buf = torch.full((R + 2 * guard, N), -7.0, dtype=torch.float32, device="cuda")
+    C = buf[guard:guard + R]
+    bsq.grouped_gemm_into(A, torch.from_numpy(off).cuda(), bsq.group_views(W, G), C, padded_scales=True)
+    bsq.sync_status()
+    host = buf.cpu().numpy()
+    assert (host[:guard] == -7.0).all() and (host[guard + R:] == -7.0).all(), "write outside C"
+    Ch = host[guard:guard + R]
+    for g in range(G):
+        lo, hi = off[g], off[g + 1]
+        if hi == lo:
+            continue
+        ref, mag = oracle.gemm_full(Ad[lo:hi], Wd[g * N:(g + 1) * N])
+        ok, err, tol = gemm_tol_ok(Ch[lo:hi], ref, mag, False)
+        assert ok.all(), (case, path, g, int((~ok).sum()))
