@@ -326,9 +326,40 @@ __device__ __forceinline__ uint32_t fp8_of_nibble(uint32_t n, uint32_t sr, uint3
     return fp8_of_nibble_exact(n, (int)sr - (int)sb);
 }
 
+// Fast path helpers.  Two E2M1 pairs (bytes 0 and 1 of w, low nibble
+// first) -> two f16x2 with the low nibble in the low half; the conversion is
+// exact (every E2M1 value is a half).
+__device__ __forceinline__ void h2_of_e2m1x4(uint32_t w, uint32_t& h01, uint32_t& h23) {
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\tmov.b32 {t0, t1, t2, t3}, %2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, t0;\n\tcvt.rn.f16x2.e2m1x2 %1, t1;\n\t}"
+        : "=r"(h01), "=r"(h23)
+        : "r"(w));
+}
+__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// f16x2 -> two E4M3 bytes (low half in the low byte), one rounding (RNE).
+__device__ __forceinline__ uint32_t e4m3x2_of_h2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return r;
+}
+
+// Per-nibble tables for the column maximum, indexed by the magnitude m
+// through a byte permute: lev1 = (m >> 1) + 1 (0 for m = 0), and a high byte
+// 0xFC for m = 0 so that a zero code becomes the 16-bit lane -1024, which
+// no row scale lifts above 0.
+constexpr uint32_t kLev1Lo = 0x02020100u;   // m 0..3 -> 0, 1, 2, 2
+constexpr uint32_t kLev1Hi = 0x04040303u;   // m 4..7 -> 3, 3, 4, 4
+constexpr uint32_t kZeroLo = 0x000000FCu;   // m 0 -> 0xFC, 1..3 -> 0
+constexpr uint32_t kZeroHi = 0x00000000u;
+
 __global__ void __launch_bounds__(kColThreads)
 repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ sin, int64_t R, int64_t C,
-                  int64_t s_tiles_in, uint8_t* __restrict__ out, uint8_t* __restrict__ sout, int64_t s_tiles_out) {
+                  int64_t s_tiles_in, uint8_t* __restrict__ out, uint8_t* __restrict__ sout, int64_t s_tiles_out,
+                  bool wide) {
     __shared__ __align__(16) uint32_t codes[kColRows * 16];    // 256 rows x 64 bytes
     __shared__ __align__(16) uint8_t sf[2 * 512];              // row scales: two 128x4 tiles
     const int tid = threadIdx.x;
@@ -355,52 +386,127 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
     if (c0 + c >= C || r0 + 32 * rb >= R) return;
     const int wi = c >> 3, sh = (c & 7) * 4;            // the word and bit offset of the 4 nibbles
     const uint8_t* srow = sf + (rb >> 2) * 512 + (rb & 3) * 4 + cb;   // + i * 16 for row i of the block
-    // pass 1: per column the largest key (m >> 1) + sr over nonzero codes, and NaN rows
-    uint32_t kmax[4] = {0, 0, 0, 0};
-    bool nan = false;
+    // pass 1: per column the largest key + 1 = (m >> 1) + 1 + sr over nonzero
+    // codes (0 if none), in 16-bit lanes for two columns at a time; the
+    // smallest and largest row scale (a NaN scale is the largest byte)
+    uint32_t acc01 = 0, acc23 = 0, smax = 0, smin = 0xFFu;
 #pragma unroll 8
     for (int i = 0; i < 32; i++) {
         const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
         const uint32_t sr = srow[i * 16];
-        nan |= sr == 0xFFu;
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint32_t m = (nb >> (4 * k)) & 7u;
-            if (m) kmax[k] = max(kmax[k], (m >> 1) + sr);
-        }
+        smax = max(smax, sr);
+        smin = min(smin, sr);
+        const uint32_t sel = nb & 0x7777u;
+        const uint32_t lev = prmt(kLev1Lo, kLev1Hi, sel), zero = prmt(kZeroLo, kZeroHi, sel);
+        const uint32_t sr2 = sr * 0x00010001u;
+        acc01 = __viaddmax_s16x2(prmt(lev, zero, 0x5140u), sr2, acc01);
+        acc23 = __viaddmax_s16x2(prmt(lev, zero, 0x7362u), sr2, acc23);
     }
+    const bool nan = smax == 0xFFu;
+    const uint32_t kp[4] = {acc01 & 0xFFFFu, acc01 >> 16, acc23 & 0xFFFFu, acc23 >> 16};
     // scale bytes: floor(log2 amax) = key - 128, e = that - 8 clamped to [-127, 127]
     uint32_t sb[4];
 #pragma unroll
-    for (int k = 0; k < 4; k++)
-        sb[k] = nan ? 0xFFu : (kmax[k] == 0 ? 0u : (uint32_t)min(max((int)kmax[k] - 9, 0), 254));
-    // pass 2: encode 8 rows at a time, 8 bytes per column per step
-    const int ncols = C - (c0 + c) < 4 ? (int)(C - (c0 + c)) : 4;
+    for (int k = 0; k < 4; k++) sb[k] = nan ? 0xFFu : (uint32_t)min(max((int)kp[k] - 10, 0), 254);
     uint8_t* dst0 = out + (c0 + c) * R + r0 + 32 * rb;
-#pragma unroll 1
-    for (int q = 0; q < 4; q++) {
-        uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
+    // Fast path: each element is code * 2^(sr - sb) exactly, formed as a
+    // half product (E2M1 -> f16x2, times the power of two built from its
+    // exponent field sr - sb + 15) and rounded once by the f16x2 -> E4M3
+    // conversion.  It needs that exponent field in [1, 30] for every row and
+    // column of the block; an all-zero column may take any power, so it
+    // takes the one at the largest row scale.  Other blocks (row scales
+    // spread over more than about 15 binades, or a NaN) take the scalar path.
+    int g[4];
+    bool fast = !nan;
 #pragma unroll
-        for (int h = 0; h < 8; h++) {
-            const int i = 8 * q + h;
-            const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
-            const uint32_t sr = srow[i * 16];
+    for (int k = 0; k < 4; k++) {
+        const int sbp = kp[k] == 0 ? (int)smax - 15 : (int)sb[k];
+        g[k] = 15 - sbp;
+        fast = fast && (int)smax + g[k] <= 30 && (int)smin + g[k] >= 1;
+    }
+    if (fast) {
+        // exponent fields of two columns in 16-bit lanes: sr * 0x00010001 + G,
+        // the low lane's borrow (G < 0) taken back from the high lane, then
+        // shifted into place (all mod 2^32, so one multiply-add per pair)
+        uint32_t G01 = ((uint32_t)g[0] & 0xFFFFu) | ((uint32_t)g[1] << 16);
+        uint32_t G23 = ((uint32_t)g[2] & 0xFFFFu) | ((uint32_t)g[3] << 16);
+        if (g[0] < 0) G01 -= 0x10000u;
+        if (g[2] < 0) G23 -= 0x10000u;
+        G01 <<= 10;
+        G23 <<= 10;
+        uint32_t ow[4][8];            // column k, rows 4 v .. 4 v + 3 in word v
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint32_t W[8];            // row 8 q + h: the E4M3 bytes of the 4 columns
+#pragma unroll
+            for (int h = 0; h < 8; h++) {
+                const int i = 8 * q + h;
+                const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
+                const uint32_t sr = srow[i * 16];
+                uint32_t h01, h23;
+                h2_of_e2m1x4(nb, h01, h23);
+                const uint32_t b01 = e4m3x2_of_h2(hmul2_rn(h01, sr * 0x04000400u + G01));
+                const uint32_t b23 = e4m3x2_of_h2(hmul2_rn(h23, sr * 0x04000400u + G23));
+                W[h] = prmt(b01, b23, 0x5410u);
+            }
+            // 4 x 4 byte transposes: rows -> columns
+            uint32_t lo[4], hi[4];
+#pragma unroll
+            for (int half = 0; half < 2; half++) {
+                const uint32_t* w4 = W + 4 * half;
+                const uint32_t t0 = prmt(w4[0], w4[1], 0x5140u), t1 = prmt(w4[0], w4[1], 0x7362u);
+                const uint32_t t2 = prmt(w4[2], w4[3], 0x5140u), t3 = prmt(w4[2], w4[3], 0x7362u);
+                uint32_t* d = half ? hi : lo;
+                d[0] = prmt(t0, t2, 0x5410u);
+                d[1] = prmt(t0, t2, 0x7632u);
+                d[2] = prmt(t1, t3, 0x5410u);
+                d[3] = prmt(t1, t3, 0x7632u);
+            }
 #pragma unroll
             for (int k = 0; k < 4; k++) {
-                const uint32_t b = fp8_of_nibble((nb >> (4 * k)) & 0xFu, sr, sb[k]) << (8 * (h & 3));
-                if (h < 4) lo[k] |= b;
-                else hi[k] |= b;
+                ow[k][2 * q] = lo[k];
+                ow[k][2 * q + 1] = hi[k];
             }
         }
+        // each column's 32 rows leave as whole 32-byte sectors
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-            if (k < ncols)
+        for (int k = 0; k < 4; k++) {
+            uint8_t* d = dst0 + (int64_t)k * R;
+            if (wide) {
+                asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(d), "r"(ow[k][0]),
+                             "r"(ow[k][1]), "r"(ow[k][2]), "r"(ow[k][3]), "r"(ow[k][4]), "r"(ow[k][5]), "r"(ow[k][6]),
+                             "r"(ow[k][7])
+                             : "memory");
+            } else {
+                reinterpret_cast<uint4*>(d)[0] = make_uint4(ow[k][0], ow[k][1], ow[k][2], ow[k][3]);
+                reinterpret_cast<uint4*>(d)[1] = make_uint4(ow[k][4], ow[k][5], ow[k][6], ow[k][7]);
+            }
+        }
+    } else {
+        // scalar path: the E4M3 byte of each code in the integer domain
+#pragma unroll 1
+        for (int q = 0; q < 4; q++) {
+            uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int h = 0; h < 8; h++) {
+                const int i = 8 * q + h;
+                const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
+                const uint32_t sr = srow[i * 16];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const uint32_t b = fp8_of_nibble((nb >> (4 * k)) & 0xFu, sr, sb[k]) << (8 * (h & 3));
+                    if (h < 4) lo[k] |= b;
+                    else hi[k] |= b;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; k++)
                 *reinterpret_cast<uint2*>(dst0 + (int64_t)k * R + 8 * q) =
                     nan ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu) : make_uint2(lo[k], hi[k]);
+        }
     }
 #pragma unroll
-    for (int k = 0; k < 4; k++)
-        if (k < ncols) sout[sf_offset(c0 + c + k, r0 / 32 + rb, s_tiles_out)] = (uint8_t)sb[k];
+    for (int k = 0; k < 4; k++) sout[sf_offset(c0 + c + k, r0 / 32 + rb, s_tiles_out)] = (uint8_t)sb[k];
 }
 
 cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st) {
@@ -408,8 +514,10 @@ cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st) {
     if (a.scales_pad && (e = cudaMemsetAsync(a.out_scales, 0, a.scales_bytes, st)) != cudaSuccess) return e;
     const int64_t R = a.rows, C = a.cols;
     dim3 grid((unsigned)((C + kColCols - 1) / kColCols), (unsigned)((R + kColRows - 1) / kColRows));
+    // a column chunk (32 rows) starts at a multiple of 32 bytes from the base
+    const bool wide = (reinterpret_cast<uintptr_t>(a.out_codes) & 31) == 0;
     repack_col_kernel<<<grid, kColThreads, 0, st>>>(a.in_codes, a.in_scales, R, C, (C / 32 + 3) / 4, a.out_codes,
-                                                   a.out_scales, (R / 32 + 3) / 4);
+                                                   a.out_scales, (R / 32 + 3) / 4, wide);
     return cudaGetLastError();
 }
 

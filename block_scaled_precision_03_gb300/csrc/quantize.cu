@@ -221,7 +221,15 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
         const int64_t c = base + u * 32 + lane;
         w[u] = c < nchunks ? ld_stream(src + c) : make_uint4(0, 0, 0, 0);
     }
+    // row and block column of this lane's block at u = 0, advanced without a
+    // division: by 32 / LPB blocks per u and by step / LPB per iteration
+    const int64_t blk_first = base / LPB + lane / LPB;
+    uint32_t rb = (uint32_t)(blk_first / blocks_per_row);
+    uint32_t jb = (uint32_t)(blk_first - (int64_t)rb * blocks_per_row);
+    const uint32_t uq = (uint32_t)(32 / LPB) / blocks_per_row, ur = (uint32_t)(32 / LPB) % blocks_per_row;
+    const uint32_t dq = (uint32_t)((step / LPB) / blocks_per_row), dr = (uint32_t)((step / LPB) % blocks_per_row);
     for (; base < nchunks; base += step) {
+        uint32_t r = rb, j = jb;
         uint4 wn[kRowUnroll];
 #pragma unroll
         for (int u = 0; u < kRowUnroll; u++) {
@@ -246,23 +254,25 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
             }
             // scale bytes: gather 4 consecutive blocks into one 32-bit store
             // when a row holds a multiple of 4 blocks, else one byte each.
-            const uint32_t blk = (uint32_t)(c / LPB);
             if (vec_sf) {
                 uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, LPB);
                 uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2 * LPB);
                 uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3 * LPB);
-                if ((lane % (4 * LPB)) == 0 && c < nchunks) {
-                    uint32_t r = blk / blocks_per_row, j = blk - r * blocks_per_row;
+                if ((lane % (4 * LPB)) == 0 && c < nchunks)
                     *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) =
                         sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-                }
             } else if ((lane % LPB) == 0 && c < nchunks) {
-                uint32_t r = blk / blocks_per_row, j = blk - r * blocks_per_row;
                 scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb;
             }
+            j += ur;
+            r += uq;
+            if (j >= blocks_per_row) { j -= blocks_per_row; ++r; }
         }
 #pragma unroll
         for (int u = 0; u < kRowUnroll; u++) w[u] = wn[u];
+        jb += dr;
+        rb += dq;
+        if (jb >= blocks_per_row) { jb -= blocks_per_row; ++rb; }
     }
 }
 
@@ -293,6 +303,12 @@ quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t
     const int64_t step = nwarps * 32 * kNvUnroll;
     uint4 w[kNvUnroll][2];
     int64_t base = warp * 32 * kNvUnroll;
+    static_assert(kNvUnroll == 1, "the block coordinates below advance one block per iteration");
+    // row r and block column j of this lane's block, advanced by `step`
+    // blocks per iteration without a division
+    uint32_t r = (uint32_t)((base + lane) / blocks_per_row);
+    uint32_t j = (uint32_t)(base + lane - (int64_t)r * blocks_per_row);
+    const uint32_t dq = (uint32_t)(step / blocks_per_row), dr = (uint32_t)(step % blocks_per_row);
 #pragma unroll
     for (int u = 0; u < kNvUnroll; u++) {
         const int64_t b = base + u * 32 + lane;
@@ -327,7 +343,6 @@ quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t
             const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
             const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
             if (b < nblocks) {
-                const uint32_t r = (uint32_t)(b / blocks_per_row), j = (uint32_t)(b - (int64_t)r * blocks_per_row);
                 if (vec_sf) {
                     if ((lane & 3) == 0)
                         *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) =
@@ -339,6 +354,9 @@ quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t
         }
 #pragma unroll
         for (int u = 0; u < kNvUnroll; u++) { w[u][0] = wn[u][0]; w[u][1] = wn[u][1]; }
+        j += dr;
+        r += dq;
+        if (j >= blocks_per_row) { j -= blocks_per_row; ++r; }
     }
     if (DELAYED) nv_acc_flush(nv, acc);
 }

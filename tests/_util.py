@@ -51,6 +51,16 @@ def assert_qtensor_equal(q, exp, what=""):
         assert np.float32(got_t) == np.float32(s_t), (what, got_t, s_t)
 
 
+def codes_at(out, align):
+    """Give out a code buffer whose address is `align` (16 or 32) modulo 32."""
+    import torch
+    if align == 16:
+        buf = torch.empty(out.codes.numel() + 16, dtype=torch.uint8, device=out.codes.device)
+        out.codes = buf[16:]
+        assert out.codes.data_ptr() % 32 == 16
+    return out
+
+
 def upload_q(bsq, fmt: str, codes_unpacked: np.ndarray, scales_rowmajor: np.ndarray, s_t=None):
     """Oracle-made quantized tensor -> device QTensor (storage layout)."""
     import torch

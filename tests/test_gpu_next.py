@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 from block_scaled_precision_03_gb300 import inputs
-from _util import dev_bf16, host_u8
+from _util import dev_bf16, host_u8, codes_at
 
 pytestmark = pytest.mark.gpu
 
@@ -128,6 +128,38 @@ def test_fp4_row_to_fp8_col_random_codes_and_scales(bsq, shape):
     out = bsq.mxfp4_to_mxfp8_col(q4)
     c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
     _check_fp8col(out, c8, s8, f"random {shape}")
+    bsq.sync_status()
+
+
+@pytest.mark.parametrize("kind", ["narrow", "spread14", "zero_columns", "sparse", "floor", "mixed"])
+@pytest.mark.parametrize("align", [32, 16])
+def test_fp4_row_to_fp8_col_scale_structures(bsq, kind, align):
+    """Row scales within a few binades (the kernel's fast path, half products),
+    spread to its limit, all-zero columns, sparse codes, scales at the E8M0
+    floor, and blocks of both paths side by side in one launch."""
+    from _util import upload_q
+    R, C = 512, 256
+    rng = np.random.default_rng(len(kind) * 131)
+    c4 = rng.integers(0, 16, (R, C)).astype(np.uint8)
+    base = rng.integers(20, 230, (R // 32, 1))
+    spread = {"narrow": 3, "spread14": 14, "zero_columns": 2, "sparse": 6, "floor": 0, "mixed": 3}[kind]
+    s_row = np.clip(np.repeat(base, 32, axis=0) + rng.integers(-spread, spread + 1, (R, 1)), 0, 254)
+    if kind == "floor":
+        s_row = rng.integers(0, 20, (R, 1))
+    if kind == "zero_columns":
+        c4[:, rng.choice(C, 40, replace=False)] = 0
+        c4[:64, :96] = 8                                  # negative zeros
+    if kind == "sparse":
+        c4[rng.random((R, C)) < 0.7] = 0
+    if kind == "mixed":
+        s_row[::3] = rng.integers(0, 255, (len(s_row[::3]), 1))   # wide spread in some blocks
+        s_row[100] = 0xFF                                          # one NaN row
+    s4 = np.repeat(s_row, C // 32, axis=1).astype(np.uint8)
+    q4 = upload_q(bsq, "mxfp4", c4, s4)
+    out = codes_at(bsq.empty("mxfp8_e4m3", C, R), align)       # both store widths
+    bsq.mxfp4_to_mxfp8_col_into(q4, out)
+    c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
+    _check_fp8col(out, c8, s8, kind)
     bsq.sync_status()
 
 

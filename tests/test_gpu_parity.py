@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 from block_scaled_precision_03_gb300 import inputs
-from _util import (expected, assert_qtensor_equal, dev_bf16, host_u8, dev_u8, upload_q, round_to_bf16,
+from _util import (expected, assert_qtensor_equal, dev_bf16, host_u8, dev_u8, upload_q, round_to_bf16, codes_at,
                    gemm_tol_ok)
 
 pytestmark = pytest.mark.gpu
@@ -135,16 +135,6 @@ def _random_mxfp4(R, C, seed, scale_lo=0, scale_hi=256):
     return codes, scales
 
 
-def _codes_at(out, align):
-    """Give out a code buffer whose address is `align` (16 or 32) modulo 32."""
-    import torch
-    if align == 16:
-        buf = torch.empty(out.codes.numel() + 16, dtype=torch.uint8, device=out.codes.device)
-        out.codes = buf[16:]
-        assert out.codes.data_ptr() % 32 == 16
-    return out
-
-
 @pytest.mark.parametrize("shape", [(64, 256), (130, 96), (1, 32), (300, 7168)])
 @pytest.mark.parametrize("align", [32, 16])
 def test_repack_bitexact(bsq, shape, align):
@@ -153,7 +143,7 @@ def test_repack_bitexact(bsq, shape, align):
     codes, scales = _random_mxfp4(R, C, R + C)
     scales.ravel()[:12] = [0, 1, 2, 5, 6, 7, 8, 9, 250, 253, 254, 255][:scales.size]
     q = upload_q(bsq, "mxfp4", codes, scales)
-    out = _codes_at(bsq.empty("mxfp8_e4m3", R, C), align)
+    out = codes_at(bsq.empty("mxfp8_e4m3", R, C), align)
     bsq.mxfp4_to_mxfp8_into(q, out)
     c8, s8 = oracle.mxfp4_to_mxfp8_rows(codes, scales)
     assert_qtensor_equal(out, (c8, oracle.swizzle_scales(s8), None), f"repack {shape}")
@@ -444,7 +434,7 @@ def test_repack_grouped_scale_layout(bsq, case, align):
     c4, s4 = oracle.mx_quantize_rows(x, "mxfp4")
     q4 = upload_q(bsq, "mxfp4", c4, s4)
     # stale bytes in the whole buffer: every byte of the capacity is written by the call
-    q8 = _codes_at(bsq.empty_grouped("mxfp8_e4m3", R, K, len(counts)), align)
+    q8 = codes_at(bsq.empty_grouped("mxfp8_e4m3", R, K, len(counts)), align)
     q8.scales.fill_(0xAB)
     q8.codes.fill_(0xAB)
     bsq.mxfp4_to_mxfp8_grouped_into(q4, q8, torch.from_numpy(off).cuda(), len(counts))
