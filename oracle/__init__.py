@@ -98,6 +98,8 @@ def _load():
     lib.bsqo_mxfp4_to_mxfp8_rows.argtypes = [p, p, c_i64, c_i64, p, p]
     lib.bsqo_mxfp4_row_to_mxfp8_col.restype = None
     lib.bsqo_mxfp4_row_to_mxfp8_col.argtypes = [p, p, c_i64, c_i64, p, p]
+    lib.bsqo_mxfp4_to_fp8_1x128.restype = None
+    lib.bsqo_mxfp4_to_fp8_1x128.argtypes = [p, p, c_i64, c_i64, p, p]
     lib.bsqo_gemm_pairs.restype = None
     lib.bsqo_gemm_pairs.argtypes = [p, p, c_i64, p, p, c_i64, p, p]
     lib.bsqo_gemm_full.restype = None
@@ -363,6 +365,21 @@ def mxfp4_row_to_mxfp8_col(codes4: np.ndarray, scales4: np.ndarray):
     codes8 = np.empty((C, R), dtype=np.uint8)
     scales8 = np.empty((C, R // 32), dtype=np.uint8)
     _load().bsqo_mxfp4_row_to_mxfp8_col(_ptr(c4), _ptr(s4), R, C, _ptr(codes8), _ptr(scales8))
+    return codes8, scales8
+
+
+def mxfp4_to_fp8_1x128(codes4: np.ndarray, scales4: np.ndarray):
+    """MXFP4 -> FP8 E4M3 with 1x128 blocks (the Hopper FP8 block): the block
+    scale is the largest of the four 32-block E8M0 scales, each element the
+    E4M3 code of its exact value over that scale (codes [R, C] unpacked,
+    scales [R, C/32]).  Returns (codes [R, C], scales [R, ceil(C/128)])."""
+    c4 = np.ascontiguousarray(codes4, dtype=np.uint8)
+    s4 = np.ascontiguousarray(scales4, dtype=np.uint8)
+    R, C = c4.shape
+    assert C % 32 == 0 and s4.shape == (R, C // 32)
+    codes8 = np.empty((R, C), dtype=np.uint8)
+    scales8 = np.empty((R, (C + 127) // 128), dtype=np.uint8)
+    _load().bsqo_mxfp4_to_fp8_1x128(_ptr(c4), _ptr(s4), R, C, _ptr(codes8), _ptr(scales8))
     return codes8, scales8
 
 

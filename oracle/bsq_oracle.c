@@ -362,6 +362,42 @@ void bsqo_mxfp4_row_to_mxfp8_col(const uint8_t* codes4, const uint8_t* scales4, 
         }
 }
 
+/* MXFP4 -> FP8 E4M3 with 1x128 blocks, the FP8 block of the Hopper path
+ * ("Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
+ * section 2, "Algoritmo de Conversao Direta": FP8 blocks hold 128
+ * elements, the conversion takes the largest of the four FP4 block scales
+ * and moves each element's exponent to it).  Readings: the 128-block scale
+ * is the largest E8M0 byte among the (up to four) 32-blocks it covers, kept
+ * as an E8M0 byte; each element is the E4M3 code (RNE) of its exact value
+ * divided by that scale, so it is exact while its own block scale is within
+ * a few binades of the largest and rounds (into E4M3's subnormals, then to
+ * zero) beyond; a NaN scale byte (0xFF, the largest byte) makes the whole
+ * 128-block NaN.
+ *   in:  codes4 [R, C] (one E2M1 code per byte), scales4 [R, C/32] (E8M0)
+ *   out: codes8 [R, C] (E4M3), scales8 [R, ceil(C/128)] (E8M0); C % 32 == 0. */
+void bsqo_mxfp4_to_fp8_1x128(const uint8_t* codes4, const uint8_t* scales4, int64_t R, int64_t C,
+                             uint8_t* codes8, uint8_t* scales8)
+{
+    const int64_t S = C / 32, G = (C + 127) / 128;
+    int64_t r, g, c, j;
+    for (r = 0; r < R; r++)
+        for (g = 0; g < G; g++) {
+            unsigned smax = 0;
+            for (j = 4 * g; j < 4 * g + 4 && j < S; j++)
+                if (scales4[r * S + j] > smax) smax = scales4[r * S + j];
+            scales8[r * G + g] = (uint8_t)smax;
+            for (c = 128 * g; c < 128 * g + 128 && c < C; c++) {
+                if (smax == 0xFFu) {
+                    codes8[r * C + c] = (uint8_t)nan_code(O_E4M3);
+                } else {
+                    const double v = bsqo_decode(O_E2M1, codes4[r * C + c]) *
+                                     bsqo_decode_e8m0(scales4[r * S + c / 32]) / bsqo_decode_e8m0(smax);
+                    codes8[r * C + c] = (uint8_t)bsqo_encode(O_E4M3, v);
+                }
+            }
+        }
+}
+
 void bsqo_gemm_pairs(const double* A, const double* B, int64_t K,
                      const int64_t* ms, const int64_t* ns, int64_t npairs,
                      double* ref, double* mag)

@@ -499,3 +499,82 @@ def test_grouped_scale_layout_rows_and_padding():
         assert P[g] % 128 == 0
     assert not m[~used].any()
     assert buf.size == 1152 * 8 and not buf[oracle.scale_pad_mask(1152, S)].any()
+
+
+# ------------------------------------------------- MXFP4 -> FP8 1x128 blocks
+# E4M3 bytes of the eight E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, worked
+# out by hand from E4M3's fields (bias 7, 3 mantissa bits): 0.5 = 2^-1 ->
+# exponent field 6 -> 0x30; 1.5 = 1.5 * 2^0 -> field 7, mantissa 4 -> 0x3C;
+# 6 = 1.5 * 2^2 -> field 9, mantissa 4 -> 0x4C; the sign is bit 7.
+E4M3_OF_E2M1 = [0x00, 0x30, 0x38, 0x3C, 0x40, 0x44, 0x48, 0x4C]
+
+
+def test_1x128_equal_scales_maps_each_code():
+    # four equal block scales: the 128-block keeps that scale and every E2M1
+    # code becomes the E4M3 code of the same value
+    codes = (np.arange(2 * 256) % 16).astype(np.uint8).reshape(2, 256)
+    scales = np.array([[90] * 8, [200] * 8], np.uint8)
+    c8, s8 = oracle.mxfp4_to_fp8_1x128(codes, scales)
+    assert s8.tolist() == [[90, 90], [200, 200]]
+    want = [E4M3_OF_E2M1[n & 7] | (0x80 if n & 8 else 0) for n in range(16)]
+    assert c8.tolist() == [[want[n] for n in row] for row in codes.tolist()]
+
+
+def test_1x128_scale_is_the_largest_of_four_and_ragged_tail():
+    # C = 160: one full 128-block and a 32-element tail block of its own
+    codes = np.zeros((3, 160), np.uint8)
+    scales = np.array([[10, 13, 12, 11, 7],
+                       [0, 0, 0, 0, 0],
+                       [254, 1, 2, 3, 255]], np.uint8)
+    _, s8 = oracle.mxfp4_to_fp8_1x128(codes, scales)
+    assert s8.tolist() == [[13, 7], [0, 0], [254, 255]]
+
+
+def test_1x128_exact_within_five_binades():
+    # a block whose scale is d <= 5 binades below the largest keeps every value
+    # (0.5 * 2^-5 = 2^-6 is E4M3's smallest normal): dequantizing the output
+    # over the 128-block scale gives back the MXFP4 values
+    rng = np.random.default_rng(60)
+    R, C = 16, 256
+    codes = rng.integers(0, 16, (R, C)).astype(np.uint8)
+    top = rng.integers(20, 230, (R, C // 128))
+    d = rng.integers(0, 6, (R, C // 32))
+    d[:, ::4] = 0                                        # each group holds its largest scale
+    scales = (np.repeat(top, 4, axis=1) - d).astype(np.uint8)
+    c8, s8 = oracle.mxfp4_to_fp8_1x128(codes, scales)
+    v4 = oracle.dequant_rows(codes, scales, "mxfp4")
+    e4m3 = oracle.decode_table(E4M3)
+    v8 = e4m3[c8] * np.repeat(np.exp2(s8.astype(np.float64) - 127.0), 128, axis=1)
+    np.testing.assert_array_equal(v8, v4)
+
+
+def test_1x128_rounding_worked_examples():
+    # one group: block 0 holds the largest scale 140, block 1 sits d binades
+    # below it; each value is code * 2^-d rounded once to E4M3 (subnormal step
+    # 2^-9), the cases below worked by hand
+    cases = [  # (E2M1 code, d, expected E4M3 byte)
+        (0x7, 8, 0x0C),    # 6 * 2^-8 = 1.5 * 2^-6: smallest normal binade, mantissa 4
+        (0x7, 9, 0x06),    # 6 * 2^-9: subnormal 6
+        (0x5, 10, 0x02),   # 3 * 2^-10 = 1.5 * 2^-9: tie between 1 and 2, even -> 2
+        (0x3, 9, 0x02),    # 1.5 * 2^-9: tie -> 2
+        (0x1, 9, 0x00),    # 0.5 * 2^-9 = 2^-10: tie between 0 and 1, even -> 0
+        (0x6, 12, 0x00),   # 4 * 2^-12 = 2^-10: tie -> 0
+        (0x6, 11, 0x01),   # 4 * 2^-11 = 2^-9: the smallest subnormal
+        (0xD, 10, 0x82),   # -3 * 2^-10: tie -> -2 subnormals
+        (0xF, 30, 0x80),   # -6 * 2^-30 rounds to -0
+    ]
+    for code, d, want in cases:
+        codes = np.zeros((1, 128), np.uint8)
+        codes[0, 32] = code
+        scales = np.array([[140, 140 - d, 140, 140]], np.uint8)
+        c8, s8 = oracle.mxfp4_to_fp8_1x128(codes, scales)
+        assert s8[0, 0] == 140 and c8[0, 32] == want, (code, d, hex(c8[0, 32]), hex(want))
+
+
+def test_1x128_nan_scale_poisons_its_block_only():
+    codes = np.full((2, 256), 0x2, np.uint8)           # 1.0 everywhere
+    scales = np.full((2, 8), 127, np.uint8)
+    scales[0, 5] = 0xFF                                # second 128-block of row 0
+    c8, s8 = oracle.mxfp4_to_fp8_1x128(codes, scales)
+    assert s8.tolist() == [[127, 255], [127, 127]]
+    assert (c8[0, 128:] == 0x7F).all() and (c8[0, :128] == 0x38).all() and (c8[1] == 0x38).all()
