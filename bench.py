@@ -209,6 +209,13 @@ class Step:
             o["A8c"] = E("mxfp8_e4m3", m["K"], m["rows"])
             self.extra_ops.append(("fp4row->fp8col A_moe", "NEXT-1", "repack",
                                    lambda: bsq.mxfp4_to_mxfp8_col_into(o["A4"], o["A8c"]), mn * B_REPACK, 0, 1))
+            # NEXT-2: MXFP4 -> FP8 E4M3 with 1x128 blocks (the Hopper FP8 block) of
+            # the MoE activations; read 0.53125 + write 1 + 1/128 B per element
+            o["A8h"] = torch.empty((m["rows"], m["K"]), dtype=torch.uint8, device="cuda")
+            o["A8hs"] = torch.empty((m["rows"], (m["K"] + 127) // 128), dtype=torch.uint8, device="cuda")
+            self.extra_ops.append(("mxfp4->fp8 1x128 A_moe", "NEXT-2", "repack",
+                                   lambda: bsq.mxfp4_to_fp8_1x128_into(o["A4"], o["A8h"], o["A8hs"]),
+                                   mn * (0.5 + 1 / 32 + 1 + 1 / 128), 0, 1))
             # NEXT-4: the MoE GEMM on MXFP4 x MXFP4 natively (weights quantized to
             # MXFP4 as well), against the step's repack + MXFP8 grouped GEMM
             o["Wm4"] = E("mxfp4", m["experts"] * m["N"], m["K"])

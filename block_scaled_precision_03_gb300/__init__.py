@@ -70,6 +70,7 @@ def lib():
         "bsq_mxfp4_to_mxfp8_grouped": (i32, [PT, PT, vp, i32, vp]),
         "bsq_mxfp4_to_mxfp8": (i32, [PT, PT, vp]),
         "bsq_mxfp4_to_mxfp8_col": (i32, [PT, PT, vp]),
+        "bsq_mxfp4_to_fp8_1x128": (i32, [PT, vp, vp, vp]),
         "bsq_sync_status": (i32, [vp]),
         "bsq_debug_timeout_probe": (i32, [ctypes.c_uint64, vp]),
         "bsq_status_string": (ctypes.c_char_p, [i32]),
@@ -283,6 +284,24 @@ def mxfp4_to_mxfp8_grouped(q: QTensor, offsets_dev, groups: int, stream=None) ->
 def mxfp4_to_mxfp8_col_into(q: QTensor, out: QTensor, stream=None):
     ci, co = q.c(), out.c()
     _check(lib().bsq_mxfp4_to_mxfp8_col(ctypes.byref(ci), ctypes.byref(co), _stream(stream)), "bsq_mxfp4_to_mxfp8_col")
+
+
+def mxfp4_to_fp8_1x128_into(q: QTensor, codes, scales, stream=None):
+    """codes: uint8 [rows, cols] E4M3; scales: uint8 [rows, ceil(cols/128)] E8M0."""
+    ci = q.c()
+    _check(lib().bsq_mxfp4_to_fp8_1x128(ctypes.byref(ci), ctypes.c_void_p(codes.data_ptr()),
+                                        ctypes.c_void_p(scales.data_ptr()), _stream(stream)), "bsq_mxfp4_to_fp8_1x128")
+
+
+def mxfp4_to_fp8_1x128(q: QTensor, stream=None):
+    """MXFP4 -> FP8 E4M3 with 1x128 blocks; returns (codes [rows, cols],
+    scales [rows, ceil(cols/128)]), both uint8 on the input's device."""
+    import torch
+    dev = q.codes.device
+    codes = torch.empty((q.rows, q.cols), dtype=torch.uint8, device=dev)
+    scales = torch.empty((q.rows, (q.cols + 127) // 128), dtype=torch.uint8, device=dev)
+    mxfp4_to_fp8_1x128_into(q, codes, scales, stream)
+    return codes, scales
 
 
 def mxfp4_to_mxfp8_col(q: QTensor, stream=None) -> QTensor:

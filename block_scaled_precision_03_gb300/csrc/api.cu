@@ -354,6 +354,23 @@ bsq_status bsq_mxfp4_to_mxfp8_col(const bsq_tensor* in, bsq_tensor* out, void* s
     return from_cuda(bsq::run_repack_col(a, static_cast<cudaStream_t>(stream)));
 }
 
+bsq_status bsq_mxfp4_to_fp8_1x128(const bsq_tensor* in, void* out_codes, void* out_scales, void* stream) {
+    bsq_status s = check_tensor(in, false);
+    if (s != BSQ_OK) return s;
+    if (in->fmt != BSQ_MXFP4_E2M1) return BSQ_ERR_UNSUPPORTED;
+    if (!out_codes || !out_scales) return BSQ_ERR_INVALID_ARG;
+    if (!al16(out_codes)) return BSQ_ERR_ALIGNMENT;
+    bsq::RepackArgs a{};
+    a.in_codes = static_cast<const uint8_t*>(in->codes);
+    a.in_scales = in->scales;
+    a.out_codes = static_cast<uint8_t*>(out_codes);
+    a.out_scales = static_cast<uint8_t*>(out_scales);
+    a.rows = in->rows;
+    a.cols = in->cols;
+    a.num_sms = num_sms();
+    return from_cuda(bsq::run_repack_1x128(a, static_cast<cudaStream_t>(stream)));
+}
+
 bsq_status bsq_sync_status(void* stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return BSQ_ERR_CUDA;

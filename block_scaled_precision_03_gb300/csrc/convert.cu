@@ -273,6 +273,120 @@ cudaError_t run_repack(const RepackArgs& a, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------------------
+// MXFP4 -> FP8 E4M3 with 1 x 128 blocks (same page and section: the Hopper
+// FP8 block holds 128 elements; the conversion takes the largest of the four
+// FP4 block scales and moves each element's exponent to it).  A thread
+// converts one 32-block.  The four scale bytes of its 128-group are one
+// 32-bit word of the tiled layout (scale columns 4g .. 4g + 3 of a row sit
+// side by side); S is their largest byte, s the block's own.  Each value is
+// code * 2^(s - S), formed as an exact half product (E2M1 -> f16x2 times
+// 2^(s - S), a normal half for s - S >= -14; below that every value of the
+// block is under half of E4M3's smallest subnormal, so the power is taken
+// as 0) and rounded once by the f16x2 -> E4M3x2 conversion.  A NaN scale
+// (0xFF, the largest byte) makes the whole group NaN.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void h2_of_e2m1x8(uint32_t w, uint32_t& h0, uint32_t& h1, uint32_t& h2, uint32_t& h3) {
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\tmov.b32 {t0, t1, t2, t3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, t0;\n\tcvt.rn.f16x2.e2m1x2 %1, t1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, t2;\n\tcvt.rn.f16x2.e2m1x2 %3, t3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+}
+__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// f16x2 -> two E4M3 bytes (low half in the low byte), one rounding (RNE).
+__device__ __forceinline__ uint32_t e4m3x2_of_h2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return r;
+}
+// 8 E2M1 codes (element k in nibble k) times the f16x2 power P2 -> 8 E4M3 bytes
+__device__ __forceinline__ uint2 e4m3x8_of_e2m1x8(uint32_t w, uint32_t P2) {
+    uint32_t h0, h1, h2, h3;
+    h2_of_e2m1x8(w, h0, h1, h2, h3);
+    const uint32_t e0 = e4m3x2_of_h2(hmul2_rn(h0, P2)), e1 = e4m3x2_of_h2(hmul2_rn(h1, P2));
+    const uint32_t e2 = e4m3x2_of_h2(hmul2_rn(h2, P2)), e3 = e4m3x2_of_h2(hmul2_rn(h3, P2));
+    return make_uint2(prmt(e0, e1, 0x5410u), prmt(e2, e3, 0x5410u));
+}
+
+template <bool WIDE>
+__global__ void __launch_bounds__(kRepackThreads)
+repack_1x128_kernel(const uint4* __restrict__ in, const uint8_t* __restrict__ sin, uint4* __restrict__ out,
+                    uint8_t* __restrict__ sout, int64_t nblocks, int64_t per_cta, uint32_t bpr, int64_t s_tiles,
+                    uint32_t groups) {
+    const int64_t b_lo = (int64_t)blockIdx.x * per_cta;
+    const int64_t b_hi = min(nblocks, b_lo + per_cta);
+    const int64_t b_first = b_lo + threadIdx.x;
+    uint32_t r = (uint32_t)(b_first / bpr);
+    uint32_t j = (uint32_t)(b_first - (int64_t)r * bpr);
+    const uint32_t dq = (uint32_t)kRepackThreads / bpr, dr = (uint32_t)kRepackThreads % bpr;
+    for (int64_t b = b_first; b < b_hi; b += kRepackThreads) {
+        const uint4 w = in[b];
+        const uint32_t g = j >> 2;
+        uint32_t word = *reinterpret_cast<const uint32_t*>(sin + sf_offset(r, 4 * g, s_tiles));
+        const uint32_t nin = bpr - 4 * g;                  // blocks of this group in the row
+        if (nin < 4) word &= (1u << (8 * nin)) - 1u;
+        const uint32_t m4 = __vmaxu4(word, word >> 16);
+        const uint32_t S = max(m4 & 0xFFu, (m4 >> 8) & 0xFFu);
+        const uint32_t s = (word >> (8 * (j & 3))) & 0xFFu;
+        uint4 o0, o1;
+        if (S == 0xFFu) {
+            o0 = o1 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        } else {
+            const int d = (int)s - (int)S;
+            const uint32_t P = d >= -14 ? (uint32_t)(d + 15) << 10 : 0u;
+            const uint32_t P2 = P | (P << 16);
+            const uint2 a = e4m3x8_of_e2m1x8(w.x, P2), bb = e4m3x8_of_e2m1x8(w.y, P2);
+            const uint2 c = e4m3x8_of_e2m1x8(w.z, P2), dd = e4m3x8_of_e2m1x8(w.w, P2);
+            o0 = make_uint4(a.x, a.y, bb.x, bb.y);
+            o1 = make_uint4(c.x, c.y, dd.x, dd.y);
+        }
+        if (WIDE) {
+            st_global_32B(out + 2 * b, o0, o1);
+        } else {
+            out[2 * b] = o0;
+            out[2 * b + 1] = o1;
+        }
+        if ((j & 3) == 0) sout[(int64_t)r * groups + g] = (uint8_t)S;
+        j += dr;
+        r += dq;
+        if (j >= bpr) { j -= bpr; ++r; }
+    }
+}
+
+cudaError_t run_repack_1x128(const RepackArgs& a, cudaStream_t st) {
+    const int64_t nblocks = a.rows * (a.cols / 32);
+    const bool wide = (reinterpret_cast<uintptr_t>(a.out_codes) & 31) == 0;
+    static int resident[2] = {0, 0};
+    int& res = resident[wide ? 1 : 0];
+    if (res == 0) {
+        const cudaError_t oe =
+            wide ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&res, repack_1x128_kernel<true>, kRepackThreads, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&res, repack_1x128_kernel<false>, kRepackThreads, 0);
+        if (oe != cudaSuccess || res < 1) res = 1;
+    }
+    int64_t grid = (int64_t)a.num_sms * res;
+    if (grid * kRepackThreads > nblocks) grid = (nblocks + kRepackThreads - 1) / kRepackThreads;
+    if (grid < 1) grid = 1;
+    int64_t per_cta = (nblocks + grid - 1) / grid;
+    per_cta = (per_cta + 31) / 32 * 32;
+    const uint32_t bpr = (uint32_t)(a.cols / 32);
+    const uint32_t groups = (bpr + 3) / 4;
+    const uint4* in = reinterpret_cast<const uint4*>(a.in_codes);
+    uint4* out = reinterpret_cast<uint4*>(a.out_codes);
+    if (wide)
+        repack_1x128_kernel<true><<<(unsigned)grid, kRepackThreads, 0, st>>>(in, a.in_scales, out, a.out_scales, nblocks,
+                                                                             per_cta, bpr, (bpr + 3) / 4, groups);
+    else
+        repack_1x128_kernel<false><<<(unsigned)grid, kRepackThreads, 0, st>>>(in, a.in_scales, out, a.out_scales, nblocks,
+                                                                              per_cta, bpr, (bpr + 3) / 4, groups);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // FP4RowToFP8Col (same page and section, kernel FP4RowToFP8Col): dequantize,
 // transpose and re-quantize column-wise to MXFP8 E4M3 in one pass, without a
 // BF16 intermediate.  An E2M1 magnitude index m = 1..7 is a * 2^b with
@@ -334,17 +448,6 @@ __device__ __forceinline__ void h2_of_e2m1x4(uint32_t w, uint32_t& h01, uint32_t
         "cvt.rn.f16x2.e2m1x2 %0, t0;\n\tcvt.rn.f16x2.e2m1x2 %1, t1;\n\t}"
         : "=r"(h01), "=r"(h23)
         : "r"(w));
-}
-__device__ __forceinline__ uint32_t hmul2_rn(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-// f16x2 -> two E4M3 bytes (low half in the low byte), one rounding (RNE).
-__device__ __forceinline__ uint32_t e4m3x2_of_h2(uint32_t h) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
-    return r;
 }
 
 // Per-nibble tables for the column maximum, indexed by the magnitude m

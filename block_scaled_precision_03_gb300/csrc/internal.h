@@ -35,6 +35,9 @@ struct RepackArgs {
 cudaError_t run_repack(const RepackArgs& a, cudaStream_t st);
 // FP4RowToFP8Col: rows, cols = the MXFP4 input's; the output is [cols, rows]
 cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st);
+// MXFP4 -> FP8 E4M3 with 1 x 128 blocks: out_codes [rows, cols], out_scales
+// [rows, ceil(cols / 128)] E8M0 bytes, both row-major
+cudaError_t run_repack_1x128(const RepackArgs& a, cudaStream_t st);
 
 struct DequantArgs {
     int fmt;

@@ -226,6 +226,24 @@ bsq_status bsq_mxfp4_to_mxfp8(const bsq_tensor* in_mxfp4, bsq_tensor* out_e4m3, 
  * gradient). */
 bsq_status bsq_mxfp4_to_mxfp8_col(const bsq_tensor* in_mxfp4, bsq_tensor* out_e4m3, void* stream);
 
+/* MXFP4 -> FP8 E4M3 with 1 x 128 blocks, the FP8 block of the pages'
+ * Hopper path.  Per row, each group of four 32-blocks (128 elements; the
+ * last group of a row may hold fewer) takes the largest of their E8M0 scale
+ * bytes S as its scale, and every element becomes the E4M3 code (RNE) of
+ * its exact value code * 2^(s - 127) over 2^(S - 127), s its own block's
+ * scale.  Exact while s >= S - 5; blocks further below round into E4M3's
+ * subnormals and then to zero.  A NaN scale byte (0xFF) in a group makes
+ * its scale 0xFF and all its codes NaN (0x7F).
+ *   in_mxfp4:   row-wise MXFP4 tensor [rows, cols], cols % 32 == 0 (device)
+ *   out_codes:  DEVICE [rows, cols] E4M3 bytes, row-major, 16-byte aligned
+ *               (BSQ_ERR_ALIGNMENT otherwise), caller-owned
+ *   out_scales: DEVICE [rows, ceil(cols / 128)] E8M0 bytes, row-major,
+ *               caller-owned
+ * Asynchronous on `stream`.  Citation: MoE FP4 page section 2, "Algoritmo
+ * de Conversao Direta" (FP8 blocks of 128, the largest of four FP4 block
+ * scales, exponents adjusted locally). */
+bsq_status bsq_mxfp4_to_fp8_1x128(const bsq_tensor* in_mxfp4, void* out_codes, void* out_scales, void* stream);
+
 /* Synchronize `stream`, read and clear the device status word, and return
  * BSQ_ERR_TIMEOUT if any kernel recorded a timed-out wait since the last
  * call, BSQ_ERR_CUDA if the stream reported an error, else BSQ_OK. */

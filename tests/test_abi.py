@@ -78,3 +78,9 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.bsq_quantize_nvfp4_delayed(ctypes.c_void_p(256), 128, 128, 1, ctypes.byref(t4), None,
                                           ctypes.c_void_p(4098), 16, null) == 3
     assert lib.bsq_quantize_nvfp4_delayed(None, 128, 128, 1, ctypes.byref(t4), None, ctypes.c_void_p(4096), 16, null) == 1
+    # 1x128 re-encode: MXFP4 input, both output pointers, 16-byte aligned codes
+    t5 = bsq.BsqTensorC(2, 0, 64, 256, 256, 512, None)
+    assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(a), ctypes.c_void_p(4096), ctypes.c_void_p(8192), null) == 2
+    assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(t5), None, ctypes.c_void_p(8192), null) == 1
+    assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(t5), ctypes.c_void_p(4096), None, null) == 1
+    assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(t5), ctypes.c_void_p(4104), ctypes.c_void_p(8192), null) == 3

@@ -260,3 +260,59 @@ def test_gemm_mxfp4_single_scale_probe(bsq):
     C = bsq.gemm(upload_q(bsq, "mxfp4", ca, sa), upload_q(bsq, "mxfp4", cb, sb), torch.float32).cpu().numpy()
     ref = 32.0 * (np.exp2(sa.astype(np.float64) - 127) @ np.exp2(sb.astype(np.float64) - 127).T)
     np.testing.assert_array_equal(C, ref.astype(np.float32))
+
+
+# ------------------------------------------------- MXFP4 -> FP8 1x128 blocks
+@pytest.mark.parametrize("shape", [(64, 256), (33, 160), (1, 32), (300, 7168), (129, 4160)])
+@pytest.mark.parametrize("spread", [0, 5, 14, 40, 254])
+def test_1x128_random_codes_and_scales(bsq, shape, spread):
+    """Every nibble; block scales up to `spread` binades below the row's
+    largest (exact, subnormal and flushed shifts); ragged last groups; NaN."""
+    from _util import upload_q
+    R, C = shape
+    rng = np.random.default_rng(R * 131 + C + spread)
+    c4 = rng.integers(0, 16, (R, C)).astype(np.uint8)
+    top = rng.integers(0, 255, (R, 1))
+    s4 = np.clip(top - rng.integers(0, spread + 1, (R, C // 32)), 0, 254).astype(np.uint8)
+    if spread == 40:
+        s4[rng.random(s4.shape) < 0.02] = 0xFF
+    q4 = upload_q(bsq, "mxfp4", c4, s4)
+    codes, scales = bsq.mxfp4_to_fp8_1x128(q4)
+    c8, s8 = oracle.mxfp4_to_fp8_1x128(c4, s4)
+    got = host_u8(codes)
+    bad = np.argwhere(got != c8)
+    assert len(bad) == 0, f"{len(bad)} codes differ, first at {tuple(bad[0])}"
+    assert np.array_equal(host_u8(scales), s8)
+    bsq.sync_status()
+
+
+@pytest.mark.parametrize("align", [32, 16])
+def test_1x128_from_bf16_both_store_widths(bsq, align):
+    # the MoE activations' path: BF16 -> MXFP4 rows (GPU) -> FP8 1x128 (GPU)
+    import torch
+    x = inputs.outlier_activations_bf16((512, 7168), 61)
+    q4, _ = bsq.quantize(dev_bf16(x), "mxfp4", "row")
+    c4, s4 = oracle.mx_quantize_rows(x, "mxfp4")
+    buf = torch.empty(512 * 7168 + 16, dtype=torch.uint8, device="cuda")
+    codes = (buf[16:] if align == 16 else buf[:-16]).view(512, 7168)
+    assert codes.data_ptr() % 32 == (16 if align == 16 else 0)
+    scales = torch.empty((512, 56), dtype=torch.uint8, device="cuda")
+    bsq.mxfp4_to_fp8_1x128_into(q4, codes, scales)
+    c8, s8 = oracle.mxfp4_to_fp8_1x128(c4, s4)
+    assert np.array_equal(host_u8(codes), c8) and np.array_equal(host_u8(scales), s8)
+
+
+def test_1x128_full_size_sampled(bsq):
+    # the MoE activations at full size (32768 x 7168): sampled rows, every group
+    d = inputs.moe_grouped()
+    A = d["A"]
+    q4, _ = bsq.quantize(dev_bf16(A), "mxfp4", "row")
+    codes, scales = bsq.mxfp4_to_fp8_1x128(q4)
+    rows = np.sort(np.random.default_rng(62).choice(32768, 48, replace=False))
+    c4, s4 = oracle.mx_quantize_rows(np.ascontiguousarray(A[rows]), "mxfp4")
+    c8, s8 = oracle.mxfp4_to_fp8_1x128(c4, s4)
+    import torch
+    idx = torch.from_numpy(rows).cuda()
+    assert np.array_equal(host_u8(codes.index_select(0, idx)), c8)
+    assert np.array_equal(host_u8(scales.index_select(0, idx)), s8)
+    bsq.sync_status()
