@@ -52,18 +52,18 @@ __device__ __forceinline__ void repack_block(const uint4 w, const uint32_t s, ui
         o0 = o1 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
         return;
     }
-    // largest magnitude index over the 32 nibbles (value order = code order)
-    uint32_t mx = __vmaxu4(__vmaxu4(w.x & 0x07070707u, (w.x >> 4) & 0x07070707u),
-                           __vmaxu4(w.y & 0x07070707u, (w.y >> 4) & 0x07070707u));
-    mx = __vmaxu4(mx, __vmaxu4(__vmaxu4(w.z & 0x07070707u, (w.z >> 4) & 0x07070707u),
-                               __vmaxu4(w.w & 0x07070707u, (w.w >> 4) & 0x07070707u)));
-    mx = max(max(mx & 0xFF, (mx >> 8) & 0xFF), max((mx >> 16) & 0xFF, mx >> 24));
+    // exponent of the largest magnitude index m (0.5 -> -1, 1|1.5 -> 0, 2|3 -> 1,
+    // 4|6 -> 2) is (m >> 1) - 1, and m >> 1 is 3 if some nibble has bits 1 and
+    // 2 set, else 2 if some nibble has bit 2, else 1 if some has bit 1, else 0:
+    // two OR reductions instead of a byte-wise maximum
+    const uint32_t any = w.x | w.y | w.z | w.w;
+    const uint32_t both = (w.x & (w.x >> 1)) | (w.y & (w.y >> 1)) | (w.z & (w.z >> 1)) | (w.w & (w.w >> 1));
     uint32_t lut_lo = 0, lut_hi = 0;
-    if (mx == 0) {
+    if ((any & 0x77777777u) == 0) {
         ns = 0;                                  // all-zero block: e = -127
     } else {
-        // exponent of the largest magnitude: 0.5 -> -1, 1|1.5 -> 0, 2|3 -> 1, 4|6 -> 2
-        const int e_c = mx == 1 ? -1 : (int)(mx >> 1) - 1;
+        const int lvl = (both & 0x22222222u) ? 3 : (any & 0x44444444u) ? 2 : (any & 0x22222222u) ? 1 : 0;
+        const int e_c = lvl - 1;
         int nb = (int)s + e_c - 8;
         if (nb < 0) nb = 0;
         ns = (uint32_t)nb;
