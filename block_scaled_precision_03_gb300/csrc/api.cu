@@ -283,10 +283,9 @@ bsq_status bsq_grouped_gemm_padded(const bsq_tensor* A, const int64_t* group_off
 }
 
 size_t bsq_grouped_scales_bytes(int32_t fmt, int64_t rows, int64_t cols, int32_t num_groups) {
-    if (num_groups < 1 || num_groups > bsq::kMaxGroups || rows < 0) return 0;
-    const size_t plain = scales_bytes(fmt, rows, cols);
-    if (plain == 0 && rows > 0) return 0;
-    const int64_t s_pad = rows > 0 ? (int64_t)plain / ((rows + 127) / 128 * 128) : 0;
+    if (num_groups < 1 || num_groups > bsq::kMaxGroups) return 0;
+    if (!valid_fmt(fmt) || rows < 0 || cols < 0 || (cols % blk(fmt)) != 0) return 0;
+    const int64_t s_pad = (cols / blk(fmt) + 3) / 4 * 4;
     return (size_t)(((rows + 127) / 128 * 128) + 128 * (int64_t)num_groups) * (size_t)s_pad;
 }
 

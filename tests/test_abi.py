@@ -47,6 +47,29 @@ def test_size_functions(lib):
     assert bsq.codes_bytes(7, 1, 1) == 0
 
 
+def test_grouped_scales_bytes_holds_every_offset_set(lib):
+    # the per-expert padded layout needs sum_g ceil(count_g / 128) * 128 scale
+    # rows (computed by the oracle); the size function's capacity must hold it
+    # for any counts, and it rejects bad group counts and shapes
+    import numpy as np
+    import oracle
+    import block_scaled_precision_03_gb300 as bsq
+    rng = np.random.default_rng(70)
+    for _ in range(200):
+        G = int(rng.integers(1, 257))
+        R = int(rng.integers(1, 5000))
+        S = int(rng.integers(1, 12))
+        cuts = np.sort(rng.integers(0, R + 1, G - 1))
+        off = np.concatenate([[0], cuts, [R]]).astype(np.int64)
+        _, total = oracle.grouped_scale_starts(off)
+        cap = bsq.grouped_scales_bytes("mxfp8_e4m3", R, 32 * S, G)
+        s_pad = (S + 3) // 4 * 4
+        assert cap % (128 * s_pad) == 0 and cap >= total * s_pad, (G, R, S, cap, total)
+    assert bsq.grouped_scales_bytes("mxfp8_e4m3", 1024, 256, 0) == 0
+    assert bsq.grouped_scales_bytes("mxfp8_e4m3", 1024, 256, 257) == 0
+    assert bsq.grouped_scales_bytes("mxfp8_e4m3", 1024, 48, 4) == 0
+
+
 def test_host_argument_checks_launch_nothing(lib):
     import block_scaled_precision_03_gb300 as bsq
     T = bsq.BsqTensorC
