@@ -101,6 +101,24 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.bsq_quantize_nvfp4_delayed(ctypes.c_void_p(256), 128, 128, 1, ctypes.byref(t4), None,
                                           ctypes.c_void_p(4098), 16, null) == 3
     assert lib.bsq_quantize_nvfp4_delayed(None, 128, 128, 1, ctypes.byref(t4), None, ctypes.c_void_p(4096), 16, null) == 1
+    # grouped GEMM: offsets, group count, NVFP4, output type and alignment, and
+    # expert weights that are not consecutive slices of one allocation
+    ga = T(0, 0, 512, 256, 256, 256, None)
+    gb = (T * 2)(T(0, 0, 128, 256, 4096, 8192, None), T(0, 0, 128, 256, 4096 + 128 * 256, 8448, None))
+    C = ctypes.c_void_p(1 << 20)
+    off = ctypes.c_void_p(1 << 16)
+    assert lib.bsq_grouped_gemm(ctypes.byref(ga), None, 2, gb, C, 1, null) == 1
+    assert lib.bsq_grouped_gemm(ctypes.byref(ga), off, 0, gb, C, 1, null) == 1
+    assert lib.bsq_grouped_gemm(ctypes.byref(ga), off, 257, gb, C, 1, null) == 2
+    assert lib.bsq_grouped_gemm(ctypes.byref(ga), off, 2, gb, C, 7, null) == 1
+    assert lib.bsq_grouped_gemm(ctypes.byref(ga), off, 2, gb, ctypes.c_void_p((1 << 20) + 8), 1, null) == 3
+    gbad = (T * 2)(T(0, 0, 128, 256, 4096, 8192, None), T(0, 0, 128, 256, 4096 + 128 * 256 + 16, 8448, None))
+    assert lib.bsq_grouped_gemm(ctypes.byref(ga), off, 2, gbad, C, 1, null) == 2
+    gshape = (T * 2)(T(0, 0, 128, 256, 4096, 8192, None), T(0, 0, 64, 256, 4096 + 128 * 256, 8448, None))
+    assert lib.bsq_grouped_gemm_padded(ctypes.byref(ga), off, 2, gshape, C, 1, null) == 1
+    gnv = T(3, 0, 512, 256, 256, 256, 512)
+    gbnv = (T * 1)(T(3, 0, 128, 256, 4096, 8192, 512))
+    assert lib.bsq_grouped_gemm(ctypes.byref(gnv), off, 1, gbnv, C, 1, null) == 2
     # 1x128 re-encode: MXFP4 input, both output pointers, 16-byte aligned codes
     t5 = bsq.BsqTensorC(2, 0, 64, 256, 256, 512, None)
     assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(a), ctypes.c_void_p(4096), ctypes.c_void_p(8192), null) == 2
