@@ -14,7 +14,13 @@
  *    GEMMs stay on native FP8 tensor cores), dense and grouped over ragged
  *    expert batches (same section, "tensores ragged").
  *  - The direct integer-domain MXFP4 -> MXFP8 re-encode (same section,
- *    "Algoritmo de Conversao Direta"; kernel FP4RowToFP8Row).
+ *    "Algoritmo de Conversao Direta"; kernel FP4RowToFP8Row), also writing
+ *    per-expert padded scales for the grouped GEMM.
+ *  - Around that path: FP4RowToFP8Col (MXFP4 rows to MXFP8 columns in one
+ *    pass, same section, "Kernels"), MXFP4 -> FP8 with 1 x 128 blocks (the
+ *    Hopper FP8 block of the same section), NVFP4 with delayed scaling
+ *    from an amax history (FP8 page, "Estrategias de escalonamento"), and
+ *    the GEMM on MXFP4 x MXFP4 operands natively.
  *
  * Conventions shared by every entry point
  *  - Matrices are row-major.  A GEMM computes C[M,N] = A[M,K] * B[N,K]^T:
@@ -44,7 +50,7 @@
  *    zero codes.
  *
  * Ownership: the caller allocates and frees every buffer (sizes from
- * bsq_codes_bytes / bsq_scales_bytes).  Pointers passed to the compute
+ * bsq_codes_bytes / bsq_scales_bytes / bsq_grouped_scales_bytes).  Pointers passed to the compute
  * calls are DEVICE pointers.  The library keeps no allocation between calls;
  * its only state is a device status word in static device memory.
  *
