@@ -58,7 +58,9 @@
  * compute calls are asynchronous on that stream.
  *
  * Errors: arguments are checked on the host before any launch; on failure
- * the call returns a status, launches nothing and writes nothing.  No C++
+ * the call returns a status, launches nothing and writes nothing.  An empty
+ * tensor (0 rows or 0 columns) is BSQ_ERR_INVALID_ARG; empty experts inside
+ * a grouped batch (equal consecutive offsets) are valid.  No C++
  * exception crosses this boundary.  Faults detected on the device (a wait
  * that exceeded its limit) set the device status word, which
  * bsq_sync_status() returns and clears.

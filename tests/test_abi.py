@@ -119,6 +119,16 @@ def test_host_argument_checks_launch_nothing(lib):
     gnv = T(3, 0, 512, 256, 256, 256, 512)
     gbnv = (T * 1)(T(3, 0, 128, 256, 4096, 8192, 512))
     assert lib.bsq_grouped_gemm(ctypes.byref(gnv), off, 1, gbnv, C, 1, null) == 2
+    # empty tensors are rejected before any launch
+    e0 = T(0, 0, 0, 256, 4096, 8192, None)
+    e4 = T(2, 0, 0, 256, 4096, 8192, None)
+    assert lib.bsq_quantize(ctypes.c_void_p(256), 0, 128, 0, 1, ctypes.byref(e0), None, null) == 1
+    assert lib.bsq_quantize(ctypes.c_void_p(256), 128, 0, 0, 1, ctypes.byref(e0), None, null) == 1
+    assert lib.bsq_dequantize(ctypes.byref(e0), ctypes.c_void_p(1 << 20), 0, null) == 1
+    assert lib.bsq_gemm(ctypes.byref(e0), ctypes.byref(a), ctypes.c_void_p(1 << 20), 0, null) == 1
+    assert lib.bsq_mxfp4_to_mxfp8(ctypes.byref(e4), ctypes.byref(e0), null) == 1
+    assert lib.bsq_mxfp4_to_mxfp8_col(ctypes.byref(e4), ctypes.byref(e0), null) == 1
+    assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(e4), ctypes.c_void_p(4096), ctypes.c_void_p(8192), null) == 1
     # 1x128 re-encode: MXFP4 input, both output pointers, 16-byte aligned codes
     t5 = bsq.BsqTensorC(2, 0, 64, 256, 256, 512, None)
     assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(a), ctypes.c_void_p(4096), ctypes.c_void_p(8192), null) == 2
