@@ -60,7 +60,10 @@
  * Errors: arguments are checked on the host before any launch; on failure
  * the call returns a status, launches nothing and writes nothing.  An empty
  * tensor (0 rows or 0 columns) is BSQ_ERR_INVALID_ARG; empty experts inside
- * a grouped batch (equal consecutive offsets) are valid.  No C++
+ * a grouped batch (equal consecutive offsets) are valid.  The GEMMs and the
+ * grouped re-encode take row counts up to 2^31 - 256 (their kernels index
+ * rows in 32 bits; the grouped GEMM also bounds num_groups x B.rows);
+ * larger ones are BSQ_ERR_UNSUPPORTED.  No C++
  * exception crosses this boundary.  Faults detected on the device (a wait
  * that exceeded its limit) set the device status word, which
  * bsq_sync_status() returns and clears.

@@ -129,6 +129,17 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.bsq_mxfp4_to_mxfp8(ctypes.byref(e4), ctypes.byref(e0), null) == 1
     assert lib.bsq_mxfp4_to_mxfp8_col(ctypes.byref(e4), ctypes.byref(e0), null) == 1
     assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(e4), ctypes.c_void_p(4096), ctypes.c_void_p(8192), null) == 1
+    # row counts past the 32-bit row indexing of the GEMM and grouped kernels
+    big = 0x7FFFFF00 + 32
+    ab = T(0, 0, big, 256, 256, 256, None)
+    assert lib.bsq_gemm(ctypes.byref(ab), ctypes.byref(a), ctypes.c_void_p(1 << 20), 0, null) == 2
+    assert lib.bsq_gemm(ctypes.byref(a), ctypes.byref(ab), ctypes.c_void_p(1 << 20), 0, null) == 2
+    assert lib.bsq_grouped_gemm(ctypes.byref(ab), off, 2, gb, C, 1, null) == 2
+    gbig = (T * 2)(T(0, 0, big // 2, 256, 4096, 8192, None), T(0, 0, big // 2, 256, 4096 + (big // 2) * 256, 8448, None))
+    assert lib.bsq_grouped_gemm(ctypes.byref(ga), off, 2, gbig, C, 1, null) == 2
+    i4 = T(2, 0, big, 256, 256, 256, None)
+    o8 = T(0, 0, big, 256, 4096, 8192, None)
+    assert lib.bsq_mxfp4_to_mxfp8_grouped(ctypes.byref(i4), ctypes.byref(o8), off, 4, null) == 2
     # 1x128 re-encode: MXFP4 input, both output pointers, 16-byte aligned codes
     t5 = bsq.BsqTensorC(2, 0, 64, 256, 256, 512, None)
     assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(a), ctypes.c_void_p(4096), ctypes.c_void_p(8192), null) == 2
