@@ -1,4 +1,9 @@
-// MXFP4 -> MXFP8 (E4M3) direct re-encode and exact dequantization.
+// MXFP4 re-encodes and exact dequantization:
+//   repack_kernel        MXFP4 -> MXFP8 E4M3 rows, plain or with per-expert
+//                        padded scales for the grouped GEMM
+//   repack_1x128_kernel  MXFP4 -> FP8 E4M3 with 1 x 128 blocks
+//   repack_col_kernel    FP4RowToFP8Col: MXFP4 rows -> MXFP8 E4M3 columns
+//   dequant_kernel       any format -> FP32 / BF16, rounded once
 //
 // Re-encode ("Practical FP4 Training for Large-Scale MoE Models on Hopper
 // GPUs", section 2, "Algoritmo de Conversao Direta" and kernel

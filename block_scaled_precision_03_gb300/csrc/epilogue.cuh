@@ -1,6 +1,9 @@
 // GEMM epilogue: one thread owns one output row segment of 128 FP32
 // accumulator values (already moved from TMEM to registers), scales them by
-// alpha (NVFP4 tensor scales) and stores them as BF16 or FP32.
+// alpha (NVFP4 tensor scales) and stores them as BF16 or FP32, either
+// directly (store_row128) or, for whole 32-row boxes, through a warp's
+// 64-byte-swizzled shared staging buffer and one TMA tile store per chunk
+// (store_tile_tma).
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
