@@ -1,7 +1,4 @@
-// Block-scaled GEMM on a CTA pair (tcgen05 cta_group::2), sm_103a: dense,
-// and grouped over ragged expert batches (a tile is two 128-row bands of one
-// expert, from the plain or the per-expert padded scale layout).  MMA kinds:
-// MXFP8 (mxf8f6f4), NVFP4 (mxf4nvf4) and MXFP4 (mxf4).
+// Dense block-scaled GEMM on a CTA pair (tcgen05 cta_group::2), sm_103a.
 //
 // C[M,N] = A[M,K] * B[N,K]^T with per-block scales and FP32 accumulation
 // ("Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
@@ -16,9 +13,8 @@
 // ring holds 3 stages of 256 K-bytes (5 of 128 for NVFP4).  The tcgen05
 // instruction queue is about one MMA deep, so the issuing thread runs in
 // lockstep with the tensor pipe; every barrier handshake costs pipe time,
-// and larger stages (8 MMAs per handshake) amortize it.  Each CTA also
-// keeps the full 256-row B scale tile so its tensor memory holds the scales
-// its half of the MMA reads.
+// and larger stages (8 MMAs per handshake) amortize it.  Each CTA also keeps the full 256-row B scale tile so
+// its tensor memory holds the scales its half of the MMA reads.
 //
 // Roles (both CTAs, 10 warps each):
 //   warp 0      TMA producer: own A / B halves and scale atoms; completion is
