@@ -73,6 +73,7 @@ def lib():
         "bsq_mxfp4_to_fp8_1x128": (i32, [PT, vp, vp, vp]),
         "bsq_sync_status": (i32, [vp]),
         "bsq_debug_timeout_probe": (i32, [ctypes.c_uint64, vp]),
+        "bsq_debug_gemm_timeout": (i32, [PT, PT, vp, i32, ctypes.c_uint64, i32, vp]),
         "bsq_status_string": (ctypes.c_char_p, [i32]),
         "bsq_version": (ctypes.c_char_p, []),
     }
@@ -317,6 +318,17 @@ def sync_status(stream=None):
 
 def debug_timeout_probe(limit_ns: int, stream=None):
     _check(lib().bsq_debug_timeout_probe(limit_ns, _stream(stream)), "bsq_debug_timeout_probe")
+
+
+def debug_gemm_timeout_into(A: QTensor, B: QTensor, C, timeout_ns: int, kernel: int = 0, stream=None):
+    """bsq_gemm into C with every wait of the kernel limited to timeout_ns
+    (test hook for the failure path; see bsq_debug_gemm_timeout)."""
+    import torch
+    ca, cb = A.c(), B.c()
+    st = lib().bsq_debug_gemm_timeout(ctypes.byref(ca), ctypes.byref(cb), ctypes.c_void_p(C.data_ptr()),
+                                      OUT_BF16 if C.dtype == torch.bfloat16 else OUT_F32, timeout_ns, kernel,
+                                      _stream(stream))
+    _check(st, "bsq_debug_gemm_timeout")
 
 
 def version() -> str:

@@ -10,9 +10,13 @@
 
 namespace {
 
-// Device status word: kernels OR failure bits into it; bsq_sync_status reads
-// and clears it.  Lives in static device memory, no allocation.
+// Device status word: kernels OR failure bits into it; bsq_sync_status takes
+// and clears it in one atomic exchange on the device.  Lives in static device
+// memory, no allocation.
 __device__ unsigned g_status_word;
+__device__ unsigned g_status_taken;     // the value the last exchange returned
+
+__global__ void status_take_kernel() { g_status_taken = atomicExch(&g_status_word, 0u); }
 
 int g_num_sms[64];
 
@@ -190,12 +194,17 @@ static bsq_status check_gemm_pair(const bsq_tensor* A, const bsq_tensor* B) {
     return BSQ_ERR_UNSUPPORTED;
 }
 
-bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type, void* stream) {
+// bsq_gemm and bsq_debug_gemm_timeout: checks and launch with a given wait
+// limit; `force_single` selects the 1-CTA kernel.
+static bsq_status gemm_common(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type, uint64_t timeout_ns,
+                              bool force_single, void* stream) {
     bsq_status s = check_gemm_pair(A, B);
     if (s != BSQ_OK) return s;
     if (!C || (out_type != BSQ_OUT_F32 && out_type != BSQ_OUT_BF16)) return BSQ_ERR_INVALID_ARG;
     if (A->rows > 0x7FFFFF00LL || B->rows > 0x7FFFFF00LL) return BSQ_ERR_UNSUPPORTED;
     if (!al16(C)) return BSQ_ERR_ALIGNMENT;
+    // MXFP4 runs on the CTA-pair kernel only
+    if (force_single && A->fmt == BSQ_MXFP4_E2M1) return BSQ_ERR_UNSUPPORTED;
     unsigned* st = status_ptr();
     if (!st) return BSQ_ERR_CUDA;
     bsq::GemmArgs a{};
@@ -213,11 +222,21 @@ bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t o
     a.C = C;
     a.out_bf16 = out_type == BSQ_OUT_BF16;
     a.num_groups = 0;
-    a.single_cta = env_single_cta();
+    a.single_cta = force_single || env_single_cta();
     a.num_sms = num_sms();
     a.status = st;
-    a.timeout_ns = kDefaultTimeoutNs;
+    a.timeout_ns = timeout_ns;
     return from_cuda(bsq::run_gemm(a, static_cast<cudaStream_t>(stream)));
+}
+
+bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type, void* stream) {
+    return gemm_common(A, B, C, out_type, kDefaultTimeoutNs, false, stream);
+}
+
+bsq_status bsq_debug_gemm_timeout(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type,
+                                  uint64_t timeout_ns, int32_t kernel, void* stream) {
+    if (timeout_ns == 0 || timeout_ns > kDefaultTimeoutNs || kernel < 0 || kernel > 1) return BSQ_ERR_INVALID_ARG;
+    return gemm_common(A, B, C, out_type, timeout_ns, kernel == 1, stream);
 }
 
 // bsq_grouped_gemm and bsq_grouped_gemm_padded: checks and launch; `padded`
@@ -371,11 +390,15 @@ bsq_status bsq_mxfp4_to_fp8_1x128(const bsq_tensor* in, void* out_codes, void* o
 }
 
 bsq_status bsq_sync_status(void* stream) {
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return BSQ_ERR_CUDA;
-    unsigned v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)) != cudaSuccess) return BSQ_ERR_CUDA;
-    if (v && cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) return BSQ_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // take-and-clear in one device-side atomic exchange, ordered after the
+    // stream's work; then read the taken value back
+    status_take_kernel<<<1, 1, 0, st>>>();
+    if (cudaGetLastError() != cudaSuccess) return BSQ_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status_taken, sizeof(v), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return BSQ_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BSQ_ERR_CUDA;
     if (v & bsq::kStatusTimeout) return BSQ_ERR_TIMEOUT;
     return BSQ_OK;
 }

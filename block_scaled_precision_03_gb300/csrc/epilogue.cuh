@@ -1,6 +1,8 @@
 // GEMM epilogue: one thread owns one output row segment of 128 FP32
 // accumulator values (already moved from TMEM to registers), scales them by
-// alpha (NVFP4 tensor scales) and stores them as BF16 or FP32, either
+// alpha, then by beta (the two NVFP4 tensor scales, one multiply each, so
+// their product, which can underflow, is never formed), and stores them as
+// BF16 or FP32, either
 // directly (store_row128) or, for whole 32-row boxes, through a warp's
 // 64-byte-swizzled shared staging buffer and one TMA tile store per chunk
 // (store_tile_tma).
@@ -12,7 +14,7 @@
 namespace bsq {
 
 __device__ __forceinline__ void store_row128(const uint32_t (&r)[4][32], void* C, int64_t ldc, int row, int col0,
-                                             int N, int out_bf16, int vec_ok, float alpha) {
+                                             int N, int out_bf16, int vec_ok, float alpha, float beta) {
     if (out_bf16) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(C) + (int64_t)row * ldc + col0;
         if (vec_ok && col0 + 128 <= N) {
@@ -21,8 +23,8 @@ __device__ __forceinline__ void store_row128(const uint32_t (&r)[4][32], void* C
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; e++) {
-                    const float x0 = __uint_as_float(r[j >> 2][(j & 3) * 8 + 2 * e]) * alpha;
-                    const float x1 = __uint_as_float(r[j >> 2][(j & 3) * 8 + 2 * e + 1]) * alpha;
+                    const float x0 = __uint_as_float(r[j >> 2][(j & 3) * 8 + 2 * e]) * alpha * beta;
+                    const float x1 = __uint_as_float(r[j >> 2][(j & 3) * 8 + 2 * e + 1]) * alpha * beta;
                     w[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x0)) |
                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x1)) << 16);
                 }
@@ -31,7 +33,7 @@ __device__ __forceinline__ void store_row128(const uint32_t (&r)[4][32], void* C
         } else {
 #pragma unroll
             for (int j = 0; j < 128; j++)
-                if (col0 + j < N) out[j] = __float2bfloat16_rn(__uint_as_float(r[j >> 5][j & 31]) * alpha);
+                if (col0 + j < N) out[j] = __float2bfloat16_rn(__uint_as_float(r[j >> 5][j & 31]) * alpha * beta);
         }
     } else {
         float* out = reinterpret_cast<float*>(C) + (int64_t)row * ldc + col0;
@@ -39,16 +41,16 @@ __device__ __forceinline__ void store_row128(const uint32_t (&r)[4][32], void* C
 #pragma unroll
             for (int j = 0; j < 32; j++) {
                 float4 v;
-                v.x = __uint_as_float(r[j >> 3][(j & 7) * 4 + 0]) * alpha;
-                v.y = __uint_as_float(r[j >> 3][(j & 7) * 4 + 1]) * alpha;
-                v.z = __uint_as_float(r[j >> 3][(j & 7) * 4 + 2]) * alpha;
-                v.w = __uint_as_float(r[j >> 3][(j & 7) * 4 + 3]) * alpha;
+                v.x = __uint_as_float(r[j >> 3][(j & 7) * 4 + 0]) * alpha * beta;
+                v.y = __uint_as_float(r[j >> 3][(j & 7) * 4 + 1]) * alpha * beta;
+                v.z = __uint_as_float(r[j >> 3][(j & 7) * 4 + 2]) * alpha * beta;
+                v.w = __uint_as_float(r[j >> 3][(j & 7) * 4 + 3]) * alpha * beta;
                 *reinterpret_cast<float4*>(out + 4 * j) = v;
             }
         } else {
 #pragma unroll
             for (int j = 0; j < 128; j++)
-                if (col0 + j < N) out[j] = __uint_as_float(r[j >> 5][j & 31]) * alpha;
+                if (col0 + j < N) out[j] = __uint_as_float(r[j >> 5][j & 31]) * alpha * beta;
         }
     }
 }
@@ -63,7 +65,7 @@ __device__ __forceinline__ void store_row128(const uint32_t (&r)[4][32], void* C
 // output coordinates of the warp's first element.
 template <bool BF16>
 __device__ __forceinline__ void store_tile_tma(const uint32_t (&r)[4][32], uint32_t buf, const void* tmap, int col0,
-                                               int row0, float alpha, int lane) {
+                                               int row0, float alpha, float beta, int lane) {
     constexpr int PER = BF16 ? 32 : 16;                // values per row per chunk
     const uint32_t row_base = buf + (uint32_t)lane * 64u;
     const uint32_t sw = (uint32_t)((lane >> 1) & 3);
@@ -78,13 +80,13 @@ __device__ __forceinline__ void store_tile_tma(const uint32_t (&r)[4][32], uint3
             for (int e = 0; e < 4; e++) {
                 if (BF16) {
                     const int c = ch * 32 + u * 8 + 2 * e;
-                    const float x0 = __uint_as_float(r[c >> 5][c & 31]) * alpha;
-                    const float x1 = __uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]) * alpha;
+                    const float x0 = __uint_as_float(r[c >> 5][c & 31]) * alpha * beta;
+                    const float x1 = __uint_as_float(r[(c + 1) >> 5][(c + 1) & 31]) * alpha * beta;
                     w[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x0)) |
                            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x1)) << 16);
                 } else {
                     const int c = ch * 16 + u * 4 + e;
-                    w[e] = __float_as_uint(__uint_as_float(r[c >> 5][c & 31]) * alpha);
+                    w[e] = __float_as_uint(__uint_as_float(r[c >> 5][c & 31]) * alpha * beta);
                 }
             }
             const uint32_t a = row_base + ((u ^ sw) << 4);

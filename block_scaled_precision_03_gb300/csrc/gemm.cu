@@ -194,13 +194,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (p.num_groups > 0) total = gt->prefix[p.num_groups];
     const uint32_t tmem = *tmem_slot;
 
+    // producer state kept for the drain at exit
+    int stage = 0, issued = 0;
+    uint32_t phase = 0;
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
             int gcur = 0;
-            int issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const TileInfo ti = tile_info(p, t, gt, gcur);
@@ -225,17 +225,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok) {
-                // let the copies already issued land before the CTA exits
-                const int pending = min(issued, STAGES);
-                int s = stage;
-                uint32_t ph = phase;
-                for (int i = 0; i < pending; i++) {
-                    if (--s < 0) { s = STAGES - 1; ph ^= 1; }
-                    volatile int no_abort = 0;
-                    mbar_wait(full0 + 8 * s, ph, &no_abort, nullptr, 100000000ull);
-                }
-            }
+            if (!ok) *abort_flag = 1;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
@@ -330,8 +320,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     if (!ok) break;
                 }
             }
-            if (!ok && any) {
-                // wait for the MMAs already issued before TMEM is released
+            if (!ok) *abort_flag = 1;
+            if (any) {
+                // every MMA issued finishes before TMEM is released (the epilogue,
+                // which otherwise sees the last tile finish, may have given up)
                 commit<1>(drain);
                 volatile int no_abort = 0;
                 mbar_wait(drain, 0, &no_abort, nullptr, 100000000ull);
@@ -341,8 +333,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // ------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int h = (warp - 2) >> 2;          // column half
-        float alpha = 1.0f;
-        if (FP4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+        // NVFP4 tensor scales, applied one after the other (their product alone can underflow)
+        float alpha = 1.0f, beta = 1.0f;
+        if (FP4) {
+            alpha = *p.ts_a;
+            beta = *p.ts_b;
+        }
         int iter = 0, gcur = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++iter) {
             const TileInfo ti = tile_info(p, t, gt, gcur);
@@ -366,16 +362,30 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             if (lo >= hi || col0 >= p.N) continue;
             if (!FP4 && p.tma_store && lo == row0 && hi == row0 + 32) {
                 const uint32_t buf = smem_u32(smOut + (warp - 2) * 2048);
-                if (p.out_bf16) store_tile_tma<true>(r, buf, &tmC, col0, row0, alpha, lane);
-                else store_tile_tma<false>(r, buf, &tmC, col0, row0, alpha, lane);
+                if (p.out_bf16) store_tile_tma<true>(r, buf, &tmC, col0, row0, alpha, beta, lane);
+                else store_tile_tma<false>(r, buf, &tmC, col0, row0, alpha, beta, lane);
             } else if (row0 + lane >= lo && row0 + lane < hi) {
-                store_row128(r, p.C, p.ldc, row0 + lane, col0, p.N, p.out_bf16, p.vec_ok, alpha);
+                store_row128(r, p.C, p.ldc, row0 + lane, col0, p.N, p.out_bf16, p.vec_ok, alpha, beta);
             }
         }
         if (lane == 0) bulk_wait_all();
     }
 
     fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        // some role gave up: the stage loads still in flight (at most the last
+        // STAGES issued; an older stage was reloaded only after it had landed)
+        // land before the CTA exits
+        const int pending = min(issued, STAGES);
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < pending; i++) {
+            if (--s < 0) { s = STAGES - 1; ph ^= 1; }
+            volatile int no_abort = 0;
+            mbar_wait(full0 + 8 * s, ph, &no_abort, nullptr, 100000000ull);
+        }
+    }
     __syncthreads();
     if (warp == 1) {
         fence_after();

@@ -16,14 +16,19 @@
 // and larger stages (8 MMAs per handshake) amortize it.  Each CTA also keeps the full 256-row B scale tile so
 // its tensor memory holds the scales its half of the MMA reads.
 //
-// Roles (both CTAs, 10 warps each):
+// Roles (both CTAs, 11 warps each):
 //   warp 0      TMA producer: own A / B halves and scale atoms; completion is
 //               signalled on the even CTA's stage barrier (cta_group::2 TMA)
-//   warp 1      TMEM owner (both CTAs); the even CTA's lane 0 issues the
-//               scale copies (tcgen05.cp) and MMAs and multicasts commits
+//   warp 1      TMEM owner (both CTAs); the even CTA's lane 0 issues the MMAs
+//               and multicasts the commits that free stages and tiles
 //   warps 2-9   epilogue on each CTA's own 128 accumulator rows
-// Every wait is bounded; a timed-out CTA records the status and exits after
-// its in-flight work drains.
+//   warp 10     the even CTA's lane 0 copies each stage's scales into tensor
+//               memory (tcgen05.cp) as soon as the stage lands, apart from the
+//               MMA thread: a scale copy costs the issuing thread about as
+//               long as an MMA, and from a second thread the copies overlap
+//               with the MMAs instead of queueing between them
+// Every wait is bounded; a CTA that gave up records the status, and before
+// the pair exits every MMA, scale copy and stage load it issued has landed.
 #include <algorithm>
 #include <cuda.h>
 #include "common.cuh"
@@ -39,7 +44,8 @@ constexpr int BN = 256;              // output columns per pair
 constexpr int BKB = 128;             // K bytes per stage
 constexpr int HALF = 128 * BKB;      // 16 KB: one CTA's 128 rows of A (or B)
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kCopyWarp = 2 + kEpiWarps;           // scale-copy issuer
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;
 constexpr int kRasterGroup = 8;      // default tiles per raster group
@@ -118,9 +124,25 @@ __device__ __forceinline__ void tile_mn(const Params2& p, int t, int& mt, int& n
     if (p.raster_n) { mt = b; nt = a; } else { mt = a; nt = b; }
 }
 
-__device__ __forceinline__ void spin_ns(uint64_t ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < ns) {
+// After an abort: the even CTA's producer makes every stage load still in
+// flight land before the pair exits.  Load k (k-th stage load of a CTA) goes
+// to stage k % S, barrier phase (k / S) & 1, on the even CTA; the even CTA
+// arms each load with both CTAs' bytes.  A load one CTA issued and the other
+// did not gets its barrier accounting completed here (the missing half's
+// bytes retired with complete_tx, or the arrival and the odd half's bytes
+// expected), then its phase is awaited with a time limit.  Loads older than
+// the last S of the CTA that issued more have landed already: a stage is
+// reloaded only after the MMAs that read its previous load completed.
+__device__ __noinline__ void drain_pair_loads(uint32_t full0, int S, int n_own, int n_peer, uint32_t cta_tx) {
+    const int n = max(n_own, n_peer);
+    for (int k = max(0, n - S); k < n; k++) {
+        const uint32_t bar = full0 + 8 * (uint32_t)(k % S);
+        const uint32_t parity = (uint32_t)((k / S) & 1);
+        const bool own = k < n_own, peer = k < n_peer;
+        if (own && !peer) tc::mbar_complete_tx(bar, cta_tx);
+        if (peer && !own) tc::mbar_expect_tx(bar, cta_tx);
+        volatile int no_abort = 0;
+        tc::mbar_wait(bar, parity, &no_abort, nullptr, 100000000ull);
     }
 }
 
@@ -184,27 +206,32 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     uint8_t* smOut = smSF + S * CF::SF_STAGE;             // epilogue staging, 2 KB per warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(smOut + kEpiWarps * 2048);
     GroupTable2* gt = reinterpret_cast<GroupTable2*>(bars + 32);
-    // bars: full[S], empty[S], tfull, tempty, drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 3);
+    // bars: full[S], empty[S], sfready[S], tfull, tempty, drain (MMAs), cdrain (scale copies)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* issued_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);   // stage loads this CTA issued
+    static_assert(8 * (3 * S + 4) + 12 <= 256, "barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = tc::cluster_rank();
     const bool leader = rank == 0;
-    const uint32_t full0 = tc::smem_u32(bars), empty0 = tc::smem_u32(bars + S);
-    const uint32_t tfull = tc::smem_u32(bars + 2 * S), tempty = tc::smem_u32(bars + 2 * S + 1);
-    const uint32_t drain = tc::smem_u32(bars + 2 * S + 2);
+    const uint32_t full0 = tc::smem_u32(bars), empty0 = tc::smem_u32(bars + S), sfr0 = tc::smem_u32(bars + 2 * S);
+    const uint32_t tfull = tc::smem_u32(bars + 3 * S), tempty = tc::smem_u32(bars + 3 * S + 1);
+    const uint32_t drain = tc::smem_u32(bars + 3 * S + 2), cdrain = tc::smem_u32(bars + 3 * S + 3);
     const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; s++) {
             tc::mbar_init(full0 + 8 * s, 1);
             tc::mbar_init(empty0 + 8 * s, 1);
+            tc::mbar_init(sfr0 + 8 * s, 1);
         }
         tc::mbar_init(tfull, 1);
         tc::mbar_init(tempty, 2 * kEpiWarps);
         tc::mbar_init(drain, 1);
+        tc::mbar_init(cdrain, 1);
         *abort_flag = 0;
+        *issued_slot = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tc::prefetch_tmap(&tmA);
         tc::prefetch_tmap(&tmB);
@@ -261,7 +288,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total = p.num_groups > 0 ? gt->prefix[p.num_groups] : p.total_tiles;
-    bool aborted = false;
+    const uint32_t sf_t0 = tmem + kSfCol0;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -270,7 +297,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int gcur = 0;
+            int gcur = 0, issued = 0;
             for (int t = cid; t < total && ok; t += ncl) {
                 const Tile2 ti = tile2(p, t, gt, gcur, rank);
                 const int arow = ti.a_row, brow = ti.b_row;
@@ -290,100 +317,42 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     }
                     tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, ti.a_band, fb);
                     tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS, ti.sfb_band, fb);
+                    ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
-            aborted = !ok;
+            *issued_slot = issued;
+            if (!ok) *abort_flag = 1;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
-        // The issuing thread runs in lockstep with the tensor pipe, so the
-        // per-step bookkeeping (test of the next stage's barrier, the next
-        // stage's scale copies, the commit freeing this stage) is spread
-        // between the MMAs of the step, and descriptors advance by plain
-        // additions.
+        // Per stage: wait for the operands (full) and for the stage's scales in
+        // tensor memory (sfready, committed by the scale-copy warp), issue the
+        // stage's MMAs, commit the stage back to the producers.
         if (lane == 0 && leader) {
-            constexpr int MPS = CF::MPS, NCP = 3 * CF::SF_ATOMS;
-            constexpr int CHUNK = (NCP + MPS - 2) / (MPS - 1);      // copies issued after each of MMAs 1..MPS-1
+            constexpr int MPS = CF::MPS;
             constexpr uint32_t OP_STEP = CF::OP_BYTES >> 4, SUB_STEP = HALF >> 4;  // descriptor address units
-            constexpr uint32_t SF_STEP = CF::SF_STAGE >> 4;
             const uint64_t ad_base = tc::desc_sw128(tc::smem_u32(smA));
             const uint64_t bd_base = tc::desc_sw128(tc::smem_u32(smB));
-            const uint64_t sfd_base = tc::desc_sf(tc::smem_u32(smSF));
-            const uint32_t sf_t0 = tmem + kSfCol0;
-            // scale copy c of stage st: atom c / 3, part c % 3 (A; B rows 0-127; B rows 128-255)
-            auto cp_one = [&](int st, int c) {
-                const int a = c / 3, part = c % 3;
-                const uint64_t sd = sfd_base + (uint64_t)(st * SF_STEP);
-                const uint32_t sfa_t = sf_t0 + st * CF::SF_COLS, sfb_t = sfa_t + CF::SFA_COLS;
-                if (part == 0) tc::cp_sf<2>(sfa_t + 4 * a, sd + 32 * a);
-                else tc::cp_sf<2>(sfb_t + 8 * a + 4 * (part - 1),
-                                  sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + a) * 512) >> 4));
-            };
-            // MMA m of a stage: FP8 takes scale byte k of the sub-step's atom
-            // (1X), NVFP4 one atom per MMA (4X), MXFP4 the byte pair 2 (m & 1)
-            // of atom m >> 1 (2X)
-            auto issue_mma = [&](int m, uint64_t adm, uint64_t bdm, uint32_t sfa_t, uint32_t sfb_t, uint32_t acc) {
-                const int sub = m >> 2, k = m & 3;
-                if (KIND == kKindNV) {
-                    tc::mma<2, tc::kMmaNV>(tmem, adm, bdm, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
-                } else if (KIND == kKindMX4) {
-                    const uint32_t id = (uint32_t)(m & 1) * 2u;
-                    tc::mma<2, tc::kMmaMX4>(tmem, adm, bdm, p.idesc | (id << 4) | (id << 29), sfa_t + 4 * (m >> 1),
-                                            sfb_t + 8 * (m >> 1), acc);
-                } else {
-                    tc::mma<2, tc::kMmaFP8>(tmem, adm, bdm, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29),
-                                            sfa_t + 4 * sub, sfb_t + 8 * sub, acc);
-                }
-            };
             int stage = 0;
             uint32_t phase = 0;
             int iter = 0;
             bool ok = true, any = false;
-            if (cid < total) {
-                ok = tc::mbar_wait(full0, 0, abort_flag, p.status, p.timeout_ns);
-                if (ok) {
-                    tc::fence_after();
-#pragma unroll
-                    for (int c = 0; c < NCP; c++) cp_one(0, c);
-                }
-            }
             for (int t = cid; t < total && ok; t += ncl, ++iter) {
                 // both CTAs' epilogue warps arrive here after their TMEM loads completed
                 // (tcgen05.wait::ld); a CTA-scope acquire suffices
                 if (!tc::mbar_wait(tempty, (iter & 1) ^ 1, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
                 tc::fence_after();
-                const bool more_tiles = t + ncl < total;
                 for (int kb = 0; kb < p.k_stages; kb++) {
+                    if (!tc::mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns) ||
+                        !tc::mbar_wait(sfr0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
                     const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + CF::SFA_COLS;
                     const uint64_t ad = ad_base + (uint64_t)(stage * OP_STEP), bd = bd_base + (uint64_t)(stage * OP_STEP);
                     const int nk = kb == p.k_stages - 1 ? p.mma_last : MPS;
-                    int nstage = stage + 1;
-                    uint32_t nphase = phase;
-                    if (nstage == S) { nstage = 0; nphase ^= 1; }
-                    const bool has_next = kb + 1 < p.k_stages || more_tiles;
-                    bool ready = false;
-                    if (nk == MPS && has_next) {
-                        // common step: no tail, a next stage exists -- straight-line issue
-#pragma unroll
-                        for (int m = 0; m < MPS; m++) {
-                            const int sub = m >> 2, k = m & 3;
-                            const uint64_t adm = ad + sub * SUB_STEP + 2 * k, bdm = bd + sub * SUB_STEP + 2 * k;
-                            const uint32_t acc = m == 0 ? (uint32_t)(kb != 0) : 1u;
-                            issue_mma(m, adm, bdm, sfa_t, sfb_t, acc);
-                            if (m == 0) {
-                                ready = tc::mbar_test(full0 + 8 * nstage, nphase);
-                            } else {
-                                if (m == 1) {
-                                    if (!ready && !tc::mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status,
-                                                                 p.timeout_ns)) { ok = false; break; }
-                                    tc::fence_after();
-                                }
-#pragma unroll
-                                for (int c = (m - 1) * CHUNK; c < m * CHUNK && c < NCP; c++) cp_one(nstage, c);
-                            }
-                        }
-                    } else
 #pragma unroll
                     for (int m = 0; m < MPS; m++) {
                         if (m < nk) {
@@ -391,47 +360,51 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                             // +32 bytes along K inside a 128-byte swizzle row = +2 in the address field
                             const uint64_t adm = ad + sub * SUB_STEP + 2 * k, bdm = bd + sub * SUB_STEP + 2 * k;
                             const uint32_t acc = (kb | m) != 0;
-                            issue_mma(m, adm, bdm, sfa_t, sfb_t, acc);
-                        }
-                        if (!has_next) continue;
-                        if (m == 0) {
-                            ready = tc::mbar_test(full0 + 8 * nstage, nphase);
-                        } else {
-                            if (!ready) {
-                                ready = tc::mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status, p.timeout_ns);
-                                if (!ready) { ok = false; break; }
+                            // FP8 takes scale byte k of the sub-step's atom (1X), NVFP4 one atom
+                            // per MMA (4X), MXFP4 the byte pair 2 (m & 1) of atom m >> 1 (2X)
+                            if (KIND == kKindNV) {
+                                tc::mma<2, tc::kMmaNV>(tmem, adm, bdm, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
+                            } else if (KIND == kKindMX4) {
+                                const uint32_t id = (uint32_t)(m & 1) * 2u;
+                                tc::mma<2, tc::kMmaMX4>(tmem, adm, bdm, p.idesc | (id << 4) | (id << 29),
+                                                        sfa_t + 4 * (m >> 1), sfb_t + 8 * (m >> 1), acc);
+                            } else {
+                                tc::mma<2, tc::kMmaFP8>(tmem, adm, bdm, p.idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29),
+                                                        sfa_t + 4 * sub, sfb_t + 8 * sub, acc);
                             }
-                            if (m == 1) tc::fence_after();
-#pragma unroll
-                            for (int c = (m - 1) * CHUNK; c < m * CHUNK && c < NCP; c++) cp_one(nstage, c);
                         }
                     }
                     any = true;
                     tc::commit<2>(empty0 + 8 * stage, 3);
                     if (kb == p.k_stages - 1) tc::commit<2>(tfull, 3);
-                    stage = nstage;
-                    phase = nphase;
-                    if (!ok) break;
+                    if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
-            if (!ok && any) {
+            if (!ok) *abort_flag = 1;
+            if (any) {
+                // every MMA issued finishes before tensor memory is released (the
+                // epilogue, which otherwise sees the last tile finish, may have given up)
                 tc::commit<2>(drain, 1);
                 volatile int no_abort = 0;
                 tc::mbar_wait(drain, 0, &no_abort, nullptr, 100000000ull);
             }
-            aborted = !ok;
         }
-    } else {
+    } else if (warp < kCopyWarp) {
         // ------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
         const int h = (warp - 2) >> 2;
         const uint32_t tempty_c0 = tc::mapa(tempty, 0);
-        float alpha = 1.0f;
-        if (KIND == kKindNV) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+        // NVFP4: the two tensor scales are applied one after the other, so that
+        // their product is never formed on its own (it can underflow FP32)
+        float alpha = 1.0f, beta = 1.0f;
+        if (KIND == kKindNV) {
+            alpha = *p.ts_a;
+            beta = *p.ts_b;
+        }
         int iter = 0, gcur = 0;
         for (int t = cid; t < total; t += ncl, ++iter) {
             const Tile2 ti = tile2(p, t, gt, gcur, rank);
-            if (!tc::mbar_wait(tfull, iter & 1, abort_flag, p.status, p.timeout_ns)) { aborted = true; break; }
+            if (!tc::mbar_wait(tfull, iter & 1, abort_flag, p.status, p.timeout_ns)) break;
             tc::fence_after();
             uint32_t r[4][32];
             const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(h * 128);
@@ -451,19 +424,75 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             if (p.tma_store && (hi == row0 + 32 || hi == p.M) && lo == row0) {
                 // whole box (rows past M are clipped by the tensor map)
                 const uint32_t buf = tc::smem_u32(smOut + (warp - 2) * 2048);
-                if (p.out_bf16) store_tile_tma<true>(r, buf, &tmC, col0, row0, alpha, lane);
-                else store_tile_tma<false>(r, buf, &tmC, col0, row0, alpha, lane);
+                if (p.out_bf16) store_tile_tma<true>(r, buf, &tmC, col0, row0, alpha, beta, lane);
+                else store_tile_tma<false>(r, buf, &tmC, col0, row0, alpha, beta, lane);
             } else if (row0 + lane >= lo && row0 + lane < hi) {
-                store_row128(r, p.C, p.ldc, row0 + lane, col0, p.N, p.out_bf16, p.vec_ok, alpha);
+                store_row128(r, p.C, p.ldc, row0 + lane, col0, p.N, p.out_bf16, p.vec_ok, alpha, beta);
             }
         }
         if (lane == 0) tc::bulk_wait_all();
+    } else {
+        // ------------------------------------------------ scale copies (even CTA)
+        // Copies each stage's scale atoms from shared memory into the stage's
+        // tensor-memory slot as soon as the stage has landed (a slot is free
+        // once its stage was loaded again: the producer reloads a stage only
+        // after the MMAs that read it completed), then commits sfready.
+        // Issued apart from the MMAs, the copies overlap with them.
+        if (lane == 0 && leader) {
+            constexpr int NCP = 3 * CF::SF_ATOMS;
+            const uint64_t sfd_base = tc::desc_sf(tc::smem_u32(smSF));
+            constexpr uint32_t SF_STEP = CF::SF_STAGE >> 4;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true, any = false;
+            for (int t = cid; t < total && ok; t += ncl) {
+                for (int kb = 0; kb < p.k_stages; kb++) {
+                    if (!tc::mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint64_t sd = sfd_base + (uint64_t)(stage * SF_STEP);
+                    const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + CF::SFA_COLS;
+                    // copy c: atom c / 3, part c % 3 (A; B rows 0-127; B rows 128-255), each
+                    // one 512-byte 128x4 tile broadcast to the four lane quarters
+#pragma unroll
+                    for (int c = 0; c < NCP; c++) {
+                        const int a = c / 3, part = c % 3;
+                        if (part == 0) tc::cp_sf<2>(sfa_t + 4 * a, sd + 32 * a);
+                        else tc::cp_sf<2>(sfb_t + 8 * a + 4 * (part - 1),
+                                          sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + a) * 512) >> 4));
+                    }
+                    tc::commit<2>(sfr0 + 8 * stage, 1);
+                    any = true;
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) *abort_flag = 1;
+            if (any) {
+                // every scale copy issued lands before tensor memory is released
+                tc::commit<2>(cdrain, 1);
+                volatile int no_abort = 0;
+                tc::mbar_wait(cdrain, 0, &no_abort, nullptr, 100000000ull);
+            }
+        }
     }
 
-    // a CTA that gave up lets copies still in flight into its shared memory land
-    if (aborted) spin_ns(200000);
+    // Both CTAs have stopped issuing.  If either gave up, the even CTA waits
+    // (bounded) for every stage load still in flight: all loads report to its
+    // barriers, and a CTA must not exit while copies into its shared memory
+    // or onto its barriers may still land.
     tc::fence_before();
     __syncthreads();
+    tc::cluster_sync();
+    if (leader && warp == 0 && lane == 0) {
+        const int peer_abort = tc::ld_cluster_s32(tc::mapa(tc::smem_u32((const void*)abort_flag), 1));
+        if (*abort_flag || peer_abort) {
+            const int n_own = *issued_slot;
+            const int n_peer = tc::ld_cluster_s32(tc::mapa(tc::smem_u32((const void*)issued_slot), 1));
+            drain_pair_loads(full0, S, n_own, n_peer, CF::CTA_TX);
+        }
+    }
     tc::cluster_sync();
     if (warp == 1) {
         tc::fence_after();

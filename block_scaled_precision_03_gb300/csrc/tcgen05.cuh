@@ -33,6 +33,17 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
 }
+// retire `bytes` of the current phase's transaction count as if they had
+// arrived (used only to settle the accounting of loads that were never issued)
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+// 32-bit load from the shared memory of a CTA of the cluster
+__device__ __forceinline__ int ld_cluster_s32(uint32_t caddr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+    return v;
+}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
@@ -63,28 +74,31 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
                  : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
-// cluster-scope acquire: for barriers that threads of the peer CTA arrive on
-__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+// test of a phase that suspends the thread for at most `hint_ns` (or until
+// the phase completes)
+__device__ __forceinline__ bool mbar_try_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile("{\n\t.reg .pred P;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
                  "selp.u32 %0, 1, 0, P;\n\t}"
-                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
     return ok != 0;
 }
 // Bounded wait, slow path: false when the CTA is aborting or the time limit
-// passed (then the abort flag and the status word are set).
-template <bool CLUSTER>
+// passed (then the abort flag and the status word are set).  The limit counts
+// from the first failed test; each test suspends the thread for at most an
+// eighth of the limit (1 us .. 1 ms), so the clock is read often enough for
+// short limits too.
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                    unsigned* status, uint64_t limit_ns) {
-    uint64_t t0 = 0;
+    const uint64_t t0 = globaltimer_ns();
+    const uint64_t h = limit_ns / 8;
+    const uint32_t hint = (uint32_t)(h < 1000 ? 1000 : (h > 1000000 ? 1000000 : h));
     for (uint32_t it = 0;; ++it) {
-        if (CLUSTER ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-        if ((it & 255u) == 255u) {
+        if (mbar_try_hint(bar, parity, hint)) return true;
+        if ((it & 3u) == 3u) {
             if (*abort_flag) return false;
-            const uint64_t now = globaltimer_ns();
-            if (t0 == 0) t0 = now;
-            else if (now - t0 > limit_ns) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 record_status(status, kStatusTimeout);
                 return false;
@@ -92,12 +106,12 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
         }
     }
 }
-// Bounded wait with an inlined first test (no call when the phase is done).
-template <bool CLUSTER = false>
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status, uint64_t limit_ns) {
-    if (CLUSTER ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-    return mbar_wait_slow<CLUSTER>(bar, parity, abort_flag, status, limit_ns);
+// Bounded wait with an inlined first test that never suspends (no call when
+// the phase is done).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned* status,
+                                          uint64_t limit_ns) {
+    if (mbar_test(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, status, limit_ns);
 }
 
 // ---------------------------------------------------------------------- TMA

@@ -255,9 +255,13 @@ bsq_status bsq_mxfp4_to_mxfp8_col(const bsq_tensor* in_mxfp4, bsq_tensor* out_e4
  * scales, exponents adjusted locally). */
 bsq_status bsq_mxfp4_to_fp8_1x128(const bsq_tensor* in_mxfp4, void* out_codes, void* out_scales, void* stream);
 
-/* Synchronize `stream`, read and clear the device status word, and return
- * BSQ_ERR_TIMEOUT if any kernel recorded a timed-out wait since the last
- * call, BSQ_ERR_CUDA if the stream reported an error, else BSQ_OK. */
+/* Take and clear the device status word (one atomic exchange on the
+ * device, ordered after the work already on `stream`), synchronize
+ * `stream`, and return BSQ_ERR_TIMEOUT if any kernel recorded a timed-out
+ * wait since the word was last taken, BSQ_ERR_CUDA if the stream reported an
+ * error, else BSQ_OK.  The word is shared by every stream of the device: a
+ * timeout recorded by a kernel on another stream is reported by whichever
+ * call takes the word first. */
 bsq_status bsq_sync_status(void* stream);
 
 /* Test hook for the failure path: launches one kernel that waits on a
@@ -265,6 +269,17 @@ bsq_status bsq_sync_status(void* stream);
  * (capped at 1e9) and records BSQ_ERR_TIMEOUT in the status word.  It
  * touches no memory besides the status word. */
 bsq_status bsq_debug_timeout_probe(uint64_t limit_ns, void* stream);
+
+/* Test hook for the GEMM kernels' failure path: bsq_gemm with every wait of
+ * the kernel limited to `timeout_ns` nanoseconds (1 .. 4e9; bsq_gemm uses
+ * 4e9) instead of the default.  With a limit shorter than the GEMM takes,
+ * the kernel gives up part-way: it records BSQ_ERR_TIMEOUT in the status
+ * word, lets every stage load, scale copy and MMA it issued land, releases
+ * tensor memory and exits; C is then partly written.  `kernel` 0 runs the
+ * kernel bsq_gemm would choose, 1 the single-CTA kernel (not for MXFP4,
+ * BSQ_ERR_UNSUPPORTED).  Argument rules and errors as for bsq_gemm. */
+bsq_status bsq_debug_gemm_timeout(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type,
+                                  uint64_t timeout_ns, int32_t kernel, void* stream);
 
 /* Static description of a status code. */
 const char* bsq_status_string(int32_t status);

@@ -146,3 +146,11 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(t5), None, ctypes.c_void_p(8192), null) == 1
     assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(t5), ctypes.c_void_p(4096), None, null) == 1
     assert lib.bsq_mxfp4_to_fp8_1x128(ctypes.byref(t5), ctypes.c_void_p(4104), ctypes.c_void_p(8192), null) == 3
+    # GEMM wait-limit hook: the limit and the kernel selector are checked first
+    C = ctypes.c_void_p(1 << 20)
+    assert lib.bsq_debug_gemm_timeout(ctypes.byref(a), ctypes.byref(a), C, 0, 0, 0, null) == 1
+    assert lib.bsq_debug_gemm_timeout(ctypes.byref(a), ctypes.byref(a), C, 0, 4_000_000_001, 0, null) == 1
+    assert lib.bsq_debug_gemm_timeout(ctypes.byref(a), ctypes.byref(a), C, 0, 1000, 2, null) == 1
+    assert lib.bsq_debug_gemm_timeout(ctypes.byref(a), ctypes.byref(b2), C, 0, 1000, 0, null) == 1
+    m4 = T(2, 0, 128, 256, 256, 256, None)
+    assert lib.bsq_debug_gemm_timeout(ctypes.byref(m4), ctypes.byref(m4), C, 0, 1000, 1, null) == 2

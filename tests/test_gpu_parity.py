@@ -377,6 +377,43 @@ def test_timeout_probe_reports_status(bsq):
     bsq.sync_status()                           # cleared; context still usable
 
 
+@pytest.mark.parametrize("fmt,kernel", [("mxfp8_e4m3", 0), ("nvfp4", 0), ("mxfp4", 0), ("mxfp8_e4m3", 1),
+                                        ("nvfp4", 1)])
+@pytest.mark.parametrize("limit_ns", [2_000, 10_000])
+def test_gemm_wait_limit_runs_out_then_recovers(bsq, fmt, kernel, limit_ns):
+    """A GEMM whose waits are limited to a few microseconds gives up part-way
+    (stage loads, scale copies and MMAs in flight), reports BSQ_ERR_TIMEOUT
+    and leaves the context usable: the next GEMM on the same buffers is
+    exact.  The waits run out; nothing faults."""
+    import torch
+    # a long K: one output tile takes tens of microseconds, far beyond the limit
+    M, N, K = 512, 512, 32768
+    x = inputs.normal_bf16((M, K), 31)
+    w = inputs.normal_bf16((N, K), 32, std=0.02)
+    ca, sa, ta = oracle.quantize_rows(x, fmt)
+    cb, sb, tb = oracle.quantize_rows(w, fmt)
+    A = upload_q(bsq, fmt, ca, sa, ta)
+    B = upload_q(bsq, fmt, cb, sb, tb)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    bsq.sync_status()
+    bsq.debug_gemm_timeout_into(A, B, C, limit_ns, kernel)
+    with pytest.raises(bsq.BsqError) as ei:
+        bsq.sync_status()
+    assert ei.value.status == 5
+    bsq.sync_status()                            # taken and cleared
+    C.fill_(float("nan"))
+    if kernel == 1:
+        bsq.debug_gemm_timeout_into(A, B, C, 4_000_000_000, 1)
+    else:
+        bsq.gemm_into(A, B, C)
+    bsq.sync_status()
+    rows = np.arange(0, M, 7)
+    Csub = C[torch.from_numpy(rows).cuda()].cpu().numpy()
+    ref, mag = oracle.gemm_full(oracle.dequant_rows(ca[rows], sa[rows], fmt, ta), oracle.dequant_rows(cb, sb, fmt, tb))
+    ok, err, tol = gemm_tol_ok(Csub, ref, mag, False)
+    assert ok.all(), f"{(~ok).sum()} outputs outside the bound after the timed-out GEMM"
+
+
 def test_quantize_rejects_unaligned_cols(bsq):
     x = inputs.normal_bf16((96, 130), 1)
     with pytest.raises(bsq.BsqError) as ei:
