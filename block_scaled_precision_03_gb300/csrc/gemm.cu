@@ -12,14 +12,15 @@
 //   warp 0      TMA producer: A tile 128 x 128 B and B tile 256 x 128 B per
 //               stage (128-byte swizzle) plus the stage's scale atoms (bulk
 //               copies of 512-byte 128x4 tiles), into a 4-stage smem ring.
-//   warp 1      TMEM owner and MMA issuer: per stage copies the scale atoms
-//               into a per-stage TMEM slot (tcgen05.cp 32x128b.warpx4) and
-//               issues four tcgen05.mma ... block_scale with M=128, N=256;
-//               commits free the smem stage and, per tile, signal the
-//               epilogue.
+//   warp 1      TMEM owner and MMA issuer: per stage four tcgen05.mma ...
+//               block_scale with M=128, N=256; commits free the smem stage
+//               and, per tile, signal the epilogue.
 //   warps 2-9   epilogue: drain the 128 x 256 FP32 accumulator from TMEM to
 //               registers, release TMEM to the MMA warp, then scale (NVFP4
 //               tensor scales), convert and store C.
+//   warp 10     scale copies: each stage's atoms into a per-stage TMEM slot
+//               (tcgen05.cp 32x128b.warpx4) as soon as the stage lands, apart
+//               from the MMA thread so that copies and MMAs overlap.
 // Every wait is bounded: past the time limit the kernel records a timeout in
 // the status word, drains its own in-flight copies and MMAs and exits.
 #include <cuda.h>
@@ -38,7 +39,8 @@ constexpr int BN = 256;            // tile columns (B rows)
 constexpr int BKB = 128;           // K bytes per stage (one 128-byte swizzle row)
 constexpr int STAGES = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kCopyWarp = 2 + kEpiWarps;   // scale-copy issuer
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;  // scale slots start after the accumulator
 constexpr int A_BYTES = BM * BKB;
@@ -138,24 +140,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint8_t* smSF = smB + STAGES * B_BYTES;
     uint8_t* smOut = smSF + STAGES * CF::SF_STAGE;      // epilogue staging, 2 KB per warp (FP8)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smOut + CF::OUT_STAGE);
-    // bars: full[STAGES], empty[STAGES], tfull, tempty, drain
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 3);
+    // bars: full[STAGES], empty[STAGES], sfready[STAGES], tfull, tempty, drain (MMAs), cdrain (copies)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     GroupTable* gt = reinterpret_cast<GroupTable*>(bars + 32);
+    static_assert(8 * (3 * STAGES + 4) + 8 <= 256, "barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
-    const uint32_t tfull = smem_u32(bars + 2 * STAGES), tempty = smem_u32(bars + 2 * STAGES + 1);
-    const uint32_t drain = smem_u32(bars + 2 * STAGES + 2);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), sfr0 = smem_u32(bars + 2 * STAGES);
+    const uint32_t tfull = smem_u32(bars + 3 * STAGES), tempty = smem_u32(bars + 3 * STAGES + 1);
+    const uint32_t drain = smem_u32(bars + 3 * STAGES + 2), cdrain = smem_u32(bars + 3 * STAGES + 3);
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; s++) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
+            mbar_init(sfr0 + 8 * s, 1);
         }
         mbar_init(tfull, 1);
         mbar_init(tempty, kEpiWarps);
         mbar_init(drain, 1);
+        mbar_init(cdrain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_tmap(&tmA);
@@ -229,95 +234,46 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        // The issuing thread runs in lockstep with the tensor pipe (the
-        // tcgen05 queue holds about one MMA), so the next stage's barrier test
-        // and scale copies are interleaved between this stage's MMAs, and the
-        // common step (full stage, a next stage exists) is branch-free.
+        // Per stage: wait for the operands (full) and for the stage's scales in
+        // tensor memory (sfready, committed by the scale-copy warp), issue the
+        // stage's four MMAs, commit the stage back to the producer.
         if (lane == 0) {
-            constexpr int MPS = 4, NCP = 3 * CF::SF_ATOMS;
-            constexpr int CHUNK = (NCP + MPS - 2) / (MPS - 1);
+            constexpr int MPS = 4;
             const uint64_t ad_base = desc_sw128(smem_u32(smA));
             const uint64_t bd_base = desc_sw128(smem_u32(smB));
-            const uint64_t sfd_base = desc_sf(smem_u32(smSF));
             const uint32_t sf_t0 = tmem + kSfCol0;
-            // scale copy c of stage st: atom c / 3, part c % 3 (A; B rows 0-127; B rows 128-255)
-            auto cp_one = [&](int st, int c) {
-                const int at = c / 3, part = c % 3;
-                const uint64_t sd = sfd_base + (uint64_t)((st * CF::SF_STAGE) >> 4);
-                const uint32_t sfa_t = sf_t0 + st * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
-                if (part == 0) cp_sf<1>(sfa_t + 4 * at, sd + 32 * at);
-                else cp_sf<1>(sfb_t + 8 * at + 4 * (part - 1),
-                              sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + at) * 512) >> 4));
-            };
-            auto issue = [&](int st, int m, uint32_t acc) {
-                const uint32_t sfa_t = sf_t0 + st * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
-                // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
-                const uint64_t ad = ad_base + (uint64_t)((st * A_BYTES) >> 4) + 2 * m;
-                const uint64_t bd = bd_base + (uint64_t)((st * B_BYTES) >> 4) + 2 * m;
-                if (FP4) mma<1, kMmaNV>(tmem, ad, bd, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
-                else mma<1, kMmaFP8>(tmem, ad, bd, p.idesc | ((uint32_t)m << 4) | ((uint32_t)m << 29), sfa_t, sfb_t, acc);
-            };
             int stage = 0;
             uint32_t phase = 0;
             int iter = 0;
             bool ok = true, any = false;
-            if ((int)blockIdx.x < total) {
-                ok = mbar_wait(full0, 0, abort_flag, p.status, p.timeout_ns);
-                if (ok) {
-                    fence_after();
-#pragma unroll
-                    for (int c = 0; c < NCP; c++) cp_one(0, c);
-                }
-            }
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++iter) {
                 if (!mbar_wait(tempty, (iter & 1) ^ 1, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
                 fence_after();
-                const bool more_tiles = t + (int)gridDim.x < total;
                 for (int kb = 0; kb < p.k_stages; kb++) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns) ||
+                        !mbar_wait(sfr0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
                     const int nk = kb == p.k_stages - 1 ? p.mma_last : MPS;
-                    int nstage = stage + 1;
-                    uint32_t nphase = phase;
-                    if (nstage == STAGES) { nstage = 0; nphase ^= 1; }
-                    const bool has_next = kb + 1 < p.k_stages || more_tiles;
-                    bool ready = false;
-                    if (nk == MPS && has_next) {
+                    const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
+                    const uint64_t ad = ad_base + (uint64_t)((stage * A_BYTES) >> 4);
+                    const uint64_t bd = bd_base + (uint64_t)((stage * B_BYTES) >> 4);
 #pragma unroll
-                        for (int m = 0; m < MPS; m++) {
-                            issue(stage, m, m == 0 ? (uint32_t)(kb != 0) : 1u);
-                            if (m == 0) {
-                                ready = mbar_test(full0 + 8 * nstage, nphase);
-                            } else {
-                                if (m == 1) {
-                                    if (!ready && !mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status,
-                                                             p.timeout_ns)) { ok = false; break; }
-                                    fence_after();
-                                }
-#pragma unroll
-                                for (int c = (m - 1) * CHUNK; c < m * CHUNK && c < NCP; c++) cp_one(nstage, c);
-                            }
-                        }
-                    } else {
-                        for (int m = 0; m < MPS; m++) {
-                            if (m < nk) issue(stage, m, (kb | m) != 0);
-                            if (!has_next) continue;
-                            if (m == 0) {
-                                ready = mbar_test(full0 + 8 * nstage, nphase);
-                            } else {
-                                if (!ready) {
-                                    ready = mbar_wait(full0 + 8 * nstage, nphase, abort_flag, p.status, p.timeout_ns);
-                                    if (!ready) { ok = false; break; }
-                                }
-                                if (m == 1) fence_after();
-                                for (int c = (m - 1) * CHUNK; c < m * CHUNK && c < NCP; c++) cp_one(nstage, c);
-                            }
+                    for (int m = 0; m < MPS; m++) {
+                        if (m < nk) {
+                            const uint32_t acc = (kb | m) != 0;
+                            // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
+                            if (FP4) mma<1, kMmaNV>(tmem, ad + 2 * m, bd + 2 * m, p.idesc, sfa_t + 4 * m, sfb_t + 8 * m, acc);
+                            else mma<1, kMmaFP8>(tmem, ad + 2 * m, bd + 2 * m,
+                                                 p.idesc | ((uint32_t)m << 4) | ((uint32_t)m << 29), sfa_t, sfb_t, acc);
                         }
                     }
                     any = true;
                     commit<1>(empty0 + 8 * stage);
                     if (kb == p.k_stages - 1) commit<1>(tfull);
-                    stage = nstage;
-                    phase = nphase;
-                    if (!ok) break;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok) *abort_flag = 1;
@@ -329,8 +285,49 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 mbar_wait(drain, 0, &no_abort, nullptr, 100000000ull);
             }
         }
+    } else if (warp == kCopyWarp) {
+        // ------------------------------------------------ scale copies
+        // Copies each stage's scale atoms into the stage's TMEM slot as soon as
+        // the stage has landed (the slot is free: the producer reloads a stage
+        // only after the MMAs that read it completed) and commits sfready.
+        // Issued apart from the MMAs, the copies overlap with them instead of
+        // holding up the next MMA.
+        if (lane == 0) {
+            constexpr int NCP = 3 * CF::SF_ATOMS;
+            const uint64_t sfd_base = desc_sf(smem_u32(smSF));
+            const uint32_t sf_t0 = tmem + kSfCol0;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true, any = false;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                for (int kb = 0; kb < p.k_stages; kb++) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+                    fence_after();
+                    const uint64_t sd = sfd_base + (uint64_t)((stage * CF::SF_STAGE) >> 4);
+                    const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + (FP4 ? 16 : 4);
+                    // copy c: atom c / 3, part c % 3 (A; B rows 0-127; B rows 128-255)
+#pragma unroll
+                    for (int c = 0; c < NCP; c++) {
+                        const int at = c / 3, part = c % 3;
+                        if (part == 0) cp_sf<1>(sfa_t + 4 * at, sd + 32 * at);
+                        else cp_sf<1>(sfb_t + 8 * at + 4 * (part - 1),
+                                      sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + at) * 512) >> 4));
+                    }
+                    commit<1>(sfr0 + 8 * stage);
+                    any = true;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) *abort_flag = 1;
+            if (any) {
+                // every copy lands before TMEM is released
+                commit<1>(cdrain);
+                volatile int no_abort = 0;
+                mbar_wait(cdrain, 0, &no_abort, nullptr, 100000000ull);
+            }
+        }
     } else {
-        // ------------------------------------------------ epilogue
+        // ------------------------------------------------ epilogue (warps 2-9)
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int h = (warp - 2) >> 2;          // column half
         // NVFP4 tensor scales, applied one after the other (their product alone can underflow)
@@ -411,16 +408,21 @@ cudaError_t launch(const GemmArgs& a, const Params& p, const CUtensorMap& ta, co
 }  // namespace
 
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t st) {
-    // Grouped GEMMs go to CTA pairs when experts average at least
-    // kPairRowsPerGroup rows: a 256-row pair tile leaves on average half a
-    // tile idle per expert, against a quarter of a 256-row span for the
-    // 128-row tiles of the single-CTA kernel.
+    // Grouped GEMMs go to CTA pairs whenever their layout allows (one tensor
+    // map over the experts' scales) and A's scales are in the per-expert
+    // padded layout: the pair's 256 x 256 tiles halve the operand traffic per
+    // FLOP, which outweighs the half tile an expert with an odd number of
+    // 128-row bands leaves idle (measured on the 64-expert Zipf workload:
+    // 0.405 ms against 0.435 ms).  With the plain layout a pair tile starts on
+    // A's own bands, idles more rows, and is chosen only when the experts
+    // average at least kPairRowsPerGroup rows.
     constexpr int64_t kPairRowsPerGroup = 1024;
     // MXFP4 x MXFP4 exists only on the CTA-pair kernel (kind::mxf4)
     if (a.fmt_a == kMXFP4) return run_gemm_pair(a, st);
     if (!a.single_cta) {
         if (a.num_groups == 0) return run_gemm_pair(a, st);
-        if (gemm_pair_grouped_ok(a) && (a.grouped_pair || a.M >= kPairRowsPerGroup * a.num_groups))
+        if (gemm_pair_grouped_ok(a) &&
+            (a.grouped_pair || a.a_grouped_sf || a.M >= kPairRowsPerGroup * a.num_groups))
             return run_gemm_pair(a, st);
     }
     const bool fp4 = a.fmt_a == kNVFP4;
