@@ -187,15 +187,21 @@ def quantize_nvfp4_delayed(x, history, axis="row", stream=None):
     return row, col
 
 
+def dequantize_into(q: QTensor, out, stream=None):
+    """Exact dequantization into `out` ([rows, cols] float32 or bfloat16)."""
+    import torch
+    c = q.c()
+    st = lib().bsq_dequantize(ctypes.byref(c), ctypes.c_void_p(out.data_ptr()),
+                              OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32, _stream(stream))
+    _check(st, "bsq_dequantize")
+    return out
+
+
 def dequantize(q: QTensor, dtype=None, stream=None):
     import torch
     dtype = dtype or torch.float32
     out = torch.empty((q.rows, q.cols), dtype=dtype, device=q.codes.device)
-    c = q.c()
-    st = lib().bsq_dequantize(ctypes.byref(c), ctypes.c_void_p(out.data_ptr()),
-                              OUT_BF16 if dtype == torch.bfloat16 else OUT_F32, _stream(stream))
-    _check(st, "bsq_dequantize")
-    return out
+    return dequantize_into(q, out, stream)
 
 
 def gemm_into(A: QTensor, B: QTensor, C, stream=None):

@@ -396,6 +396,16 @@ def gemm_pairs(A: np.ndarray, B: np.ndarray, ms, ns):
     return ref, mag
 
 
+def gemm_full_matmul(A: np.ndarray, B: np.ndarray):
+    """ref = A B^T and mag = |A| |B|^T in FP64 with numpy's matrix product
+    (the library primitive as the summation step; the exactly dequantized
+    products need at most 24 significant bits, so only the FP64 summation
+    rounds, far below the 1e-5 bound).  For full-output checks."""
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    return A @ B.T, np.abs(A) @ np.abs(B).T
+
+
 def gemm_full(A: np.ndarray, B: np.ndarray):
     A = np.ascontiguousarray(A, dtype=np.float64)
     B = np.ascontiguousarray(B, dtype=np.float64)

@@ -188,14 +188,18 @@ void bsqo_mx_block(int fmt, const double* v, int n, uint8_t* codes, uint8_t* sca
 void bsqo_mx_quantize_rows(int fmt, int blk, const uint16_t* x, int64_t R, int64_t C,
                            uint8_t* codes, uint8_t* scales)
 {
-    int64_t r, j;
-    int i;
-    double v[64];
-    for (r = 0; r < R; r++)
+    int64_t r;
+    /* rows are independent: spread over threads, each row as written */
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; r++) {
+        int64_t j;
+        int i;
+        double v[64];
         for (j = 0; j < C / blk; j++) {
             for (i = 0; i < blk; i++) v[i] = bsqo_bf16_to_double(x[r * C + j * blk + i]);
             bsqo_mx_block(fmt, v, blk, codes + r * C + j * blk, scales + r * (C / blk) + j);
         }
+    }
 }
 
 /* ---------------------------------------------------------------------
@@ -254,9 +258,12 @@ float bsqo_nvfp4_delayed_tensor_scale(const float* hist, int64_t n)
 void bsqo_nvfp4_quantize_rows(const uint16_t* x, int64_t R, int64_t C, float s_t,
                               uint8_t* codes, uint8_t* scales)
 {
-    int64_t r, j;
-    int i;
-    for (r = 0; r < R; r++)
+    int64_t r;
+    /* rows are independent: spread over threads, each row as written */
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; r++) {
+        int64_t j;
+        int i;
         for (j = 0; j < C / 16; j++) {
             const uint16_t* xb = x + r * C + j * 16;
             uint8_t* cb = codes + r * C + j * 16;
@@ -287,6 +294,7 @@ void bsqo_nvfp4_quantize_rows(const uint16_t* x, int64_t R, int64_t C, float s_t
                 cb[i] = (uint8_t)bsqo_encode(O_E2M1, (double)qi);
             }
         }
+    }
 }
 
 /* ---------------------------------------------------------------------
@@ -296,21 +304,27 @@ void bsqo_nvfp4_quantize_rows(const uint16_t* x, int64_t R, int64_t C, float s_t
 void bsqo_mx_dequant_rows(int fmt, int blk, const uint8_t* codes, const uint8_t* scales,
                           int64_t R, int64_t C, double* out)
 {
-    int64_t r, k;
-    for (r = 0; r < R; r++)
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; r++) {
+        int64_t k;
         for (k = 0; k < C; k++)
             out[r * C + k] = bsqo_decode(fmt, codes[r * C + k]) *
                              bsqo_decode_e8m0(scales[r * (C / blk) + k / blk]);
+    }
 }
 
 void bsqo_nvfp4_dequant_rows(const uint8_t* codes, const uint8_t* scales, float s_t,
                              int64_t R, int64_t C, double* out)
 {
-    int64_t r, k;
-    for (r = 0; r < R; r++)
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; r++) {
+        int64_t k;
         for (k = 0; k < C; k++)
             out[r * C + k] = bsqo_decode(O_E2M1, codes[r * C + k]) *
                              bsqo_decode(O_UE4M3, scales[r * (C / 16) + k / 16]) * (double)s_t;
+    }
 }
 
 /* ---------------------------------------------------------------------
@@ -322,15 +336,18 @@ void bsqo_nvfp4_dequant_rows(const uint8_t* codes, const uint8_t* scales, float 
 void bsqo_mxfp4_to_mxfp8_rows(const uint8_t* codes4, const uint8_t* scales4, int64_t R, int64_t C,
                               uint8_t* codes8, uint8_t* scales8)
 {
-    int64_t r, j;
-    int i;
-    double v[32];
-    for (r = 0; r < R; r++)
+    int64_t r;
+#pragma omp parallel for schedule(static)
+    for (r = 0; r < R; r++) {
+        int64_t j;
+        int i;
+        double v[32];
         for (j = 0; j < C / 32; j++) {
             double s = bsqo_decode_e8m0(scales4[r * (C / 32) + j]);
             for (i = 0; i < 32; i++) v[i] = bsqo_decode(O_E2M1, codes4[r * C + j * 32 + i]) * s;
             bsqo_mx_block(O_E4M3, v, 32, codes8 + r * C + j * 32, scales8 + r * (C / 32) + j);
         }
+    }
 }
 
 /* ---------------------------------------------------------------------

@@ -52,12 +52,15 @@ def assert_qtensor_equal(q, exp, what=""):
 
 
 def codes_at(out, align):
-    """Give out a code buffer whose address is `align` (16 or 32) modulo 32."""
+    """Give out a code buffer whose address is `align` (16 or 32) modulo 32;
+    its code and scale bytes start as 0xAB."""
     import torch
     if align == 16:
         buf = torch.empty(out.codes.numel() + 16, dtype=torch.uint8, device=out.codes.device)
         out.codes = buf[16:]
         assert out.codes.data_ptr() % 32 == 16
+    out.codes.fill_(0xAB)
+    out.scales.fill_(0xAB)
     return out
 
 
@@ -88,3 +91,101 @@ def gemm_tol_ok(C: np.ndarray, ref: np.ndarray, mag: np.ndarray, bf16: bool):
         tol = tol * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(ref)
     err = np.abs(C.astype(np.float64) - ref)
     return err <= tol, err, tol
+
+
+POISON = 0xAB
+
+
+def poisoned_qtensor(bsq, fmt: str, rows: int, cols: int):
+    """An output QTensor whose code and scale bytes are all 0xAB (and whose
+    NVFP4 tensor scale is NaN), so that any byte a kernel fails to write
+    differs from the expected one."""
+    import torch
+    q = bsq.empty(fmt, rows, cols)
+    q.codes.fill_(POISON)
+    q.scales.fill_(POISON)
+    if q.tensor_scale is not None:
+        q.tensor_scale.fill_(float("nan"))
+    return q
+
+
+def guarded(shape, dtype, guard_bytes: int = 4096):
+    """An output tensor of `shape` inside a larger 0xAB-filled allocation
+    with guard bands of `guard_bytes` on both sides; returns (tensor, check)
+    where check() asserts that the guard bands are untouched."""
+    import torch
+    n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    buf = torch.full((guard_bytes + n + guard_bytes,), POISON, dtype=torch.uint8, device="cuda")
+    t = buf[guard_bytes:guard_bytes + n].view(dtype).view(*shape)
+
+    def check():
+        lo = buf[:guard_bytes].cpu().numpy()
+        hi = buf[guard_bytes + n:].cpu().numpy()
+        assert (lo == POISON).all() and (hi == POISON).all(), "a kernel wrote outside its output"
+    return t, check
+
+
+# ---- library calls with poisoned outputs (every output byte starts as 0xAB;
+# dense and grouped GEMM outputs also sit between guard bands)
+def qz(bsq, x_dev, fmt: str, axis: str = "row"):
+    R, C = x_dev.shape
+    row = poisoned_qtensor(bsq, fmt, R, C) if axis in ("row", "both") else None
+    col = poisoned_qtensor(bsq, fmt, C, R) if axis in ("col", "both") else None
+    bsq.quantize_into(x_dev, fmt, axis, row, col)
+    return row, col
+
+
+def qz_delayed(bsq, x_dev, history, axis: str = "row"):
+    R, C = x_dev.shape
+    row = poisoned_qtensor(bsq, "nvfp4", R, C) if axis in ("row", "both") else None
+    col = poisoned_qtensor(bsq, "nvfp4", C, R) if axis in ("col", "both") else None
+    bsq.quantize_nvfp4_delayed_into(x_dev, axis, row, col, history)
+    return row, col
+
+
+def deq(bsq, q, dtype):
+    out, check = guarded((q.rows, q.cols), dtype)
+    bsq.dequantize_into(q, out)
+    check()
+    return out
+
+
+def gemm_g(bsq, A, B, dtype):
+    C, check = guarded((A.rows, B.rows), dtype)
+    bsq.gemm_into(A, B, C)
+    check()
+    return C
+
+
+def grouped_g(bsq, A, offsets_dev, groups, dtype, padded_scales=False):
+    C, check = guarded((A.rows, groups[0].rows), dtype)
+    bsq.grouped_gemm_into(A, offsets_dev, groups, C, padded_scales=padded_scales)
+    check()
+    return C
+
+
+def repack(bsq, q4):
+    out = poisoned_qtensor(bsq, "mxfp8_e4m3", q4.rows, q4.cols)
+    bsq.mxfp4_to_mxfp8_into(q4, out)
+    return out
+
+
+def repack_grouped(bsq, q4, offsets_dev, groups: int):
+    out = poisoned_qtensor(bsq, "mxfp8_e4m3", q4.rows, q4.cols)
+    out.scales = bsq.empty_grouped("mxfp8_e4m3", q4.rows, q4.cols, groups).scales.fill_(POISON)
+    bsq.mxfp4_to_mxfp8_grouped_into(q4, out, offsets_dev, groups)
+    return out
+
+
+def repack_col(bsq, q4):
+    out = poisoned_qtensor(bsq, "mxfp8_e4m3", q4.cols, q4.rows)
+    bsq.mxfp4_to_mxfp8_col_into(q4, out)
+    return out
+
+
+def repack_1x128(bsq, q4):
+    import torch
+    codes = torch.full((q4.rows, q4.cols), POISON, dtype=torch.uint8, device="cuda")
+    scales = torch.full((q4.rows, (q4.cols + 127) // 128), POISON, dtype=torch.uint8, device="cuda")
+    bsq.mxfp4_to_fp8_1x128_into(q4, codes, scales)
+    return codes, scales

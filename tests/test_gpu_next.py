@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 from block_scaled_precision_03_gb300 import inputs
-from _util import dev_bf16, host_u8, codes_at
+from _util import (dev_bf16, host_u8, codes_at, qz, qz_delayed, gemm_g, deq, grouped_g, repack_grouped, repack_col, repack_1x128, repack, poisoned_qtensor, guarded)
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +43,7 @@ def test_delayed_nvfp4_matches_oracle(bsq, shape, axis):
     x = inputs.outlier_activations_bf16(shape, 11)
     hist0 = np.float32([3.0, 0.0, 7.5, 1.0] + [0.0] * 12)
     h = torch.from_numpy(hist0.copy()).cuda()
-    row, col = bsq.quantize_nvfp4_delayed(dev_bf16(x), h, axis)
+    row, col = qz_delayed(bsq, dev_bf16(x), h, axis)
     exp = oracle.nvfp4_delayed_quantize(x, hist0, axis)
     if row is not None:
         _check_delayed(row, *exp["row"], exp["s_t"], f"row {shape}")
@@ -60,7 +60,7 @@ def test_delayed_nvfp4_consecutive_steps(bsq):
     h = torch.from_numpy(hist.copy()).cuda()
     for step, scale in enumerate((1.0, 8.0, 0.25)):
         x = inputs.normal_bf16((128, 256), 20 + step, std=scale)
-        row, _ = bsq.quantize_nvfp4_delayed(dev_bf16(x), h, "row")
+        row, _ = qz_delayed(bsq, dev_bf16(x), h, "row")
         exp = oracle.nvfp4_delayed_quantize(x, hist, "row")
         _check_delayed(row, *exp["row"], exp["s_t"], f"step {step}")
         hist = exp["history"]
@@ -73,10 +73,10 @@ def test_delayed_nvfp4_saturates(bsq):
     x = inputs.normal_bf16((64, 256), 30)
     hist0 = np.float32([_abs_max(x) / 64.0] + [0.0] * 15)
     h = torch.from_numpy(hist0.copy()).cuda()
-    row, _ = bsq.quantize_nvfp4_delayed(dev_bf16(x), h, "row")
+    row, _ = qz_delayed(bsq, dev_bf16(x), h, "row")
     exp = oracle.nvfp4_delayed_quantize(x, hist0, "row")
     _check_delayed(row, *exp["row"], exp["s_t"], "saturating")
-    v = bsq.dequantize(row, torch.float32).cpu().numpy()
+    v = deq(bsq, row, torch.float32).cpu().numpy()
     assert np.abs(v).max() == np.float32(6.0 * 448.0 * exp["s_t"])
 
 
@@ -86,10 +86,10 @@ def test_delayed_nvfp4_full_size_equals_just_in_time(bsq):
     import torch
     X = inputs.nvfp4_forward()["X"]
     xd = dev_bf16(X)
-    jit, _ = bsq.quantize(xd, "nvfp4", "row")
+    jit, _ = qz(bsq, xd, "nvfp4", "row")
     h = torch.zeros(16, dtype=torch.float32, device="cuda")
     h[3] = oracle.tensor_amax(X)
-    dl, _ = bsq.quantize_nvfp4_delayed(xd, h, "row")
+    dl, _ = qz_delayed(bsq, xd, h, "row")
     assert torch.equal(jit.codes, dl.codes) and torch.equal(jit.scales, dl.scales)
     assert torch.equal(jit.tensor_scale, dl.tensor_scale)
     assert float(h[0]) == oracle.tensor_amax(X) and float(h[4]) == oracle.tensor_amax(X) and float(h[3]) == 0.0
@@ -100,7 +100,7 @@ def test_delayed_nvfp4_empty_history_unit_scale(bsq):
     import torch
     x = inputs.normal_bf16((32, 64), 31)
     h = torch.zeros(16, dtype=torch.float32, device="cuda")
-    row, _ = bsq.quantize_nvfp4_delayed(dev_bf16(x), h, "row")
+    row, _ = qz_delayed(bsq, dev_bf16(x), h, "row")
     assert float(row.tensor_scale.cpu()[0]) == 1.0
     c, s, _ = oracle.nvfp4_quantize_rows(x, 1.0)
     _check_delayed(row, c, s, 1.0, "unit scale")
@@ -125,7 +125,7 @@ def test_fp4_row_to_fp8_col_random_codes_and_scales(bsq, shape):
     s4[rng.random(s4.shape) < 0.01] = 0xFF
     s4[0, 0], s4[-1, -1] = 0, 254
     q4 = upload_q(bsq, "mxfp4", c4, s4)
-    out = bsq.mxfp4_to_mxfp8_col(q4)
+    out = repack_col(bsq, q4)
     c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
     _check_fp8col(out, c8, s8, f"random {shape}")
     bsq.sync_status()
@@ -166,9 +166,9 @@ def test_fp4_row_to_fp8_col_scale_structures(bsq, kind, align):
 def test_fp4_row_to_fp8_col_from_bf16(bsq):
     # the MoE path: BF16 activations -> MXFP4 rows (GPU) -> FP8 columns (GPU)
     x = inputs.normal_bf16((1024, 7168), 50)
-    q4, _ = bsq.quantize(dev_bf16(x), "mxfp4", "row")
+    q4, _ = qz(bsq, dev_bf16(x), "mxfp4", "row")
     c4, s4 = oracle.mx_quantize_rows(x, "mxfp4")
-    out = bsq.mxfp4_to_mxfp8_col(q4)
+    out = repack_col(bsq, q4)
     c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
     _check_fp8col(out, c8, s8, "from bf16")
 
@@ -178,8 +178,8 @@ def test_fp4_row_to_fp8_col_full_size_sampled(bsq):
     # 32-column groups (every row, every scale block of those columns)
     d = inputs.moe_grouped()
     A = d["A"]
-    q4, _ = bsq.quantize(dev_bf16(A), "mxfp4", "row")
-    out = bsq.mxfp4_to_mxfp8_col(q4)
+    q4, _ = qz(bsq, dev_bf16(A), "mxfp4", "row")
+    out = repack_col(bsq, q4)
     rng = np.random.default_rng(51)
     groups = np.sort(rng.choice(7168 // 32, size=4, replace=False))
     S_out = 32768 // 32
@@ -211,12 +211,12 @@ def _mx4_gemm_check(bsq, xa, xb, out, groups=None):
     Ad = oracle.dequant_rows(ca, sa, "mxfp4")
     Bd = oracle.dequant_rows(cb, sb, "mxfp4")
     if groups is None:
-        C = bsq.gemm(A, B, dt).float().cpu().numpy()
+        C = gemm_g(bsq, A, B, dt).float().cpu().numpy()
         pairs = [(slice(0, xa.shape[0]), slice(0, xb.shape[0]))]
     else:
         off = inputs.group_offsets(groups)
         N = xb.shape[0] // len(groups)
-        C = bsq.grouped_gemm(A, torch.from_numpy(off).cuda(), bsq.group_views(B, len(groups)), dt)
+        C = grouped_g(bsq, A, torch.from_numpy(off).cuda(), bsq.group_views(B, len(groups)), dt)
         C = C.float().cpu().numpy()
         pairs = [(slice(off[g], off[g + 1]), slice(g * N, (g + 1) * N)) for g in range(len(groups)) if off[g + 1] > off[g]]
     for rows, brows in pairs:
@@ -257,7 +257,7 @@ def test_gemm_mxfp4_single_scale_probe(bsq):
     rng = np.random.default_rng(64)
     sa = (127 + rng.integers(-3, 4, (M, K // 32))).astype(np.uint8)
     sb = (127 + rng.integers(-3, 4, (N, K // 32))).astype(np.uint8)
-    C = bsq.gemm(upload_q(bsq, "mxfp4", ca, sa), upload_q(bsq, "mxfp4", cb, sb), torch.float32).cpu().numpy()
+    C = gemm_g(bsq, upload_q(bsq, "mxfp4", ca, sa), upload_q(bsq, "mxfp4", cb, sb), torch.float32).cpu().numpy()
     ref = 32.0 * (np.exp2(sa.astype(np.float64) - 127) @ np.exp2(sb.astype(np.float64) - 127).T)
     np.testing.assert_array_equal(C, ref.astype(np.float32))
 
@@ -277,7 +277,7 @@ def test_1x128_random_codes_and_scales(bsq, shape, spread):
     if spread == 40:
         s4[rng.random(s4.shape) < 0.02] = 0xFF
     q4 = upload_q(bsq, "mxfp4", c4, s4)
-    codes, scales = bsq.mxfp4_to_fp8_1x128(q4)
+    codes, scales = repack_1x128(bsq, q4)
     c8, s8 = oracle.mxfp4_to_fp8_1x128(c4, s4)
     got = host_u8(codes)
     bad = np.argwhere(got != c8)
@@ -291,12 +291,12 @@ def test_1x128_from_bf16_both_store_widths(bsq, align):
     # the MoE activations' path: BF16 -> MXFP4 rows (GPU) -> FP8 1x128 (GPU)
     import torch
     x = inputs.outlier_activations_bf16((512, 7168), 61)
-    q4, _ = bsq.quantize(dev_bf16(x), "mxfp4", "row")
+    q4, _ = qz(bsq, dev_bf16(x), "mxfp4", "row")
     c4, s4 = oracle.mx_quantize_rows(x, "mxfp4")
-    buf = torch.empty(512 * 7168 + 16, dtype=torch.uint8, device="cuda")
+    buf = torch.full((512 * 7168 + 16,), 0xAB, dtype=torch.uint8, device="cuda")
     codes = (buf[16:] if align == 16 else buf[:-16]).view(512, 7168)
     assert codes.data_ptr() % 32 == (16 if align == 16 else 0)
-    scales = torch.empty((512, 56), dtype=torch.uint8, device="cuda")
+    scales = torch.full((512, 56), 0xAB, dtype=torch.uint8, device="cuda")
     bsq.mxfp4_to_fp8_1x128_into(q4, codes, scales)
     c8, s8 = oracle.mxfp4_to_fp8_1x128(c4, s4)
     assert np.array_equal(host_u8(codes), c8) and np.array_equal(host_u8(scales), s8)
@@ -306,8 +306,8 @@ def test_1x128_full_size_sampled(bsq):
     # the MoE activations at full size (32768 x 7168): sampled rows, every group
     d = inputs.moe_grouped()
     A = d["A"]
-    q4, _ = bsq.quantize(dev_bf16(A), "mxfp4", "row")
-    codes, scales = bsq.mxfp4_to_fp8_1x128(q4)
+    q4, _ = qz(bsq, dev_bf16(A), "mxfp4", "row")
+    codes, scales = repack_1x128(bsq, q4)
     rows = np.sort(np.random.default_rng(62).choice(32768, 48, replace=False))
     c4, s4 = oracle.mx_quantize_rows(np.ascontiguousarray(A[rows]), "mxfp4")
     c8, s8 = oracle.mxfp4_to_fp8_1x128(c4, s4)

@@ -9,8 +9,7 @@ import pytest
 
 import oracle
 from block_scaled_precision_03_gb300 import inputs
-from _util import (expected, assert_qtensor_equal, dev_bf16, host_u8, dev_u8, upload_q, round_to_bf16, codes_at,
-                   gemm_tol_ok)
+from _util import (expected, assert_qtensor_equal, dev_bf16, host_u8, dev_u8, upload_q, round_to_bf16, codes_at, gemm_tol_ok, qz, qz_delayed, gemm_g, deq, grouped_g, repack_grouped, repack_col, repack_1x128, repack, poisoned_qtensor, guarded)
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +40,7 @@ ROW_SHAPES = [(256, 256), (130, 96), (7, 32), (1, 4096), (384, 1056), (129, 160)
 @pytest.mark.parametrize("kind", ["outlier", "grad", "weight"])
 def test_quantize_rows(bsq, fmt, shape, kind):
     x = _gen(shape, 11, kind)
-    row, _ = bsq.quantize(dev_bf16(x), fmt, "row")
+    row, _ = qz(bsq, dev_bf16(x), fmt, "row")
     assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} row {shape}")
 
 
@@ -56,7 +55,7 @@ def test_quantize_cols_and_both(bsq, fmt, shape, axis):
     if axis == "both" and C % oracle.BLOCK[fmt]:
         pytest.skip("row-wise blocks need cols % block == 0")
     x = _gen(shape, 5, "grad" if fmt == "mxfp8_e5m2" else "outlier")
-    row, col = bsq.quantize(dev_bf16(x), fmt, axis)
+    row, col = qz(bsq, dev_bf16(x), fmt, axis)
     exp = expected(x, fmt, axis)
     assert_qtensor_equal(col, exp["col"], f"{fmt} col {shape}")
     if axis == "both":
@@ -79,7 +78,7 @@ def test_quantize_every_bf16_pattern(bsq, fmt, order):
     if fmt == "nvfp4":
         # the tensor amax ignores non-finite values; keep them in blocks
         pass
-    row, _ = bsq.quantize(dev_bf16(x), fmt, "row")
+    row, _ = qz(bsq, dev_bf16(x), fmt, "row")
     assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} all-bf16 order={order}")
 
 
@@ -101,7 +100,7 @@ def test_quantize_every_bf16_pattern_scaled_blocks(bsq, fmt):
     x = np.ascontiguousarray(np.concatenate(blocks)[:, :32])
     if fmt == "nvfp4":
         x = np.ascontiguousarray(x.reshape(-1, 16))
-    row, _ = bsq.quantize(dev_bf16(x), fmt, "row")
+    row, _ = qz(bsq, dev_bf16(x), fmt, "row")
     assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} anchored")
 
 
@@ -112,13 +111,13 @@ def test_quantize_zero_and_nonfinite_blocks(bsq):
     x[3, :] = 0x8000          # -0
     x[3, 33] = 0x3F80
     for fmt in FMTS:
-        row, col = bsq.quantize(dev_bf16(x), fmt, "row")
+        row, col = qz(bsq, dev_bf16(x), fmt, "row")
         assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} special")
 
 
 def test_nvfp4_tensor_scale_shared(bsq):
     x = inputs.outlier_activations_bf16((128, 256), 9)
-    row, col = bsq.quantize(dev_bf16(x), "nvfp4", "both")
+    row, col = qz(bsq, dev_bf16(x), "nvfp4", "both")
     st = oracle.nvfp4_tensor_scale(x)
     assert float(row.tensor_scale.cpu()[0]) == st == float(col.tensor_scale.cpu()[0])
 
@@ -161,7 +160,7 @@ def test_repack_every_nibble_pair_every_scale(bsq):
     codes = np.tile(base, (1, 8))                         # 256 rows x 256
     scales = np.arange(256 * 8, dtype=np.uint32).reshape(256, 8).astype(np.uint8)
     q = upload_q(bsq, "mxfp4", codes, scales)
-    out = bsq.mxfp4_to_mxfp8(q)
+    out = repack(bsq, q)
     c8, s8 = oracle.mxfp4_to_mxfp8_rows(codes, scales)
     assert_qtensor_equal(out, (c8, oracle.swizzle_scales(s8), None), "repack exhaustive")
 
@@ -175,7 +174,7 @@ def test_dequantize_exact(bsq, fmt, out):
     c, s, t = oracle.quantize_rows(x, fmt)
     q = upload_q(bsq, fmt, c, s, t)
     ref = oracle.dequant_rows(c, s, fmt, t)
-    got = bsq.dequantize(q, torch.float32 if out == "f32" else torch.bfloat16)
+    got = deq(bsq, q, torch.float32 if out == "f32" else torch.bfloat16)
     if out == "f32":
         np.testing.assert_array_equal(got.cpu().numpy(), ref.astype(np.float32))
     else:
@@ -196,7 +195,7 @@ def _check_gemm(bsq, xa, fa, xb, fb, dtype_name, full=True):
     A = upload_q(bsq, fa, ca, sa, ta)
     B = upload_q(bsq, fb, cb, sb, tb)
     dt = torch.float32 if dtype_name == "f32" else torch.bfloat16
-    C = bsq.gemm(A, B, dt).float().cpu().numpy()
+    C = gemm_g(bsq, A, B, dt).float().cpu().numpy()
     Ad = oracle.dequant_rows(ca, sa, fa, ta)
     Bd = oracle.dequant_rows(cb, sb, fb, tb)
     ref, mag = oracle.gemm_full(Ad, Bd)
@@ -249,7 +248,7 @@ def test_gemm_single_scale_probe(bsq):
     sb = (127 + rng.integers(-3, 4, (N, K // 32))).astype(np.uint8)
     A = upload_q(bsq, "mxfp8_e4m3", ca, sa)
     B = upload_q(bsq, "mxfp8_e4m3", cb, sb)
-    C = bsq.gemm(A, B, torch.float32).cpu().numpy()
+    C = gemm_g(bsq, A, B, torch.float32).cpu().numpy()
     ref = 32.0 * (np.exp2(sa.astype(np.float64) - 127) @ np.exp2(sb.astype(np.float64) - 127).T)
     np.testing.assert_array_equal(C, ref.astype(np.float32))
 
@@ -266,7 +265,7 @@ def test_grouped_gemm_small(bsq):
     A = upload_q(bsq, "mxfp8_e4m3", ca, sa)
     W = upload_q(bsq, "mxfp8_e4m3", cw, sw)
     offd = torch.from_numpy(off).cuda()
-    C = bsq.grouped_gemm(A, offd, bsq.group_views(W, G), torch.float32).cpu().numpy()
+    C = grouped_g(bsq, A, offd, bsq.group_views(W, G), torch.float32).cpu().numpy()
     Ad = oracle.dequant_rows(ca, sa, "mxfp8_e4m3")
     Wd = oracle.dequant_rows(cw, sw, "mxfp8_e4m3")
     for g in range(G):
@@ -355,7 +354,7 @@ def test_grouped_gemm_scattered_scales(bsq):
     # same codes; each expert's scales copied to its own allocation, in reverse order
     own = [v.scales.clone() for v in views[::-1]][::-1]
     scattered = [bsq.QTensor(v.fmt, v.rows, v.cols, v.codes, sc, v.tensor_scale) for v, sc in zip(views, own)]
-    C = bsq.grouped_gemm(A, torch.from_numpy(off).cuda(), scattered, torch.float32).cpu().numpy()
+    C = grouped_g(bsq, A, torch.from_numpy(off).cuda(), scattered, torch.float32).cpu().numpy()
     Ad = oracle.dequant_rows(ca, sa, "mxfp8_e4m3")
     Wd = oracle.dequant_rows(cw, sw, "mxfp8_e4m3")
     for g in range(G):
@@ -417,7 +416,7 @@ def test_gemm_wait_limit_runs_out_then_recovers(bsq, fmt, kernel, limit_ns):
 def test_quantize_rejects_unaligned_cols(bsq):
     x = inputs.normal_bf16((96, 130), 1)
     with pytest.raises(bsq.BsqError) as ei:
-        bsq.quantize(dev_bf16(x), "mxfp8_e4m3", "col")
+        qz(bsq, dev_bf16(x), "mxfp8_e4m3", "col")
     assert ei.value.status == 3
 
 

@@ -240,6 +240,61 @@ def test_nvfp4_division_is_fp32():
     np.testing.assert_array_equal(codes, ref)
 
 
+def test_nvfp4_block_scale_two_fp32_divisions():
+    """The NVFP4 block scale is UE4M3(RNE((amax_b / 6) / s_t)) with both
+    divisions in FP32 (the recipe of the NVFP4 forward workload), on every
+    block: checked against numpy float32 arithmetic with two independent
+    encoders (a UE4M3 value-table RNE and torch's float8_e4m3fn cast), on
+    seeded tensors of the workload's distributions and on tensors whose
+    quotients sit on, or 1-3 ulps either side of, every UE4M3 rounding
+    midpoint.  The two plausible slips, amax_b / (6 s_t) and a quotient
+    rounded once from double precision, each change some of those bytes."""
+    import _nvfp4_edges as E
+    f32 = np.float32
+    cases = [(inputs.normal_bf16((64, 256), 40), None), (inputs.normal_bf16((64, 256), 41, std=0.02), None),
+             (inputs.outlier_activations_bf16((64, 256), 42), None), (inputs.loguniform_grad_bf16((64, 256), 43), None)]
+    cases += [(E.jit_scale_tensor(t), None) for t in (0, 37, 101)]
+    for j in (-16, -5, -1, 0, 1, 4, 9, 16):
+        _, s_t = E.delayed_history(j)
+        cases.append((E.delayed_tensor(j), float(s_t)))
+    slip_one_division = slip_double = 0
+    for x, s_t_given in cases:
+        codes, scales, s_t = oracle.nvfp4_quantize_rows(x, s_t_given)
+        R, C = x.shape
+        amax = np.abs(E.bf16_to_f32(x).reshape(R, C // 16, 16)).max(axis=2)
+        q = E.block_q(amax, s_t)
+        np.testing.assert_array_equal(scales, E.ue4m3_code(q))
+        via_torch = torch.from_numpy(np.minimum(q, f32(448))).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        np.testing.assert_array_equal(scales, via_torch)
+        slip_one_division += int((E.ue4m3_code((amax / (f32(6) * f32(s_t))).astype(f32)) != scales).sum())
+        slip_double += int((E.ue4m3_code(amax.astype(np.float64) / 6.0 / np.float64(s_t)) != scales).sum())
+    assert slip_one_division > 0 and slip_double > 0
+
+
+def test_nvfp4_edge_inputs_reach_every_boundary():
+    """The adversarial NVFP4 inputs of the GPU parity tests do what they are
+    for: under delayed scaling the element quotients reach every E2M1 edge
+    and the block quotients every UE4M3 midpoint at distances -3..3 ulps;
+    under just-in-time scaling (BF16 inputs) every edge is hit exactly."""
+    import _nvfp4_edges as E
+    el, sc = set(), set()
+    for j in E.DELAYED_J:
+        hist, s_t = E.delayed_history(j)
+        x = E.delayed_tensor(j)
+        d = oracle.nvfp4_delayed_quantize(x, hist, "row")
+        assert d["s_t"] == float(s_t)
+        el |= E.quotient_coverage(x, d["row"][1], s_t)
+        sc |= E.scale_coverage(x, s_t)
+    assert el == {(e, k) for e in range(8) for k in range(-3, 4)}
+    assert {k for _, k in sc} == set(range(-3, 4))
+    jit = set()
+    for t in (0, 64, 127):
+        x = E.jit_element_tensor(t)
+        _, scales, s_t = oracle.nvfp4_quantize_rows(x)
+        jit |= E.quotient_coverage(x, scales, s_t)
+    assert {(e, 0) for e in range(8)} <= jit
+
+
 # ------------------------------------------------------------------- repack
 REPACK_SCALES = [0, 1, 2, 5, 6, 7, 8, 9, 10, 60, 117, 118, 119, 120, 127, 128, 200, 254, 255]
 
