@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--cpu-reps", type=int, default=12)
     ap.add_argument("--part", default="all", choices=["all", "fwd", "bwd", "nv", "moe"],
                     help="run one part of the step only (profiling)")
+    ap.add_argument("--cpu-leg", default="", choices=["", "rows", "gemm"],
+                    help=argparse.SUPPRESS)      # internal: the CPU baseline, run in its own process
     return ap.parse_args()
 
 
@@ -390,6 +392,74 @@ def cpu_forward_slice(host, rows=64, wrows=2048):
     return time.perf_counter() - t0, 2.0 * rows * wrows * X.shape[1]
 
 
+# Rows of the step timed on the oracle, single-threaded, on a bounded sample:
+# (name, sample rows, row length, algorithmic bytes per element) -- the bytes
+# are the same per-element figures the GPU rows use.
+CPU_ROWS = (("quant X e4m3 row", 512, 4096, 2 + 1 + 1 / 32),
+            ("quant X nvfp4", 512, 4096, 2 + 2 + 0.5 + 1 / 16),
+            ("quant A_moe mxfp4 row", 256, 7168, 2 + 0.5 + 1 / 32),
+            ("repack mxfp4->mxfp8", 256, 7168, 0.5 + 1 / 32 + 1 + 1 / 32))
+
+
+def cpu_rows_leg(min_seconds=2.0):
+    """The oracle's quantize and re-encode on a bounded sample of each row's
+    tensor (same distribution and row length), GB/s of algorithmic bytes.
+    Runs in its own process with OMP_NUM_THREADS=1."""
+    import oracle
+    from block_scaled_precision_03_gb300 import inputs
+    out = {}
+    for name, rows, cols, bpe in CPU_ROWS:
+        if name == "quant X e4m3 row":
+            x = inputs.outlier_activations_bf16((rows, cols), 0)
+            fn = lambda: oracle.mx_quantize_rows(x, "mxfp8_e4m3")
+        elif name == "quant X nvfp4":
+            x = inputs.normal_bf16((rows, cols), 10)
+            fn = lambda: oracle.nvfp4_quantize_rows(x)          # tensor amax, then the blocks
+        elif name == "quant A_moe mxfp4 row":
+            x = inputs.normal_bf16((rows, cols), 21)
+            fn = lambda: oracle.mx_quantize_rows(x, "mxfp4")
+        else:
+            c4, s4 = oracle.mx_quantize_rows(inputs.normal_bf16((rows, cols), 21), "mxfp4")
+            fn = lambda: oracle.mxfp4_to_mxfp8_rows(c4, s4)
+        fn()
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_seconds:
+                break
+        out[name] = {"gbs": round(rows * cols * bpe * n / dt / 1e9, 4), "threads": 1,
+                     "sample": f"{rows}x{cols} of the same distribution", "seconds": round(dt, 2)}
+    return out
+
+
+def cpu_gemm_leg(reps):
+    from block_scaled_precision_03_gb300 import inputs
+    host = {"X": inputs.outlier_activations_bf16((CPU_ROWS_X, 4096), 0),
+            "W": inputs.normal_bf16((2048, 4096), 1, std=0.02)}
+    ts = [cpu_forward_slice(host, CPU_ROWS_X) for _ in range(max(1, reps))]
+    t_tot = sum(t for t, _ in ts)
+    return {"value": ts[0][1] * len(ts) / t_tot / 1e12, "seconds": round(t_tot, 2)}
+
+
+def run_cpu_leg(leg, reps, threads=None):
+    """One CPU-baseline leg in a child process (the GPU process never loads
+    the oracle); returns its JSON result or None."""
+    env = dict(os.environ)
+    if threads is not None:
+        env["OMP_NUM_THREADS"] = str(threads)
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-leg", leg, "--cpu-reps", str(reps)],
+                           env=env, capture_output=True, text=True, timeout=600)
+        for line in r.stdout.splitlines()[::-1]:
+            if line.startswith("{"):
+                return json.loads(line)
+    except Exception:
+        pass
+    return None
+
+
 def cpu_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -402,7 +472,8 @@ def cpu_sample(rows, wrows):
             f"FP64 GEMM {rows}x{wrows}x4096")
 
 
-CPU_SAMPLE = cpu_sample(64, 2048)
+CPU_ROWS_X = 512
+CPU_SAMPLE = cpu_sample(CPU_ROWS_X, 2048)
 REF_ROWS, REF_WROWS = 64, 256      # one reference-arm step: a bounded slice (~0.1 s of CPU work)
 
 
@@ -471,6 +542,10 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
+    if args.cpu_leg:
+        res = cpu_rows_leg() if args.cpu_leg == "rows" else cpu_gemm_leg(args.cpu_reps)
+        print(json.dumps(res), flush=True)
+        return
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, rank, world)
@@ -622,12 +697,14 @@ def main():
                "h2d_bytes_per_step": step.h2d, "d2h_bytes_per_step": step.d2h}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and "X" in host:
-        reps = max(1, args.cpu_reps)
-        ts = [cpu_forward_slice(host) for _ in range(reps)]
-        t_tot = sum(t for t, _ in ts)
-        cpu = {"value": ts[0][1] * reps / t_tot / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
-               "kind": "oracle", "sample": CPU_SAMPLE, "seconds": round(t_tot, 2)}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        g = run_cpu_leg("gemm", args.cpu_reps)
+        rows_cpu = run_cpu_leg("rows", 1, threads=1)
+        if g is not None:
+            cpu = {"value": g["value"], "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                   "sample": CPU_SAMPLE, "seconds": g["seconds"], "process": "child process (oracle not in the GPU process)",
+                   "rows": rows_cpu, "rows_note": "single-threaded oracle quantize / re-encode, GB/s of the same "
+                                                  "algorithmic bytes as the GPU rows"}
 
     if rank == 0:
         line = {

@@ -232,10 +232,20 @@ def group_views(B: QTensor, groups: int) -> list[QTensor]:
             for g in range(groups)]
 
 
+def _check_offsets(offsets_dev, groups: int):
+    """The C ABI reads groups + 1 int64 row offsets from device memory and
+    cannot check them; a wrong tensor is rejected here."""
+    import torch
+    if not (isinstance(offsets_dev, torch.Tensor) and offsets_dev.dtype == torch.int64 and offsets_dev.is_cuda
+            and offsets_dev.is_contiguous() and offsets_dev.numel() == groups + 1):
+        raise BsqError(1, f"group offsets must be a contiguous int64 CUDA tensor of {groups + 1} entries")
+
+
 def grouped_gemm_into(A: QTensor, offsets_dev, B_groups: list[QTensor], C, stream=None, padded_scales=False):
     """Grouped GEMM into C; padded_scales: A's scales are in the per-expert
     padded layout (from mxfp4_to_mxfp8_grouped)."""
     import torch
+    _check_offsets(offsets_dev, len(B_groups))
     ca = A.c()
     arr = (BsqTensorC * len(B_groups))(*[b.c() for b in B_groups])
     f = lib().bsq_grouped_gemm_padded if padded_scales else lib().bsq_grouped_gemm
@@ -276,6 +286,7 @@ def empty_grouped(fmt, rows: int, cols: int, groups: int, device="cuda") -> QTen
 
 
 def mxfp4_to_mxfp8_grouped_into(q: QTensor, out: QTensor, offsets_dev, groups: int, stream=None):
+    _check_offsets(offsets_dev, groups)
     ci, co = q.c(), out.c()
     _check(lib().bsq_mxfp4_to_mxfp8_grouped(ctypes.byref(ci), ctypes.byref(co), ctypes.c_void_p(offsets_dev.data_ptr()),
                                             groups, _stream(stream)), "bsq_mxfp4_to_mxfp8_grouped")

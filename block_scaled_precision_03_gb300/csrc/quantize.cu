@@ -52,66 +52,101 @@ __device__ __forceinline__ void mx_encode(const float* x, uint32_t sbyte, uint32
     }
 }
 
-// NVFP4 per-block scale byte from the block amax and the tensor scale:
-// UE4M3(RNE((amax_b / 6) / s_t)) with both divisions IEEE FP32.  The E4M3
-// code only depends on which side of its rounding boundaries (values with at
-// most 5 significant bits, including the saturation point 464) the quotient
-// falls.  q0 = amax_b * RN(1/6) * RN(1/s_t) is within about 5 ulp of the
-// two-step quotient, so it decides the code unless it lies within 15 ulp of
-// a value whose low 18 mantissa bits are zero; then the exact divisions do.
-// The exact divisions are out of line so the compiler branches around them
-// instead of issuing them predicated on every lane.
+// Correctly rounded a / b from r = RN(1 / b) (Markstein's theorem): q0 =
+// RN(a r) lies within one ulp of a / b, the residual q0 b - a is exact in
+// one FMA, and one correction with r rounds to RN(a / b).  Holds while b, r
+// and the quotient are normal and nothing overflows; the callers keep to
+// that range and divide exactly outside it.  The residual is formed as q0 b
+// - a and subtracted, so a zero a keeps its sign.
+__device__ __forceinline__ float div_from_rcp(float a, float b, float r) {
+    const float q0 = __fmul_rn(a, r);
+    const float e = __fmaf_rn(q0, b, -a);
+    return __fmaf_rn(-e, r, q0);
+}
+
+// The exact IEEE divisions of the recipe, out of line so that the compiler
+// branches around them instead of issuing them predicated on every lane.
 __device__ __noinline__ float nv_exact_block_q(float amax_b, float s_t) {
     return __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_t);
 }
 __device__ __noinline__ float nv_exact_div(float x, float d) { return __fdiv_rn(x, d); }
 
-__device__ __forceinline__ uint32_t nv_scale_byte(uint32_t amax_bits, float s_t, float inv_st) {
-    if (amax_bits >= 0x7F80u) return 0x7Fu;      // NaN/Inf in the block
+// Per-tensor constants of the NVFP4 block step: s_t, RN(1 / s_t), and
+// whether the reciprocal route applies (s_t and 1 / s_t normal).
+struct NvT {
+    float s_t, rst;
+    bool fast;
+};
+__device__ __forceinline__ NvT nv_tensor_consts(float s_t) {
+    NvT t;
+    t.s_t = s_t;
+    t.rst = __frcp_rn(s_t);
+    t.fast = s_t >= 1.17549435e-38f && t.rst < 1.0e38f;
+    return t;
+}
+
+// NVFP4 per-block scale byte from the block amax (BF16 bits, sign cleared):
+// UE4M3(RNE((amax_b / 6) / s_t)), both divisions IEEE FP32 (through
+// div_from_rcp; amax_b below 2^-100 or a subnormal s_t divide exactly).
+// `sat`: the quotient lies beyond the UE4M3 range (>= 464), so the block's
+// element quotients are unbounded.  A block holding NaN/Inf gets 0x7F.
+__device__ __forceinline__ uint32_t nv_scale_byte(uint32_t amax_bits, const NvT& t, bool& sat) {
+    sat = false;
+    if (amax_bits >= 0x7F80u) return 0x7Fu;
     const float amax_b = __uint_as_float(amax_bits << 16);
-    float q = __fmul_rn(__fmul_rn(amax_b, 1.0f / 6.0f), inv_st);
-    const uint32_t low = __float_as_uint(q) & 0x3FFFFu;
-    if (low < 16u || low > 0x3FFEFu) q = nv_exact_block_q(amax_b, s_t);
+    float q;
+    if (t.fast && amax_bits >= 0x0D80u) {
+        const float a6 = div_from_rcp(amax_b, 6.0f, 1.0f / 6.0f);
+        const float q0 = __fmul_rn(a6, t.rst);
+        if (q0 > 470.0f) {              // beyond 464 + one ulp: saturates to 448
+            sat = true;
+            return 0x7Eu;
+        }
+        q = __fmaf_rn(-__fmaf_rn(q0, t.s_t, -a6), t.rst, q0);
+    } else {
+        q = nv_exact_block_q(amax_b, t.s_t);
+    }
+    sat = q >= 464.0f;
     return cvt_e4m3x2(q, 0.0f) & 0xFFu;
 }
 
-__device__ __forceinline__ float rcp_approx(float d) {
-    float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(d));
+// Eight values -> eight E2M1 nibbles (element i in nibble i), RNE with
+// saturation, four cvt and one byte pack.
+__device__ __forceinline__ uint32_t pack8_e2m1(const float* v) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r) : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
     return r;
 }
 
-// NVFP4: encode n values (multiple of 8) of one block with scale byte sb.
+// NVFP4: encode n values (multiple of 8) of one block with scale byte sb:
+// code = E2M1(RNE(x / d)), d = RN(s_b s_t), x / d correctly rounded.  Within
+// the scale's range |x / d| <= 9 and the reciprocal route applies while d
+// and 1 / d are normal; saturated blocks and subnormal d divide exactly.
 template <int N>
-__device__ __forceinline__ void nv_encode(const float* x, uint32_t sb, float s_t, uint32_t* out) {
+__device__ __forceinline__ void nv_encode(const float* x, uint32_t sb, bool sat, float s_t, uint32_t* out) {
     if (sb == 0 || sb == 0x7F) {
 #pragma unroll
         for (int i = 0; i < N / 8; i++) out[i] = 0u;
         return;
     }
     const float d = __fmul_rn(e4m3_to_float(sb), s_t);
-    // The E2M1 code of RN(x / d) only depends on which side of the rounding
-    // midpoints {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5} (and of the binade
-    // edges) the quotient falls.  With r within one ulp of 1/d (hardware
-    // reciprocal), q0 = RN(x * r) is within about 3 ulp of x / d, so whenever
-    // q0 is more than 15 ulps away from every value with at most two
-    // significant mantissa bits (the midpoints are such values) it yields
-    // the same code; otherwise the exact IEEE division decides.
-    const float r = rcp_approx(d);
+    const float r = __frcp_rn(d);
     float v[N];
-    bool near = false;          // any quotient within 15 ulp of a 2-bit value
+    if (!sat && d >= 1.17549435e-38f && r < 1.0e38f) {
 #pragma unroll
-    for (int i = 0; i < N; i++) {
-        v[i] = __fmul_rn(x[i], r);
-        near |= ((__float_as_uint(v[i]) & 0x1FFFFFu) - 16u) > (0x1FFFEFu - 16u);
-    }
-    if (near) {
+        for (int i = 0; i < N; i++) v[i] = div_from_rcp(x[i], d, r);
+    } else {
 #pragma unroll
-        for (int i = 0; i < N; i++)
-            if (((__float_as_uint(v[i]) & 0x1FFFFFu) - 16u) > (0x1FFFEFu - 16u)) v[i] = __fdiv_rn(x[i], d);
+        for (int i = 0; i < N; i++) v[i] = nv_exact_div(x[i], d);
     }
 #pragma unroll
-    for (int i = 0; i < N / 8; i++) out[i] = pack8_fp4(v + 8 * i);
+    for (int i = 0; i < N / 8; i++) out[i] = pack8_e2m1(v + 8 * i);
 }
 
 __device__ __forceinline__ float nv_tensor_scale(const unsigned* amax_bits) {
@@ -205,11 +240,8 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
     const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
     const bool vec_sf = (blocks_per_row & 3u) == 0;
-    float s_t = 1.0f, inv_st = 1.0f;
-    if (FMT == kNVFP4) {
-        s_t = nv_scale_of(nv);
-        inv_st = __frcp_rn(s_t);
-    }
+    NvT nt{1.0f, 1.0f, true};
+    if (FMT == kNVFP4) nt = nv_tensor_consts(nv_scale_of(nv));
 
     // software pipeline: the loads of the next iteration are in flight while
     // the current chunks are encoded
@@ -242,11 +274,12 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
             uint32_t am = absmax8(w[u]);
             am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
             if (LPB == 4) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t, inv_st) : mx_scale_byte<FMT>(am);
+            bool sat = false;
+            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, nt, sat) : mx_scale_byte<FMT>(am);
             float f[8];
             unpack8(w[u], f);
             uint32_t out[2];
-            if (FMT == kNVFP4) nv_encode<8>(f, sb, s_t, out);
+            if (FMT == kNVFP4) nv_encode<8>(f, sb, sat, nt.s_t, out);
             else mx_encode<FMT, 8>(f, sb, out);
             if (c < nchunks) {
                 if (is_fp4(FMT)) reinterpret_cast<uint32_t*>(codes)[c] = out[0];
@@ -297,8 +330,7 @@ quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t
     const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
     const bool vec_sf = (blocks_per_row & 3u) == 0;
-    const float s_t = nv_scale_of(nv);
-    const float inv_st = __frcp_rn(s_t);
+    const NvT nt = nv_tensor_consts(nv_scale_of(nv));
     uint32_t acc = 0;                 // delayed scaling: running amax of this tensor
     const int64_t step = nwarps * 32 * kNvUnroll;
     uint4 w[kNvUnroll][2];
@@ -332,12 +364,13 @@ quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t
                                         w[u][1].x, w[u][1].y, w[u][1].z, w[u][1].w};
                 nv_acc_group(acc, am, ws, 8);
             }
-            const uint32_t sb = nv_scale_byte(am, s_t, inv_st);
+            bool sat;
+            const uint32_t sb = nv_scale_byte(am, nt, sat);
             float f[16];
             unpack8(w[u][0], f);
             unpack8(w[u][1], f + 8);
             uint32_t out[2];
-            nv_encode<16>(f, sb, s_t, out);
+            nv_encode<16>(f, sb, sat, nt.s_t, out);
             if (b < nblocks) reinterpret_cast<uint2*>(codes)[b] = make_uint2(out[0], out[1]);
             const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
             const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
@@ -383,11 +416,8 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
     const int tid = threadIdx.x;
     const int64_t r0 = (int64_t)blockIdx.y * kTile;
     const int64_t c0 = (int64_t)blockIdx.x * kTile;
-    float s_t = 1.0f, inv_st = 1.0f;
-    if (FMT == kNVFP4) {
-        s_t = nv_scale_of(nv);
-        inv_st = __frcp_rn(s_t);
-    }
+    NvT nt{1.0f, 1.0f, true};
+    if (FMT == kNVFP4) nt = nv_tensor_consts(nv_scale_of(nv));
 
     // load: 128 rows x 16 chunks of 8 bf16
 #pragma unroll
@@ -424,9 +454,10 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
                 float f[BLK];
 #pragma unroll
                 for (int r = 0; r < BLK; r++) f[r] = half ? bf16hi(w[r]) : bf16lo(w[r]);
-                uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t, inv_st) : mx_scale_byte<FMT>(am);
+                bool sat = false;
+                uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, nt, sat) : mx_scale_byte<FMT>(am);
                 uint32_t out[BLK / 4];
-                if (FMT == kNVFP4) nv_encode<BLK>(f, sb, s_t, out);
+                if (FMT == kNVFP4) nv_encode<BLK>(f, sb, sat, nt.s_t, out);
                 else mx_encode<FMT, BLK>(f, sb, out);
                 const int cl = 2 * cp + half;
                 sf_col[cl * NB + rb] = (uint8_t)sb;
@@ -460,9 +491,10 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
                 am = max(am, absmax8(v));
                 unpack8(v, f + 8 * q);
             }
-            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, s_t, inv_st) : mx_scale_byte<FMT>(am);
+            bool sat = false;
+            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, nt, sat) : mx_scale_byte<FMT>(am);
             uint32_t out[BLK / 4];
-            if (FMT == kNVFP4) nv_encode<BLK>(f, sb, s_t, out);
+            if (FMT == kNVFP4) nv_encode<BLK>(f, sb, sat, nt.s_t, out);
             else mx_encode<FMT, BLK>(f, sb, out);
             sf_row[rr * NB + cb] = (uint8_t)sb;
             const int64_t gr = r0 + rr, gc = c0 + cb * BLK;

@@ -154,3 +154,20 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.bsq_debug_gemm_timeout(ctypes.byref(a), ctypes.byref(b2), C, 0, 1000, 0, null) == 1
     m4 = T(2, 0, 128, 256, 256, 256, None)
     assert lib.bsq_debug_gemm_timeout(ctypes.byref(m4), ctypes.byref(m4), C, 0, 1000, 1, null) == 2
+
+
+def test_binding_rejects_bad_group_offsets():
+    """The grouped calls read int64 device offsets the C ABI cannot check:
+    the binding rejects a wrong dtype, a host tensor, a strided view or a
+    wrong length before any CUDA call."""
+    import torch
+    import block_scaled_precision_03_gb300 as bsq
+    A = bsq.QTensor(0, 256, 256, None, None, None)
+    groups = [bsq.QTensor(0, 128, 256, None, None, None)] * 2
+    bad = [torch.zeros(3, dtype=torch.int32), torch.zeros(3, dtype=torch.int64), torch.zeros(6, dtype=torch.int64)[::2],
+           torch.zeros(4, dtype=torch.int64)]
+    for off in bad:
+        with pytest.raises(bsq.BsqError):
+            bsq.grouped_gemm_into(A, off, groups, None)
+        with pytest.raises(bsq.BsqError):
+            bsq.mxfp4_to_mxfp8_grouped_into(A, A, off, 2)
