@@ -310,6 +310,152 @@ quantize_rows_kernel(const uint4* __restrict__ src, int64_t nchunks, uint32_t bl
 }
 
 // ---------------------------------------------------------------------------
+// Row-wise MX kernel for 32-byte aligned source and codes: one thread = one
+// 32-element block, read with two 32-byte loads (a warp instruction covers
+// 32 whole sectors) and written with one 32-byte (FP8) or 16-byte (FP4)
+// store; the block amax needs no shuffle and the scale byte is computed once
+// per block.  Two blocks per thread per iteration, the next iteration's
+// loads in flight while these encode.
+// ---------------------------------------------------------------------------
+constexpr int kWideUnroll = 2;
+
+__device__ __forceinline__ void ld_v8(const void* p, uint32_t* r) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void st_v8(void* p, const uint32_t* r) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+// four FP32 values -> four FP8 codes in one word (first value in the low byte)
+template <int FMT>
+__device__ __forceinline__ uint32_t pack4_fp8(float a, float b, float c, float d) {
+    uint32_t r;
+    if (FMT == kE4M3)
+        asm("{\n\t.reg .b16 h0, h1;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
+            "mov.b32 %0, {h0, h1};\n\t}"
+            : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+    else
+        asm("{\n\t.reg .b16 h0, h1;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 h0, %2, %1;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 h1, %4, %3;\n\t"
+            "mov.b32 %0, {h0, h1};\n\t}"
+            : "=r"(r) : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kRowThreads)
+quantize_rows_wide_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row, int64_t s_tiles,
+                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    static_assert(FMT != kNVFP4, "MX formats only");
+    constexpr int U = kWideUnroll;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
+    const bool vec_sf = (blocks_per_row & 3u) == 0;
+    // a warp takes U x 32 consecutive blocks per iteration (lane-consecutive
+    // within each u, so the four blocks of one scale word sit in four lanes)
+    const int64_t step = nwarps * 32 * U;
+    int64_t base = warp * 32 * U;
+    uint32_t w[U][16];
+#pragma unroll
+    for (int u = 0; u < U; u++) {
+        const int64_t b = base + u * 32 + lane;
+        if (b < nblocks) {
+            ld_v8(src + b * 64, w[u]);
+            ld_v8(src + b * 64 + 32, w[u] + 8);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; k++) w[u][k] = 0;
+        }
+    }
+    const int64_t b0 = base + lane;
+    uint32_t rb = (uint32_t)(b0 / blocks_per_row);
+    uint32_t jb = (uint32_t)(b0 - (int64_t)rb * blocks_per_row);
+    const uint32_t uq = 32u / blocks_per_row, ur = 32u % blocks_per_row;
+    const uint32_t dq = (uint32_t)(step / blocks_per_row), dr = (uint32_t)(step % blocks_per_row);
+    for (; base < nblocks; base += step) {
+        uint32_t wn[U][16];
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t b = base + step + u * 32 + lane;
+            if (b < nblocks) {
+                ld_v8(src + b * 64, wn[u]);
+                ld_v8(src + b * 64 + 32, wn[u] + 8);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; k++) wn[u][k] = 0;
+            }
+        }
+        uint32_t r = rb, j = jb;
+#pragma unroll
+        for (int u = 0; u < U; u++) {
+            const int64_t b = base + u * 32 + lane;
+            uint32_t m = 0;
+#pragma unroll
+            for (int k = 0; k < 16; k++) m = __vmaxu2(m, w[u][k] & 0x7FFF7FFFu);
+            const uint32_t sb = mx_scale_byte<FMT>(max(m & 0xFFFFu, m >> 16));
+            uint32_t out[8];
+            if (sb == 0xFFu) {
+                // NaN/Inf in the block: NaN scale, NaN codes (E2M1 has no NaN: 0)
+#pragma unroll
+                for (int k = 0; k < 8; k++) out[k] = is_fp4(FMT) ? 0u : 0x7F7F7F7Fu;
+            } else {
+                const float inv = mx_inv_scale(sb);
+                if (is_fp4(FMT)) {
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            f[2 * e] = bf16lo(w[u][4 * k + e]) * inv;
+                            f[2 * e + 1] = bf16hi(w[u][4 * k + e]) * inv;
+                        }
+                        out[k] = pack8_e2m1(f);
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; k++)
+                        out[k] = pack4_fp8<FMT>(bf16lo(w[u][2 * k]) * inv, bf16hi(w[u][2 * k]) * inv,
+                                                bf16lo(w[u][2 * k + 1]) * inv, bf16hi(w[u][2 * k + 1]) * inv);
+                }
+            }
+            if (b < nblocks) {
+                if (is_fp4(FMT)) *reinterpret_cast<uint4*>(codes + b * 16) = make_uint4(out[0], out[1], out[2], out[3]);
+                else st_v8(codes + b * 32, out);
+            }
+            // scale bytes: 4 consecutive blocks -> one 32-bit store when a row
+            // holds a multiple of 4 blocks, else one byte each
+            if (vec_sf) {
+                const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
+                const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
+                const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
+                if ((lane & 3) == 0 && b < nblocks)
+                    *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) =
+                        sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+            } else if (b < nblocks) {
+                scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb;
+            }
+            j += ur;
+            r += uq;
+            if (j >= blocks_per_row) { j -= blocks_per_row; ++r; }
+        }
+#pragma unroll
+        for (int u = 0; u < U; u++)
+#pragma unroll
+            for (int k = 0; k < 16; k++) w[u][k] = wn[u][k];
+        jb += dr;
+        rb += dq;
+        if (jb >= blocks_per_row) { jb -= blocks_per_row; ++rb; }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // NVFP4 row-wise kernel: one thread = one 16-element block (two 16-byte
 // loads), so the per-block scale work is done once and needs no shuffle.
 // ---------------------------------------------------------------------------
@@ -395,11 +541,21 @@ quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t
 }
 
 // ---------------------------------------------------------------------------
-// Tile kernel for column-wise and both: 128 x 128 BF16 tile in smem.
+// Tile kernel for column-wise and both.  A CTA covers a 128 x 128 BF16 tile;
+// each thread loads an 8 x 8 sub-tile straight into registers (eight 16-byte
+// row loads) and encodes it in both directions without shared memory: the
+// 32 (NVFP4: 16) rows of a column block are the four (two) lanes of a warp
+// that differ in lane bits 0-1, the columns of a row block the lanes that
+// differ in bits 2-3, so block maxima are warp shuffles.  Warp w covers rows
+// 32 (w & 3).. and columns 64 (w >> 2)..; lane (q = lane & 3, g = lane >> 2)
+// rows 8 q.. and columns 8 g.. of it.  A column's 8 codes leave as one 8-byte
+// (FP4: 4-byte) store, four lanes filling 32 contiguous bytes; only the
+// scale bytes go through shared memory, to leave as 32-bit words.
 // ---------------------------------------------------------------------------
 constexpr int kTile = 128;
 constexpr int kTileThreads = 256;
-constexpr int kPitchW = kTile / 2 + 4;      // row pitch in 32-bit words (272 B)
+
+__device__ __forceinline__ uint32_t vmax4(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
 
 template <int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kTileThreads)
@@ -409,129 +565,121 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
                      const NvScale nv) {
     constexpr int BLK = block_of(FMT);
     constexpr int NB = kTile / BLK;                 // blocks per tile edge: 4 or 8
-    __shared__ __align__(16) uint32_t tile[kTile * kPitchW];
+    constexpr int LB = BLK / 8;                     // lanes per block along either axis: 4 or 2
     __shared__ __align__(16) uint8_t sf_col[kTile * NB];   // [column][row-block]
     __shared__ __align__(16) uint8_t sf_row[kTile * NB];   // [row][col-block]
 
-    const int tid = threadIdx.x;
-    const int64_t r0 = (int64_t)blockIdx.y * kTile;
-    const int64_t c0 = (int64_t)blockIdx.x * kTile;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q = lane & 3, g = lane >> 2;
+    const int tr = (warp & 3) * 32 + q * 8;         // sub-tile origin within the tile
+    const int tc = (warp >> 2) * 64 + g * 8;
+    const int64_t gr0 = (int64_t)blockIdx.y * kTile + tr;
+    const int64_t gc0 = (int64_t)blockIdx.x * kTile + tc;
+    const bool col_in = gc0 < C, row_in = gr0 < R;  // R % BLK == 0 and C % 8 == 0: chunks are whole
     NvT nt{1.0f, 1.0f, true};
     if (FMT == kNVFP4) nt = nv_tensor_consts(nv_scale_of(nv));
 
-    // load: 128 rows x 16 chunks of 8 bf16
+    uint4 w[8];
 #pragma unroll
-    for (int i = 0; i < (kTile * 16) / kTileThreads; i++) {
-        int idx = tid + i * kTileThreads;
-        int rr = idx >> 4, ch = idx & 15;
-        int64_t gr = r0 + rr, gc = c0 + ch * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (gr < R && gc < C) v = ld_stream(reinterpret_cast<const uint4*>(src + gr * C + gc));
-        *reinterpret_cast<uint4*>(&tile[rr * kPitchW + ch * 4]) = v;
-    }
-    __syncthreads();
+    for (int i = 0; i < 8; i++)
+        w[i] = (row_in && col_in) ? ld_stream(reinterpret_cast<const uint4*>(src + (gr0 + i) * C + gc0))
+                                  : make_uint4(0, 0, 0, 0);
 
-    uint32_t acc = 0;
     if (COL) {
-        // task = (row-block rb, column pair cp): two columns x BLK rows
-        constexpr int TASKS = NB * (kTile / 2);
-#pragma unroll 1
-        for (int id = tid; id < TASKS; id += kTileThreads) {
-            const int cp = id % (kTile / 2), rb = id / (kTile / 2);
-            uint32_t w[BLK];
-            uint32_t am_lo = 0, am_hi = 0;
+        // column maxima of the 8 rows (packed |bf16| pairs), then across the block's lanes
+        uint32_t cm[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int r = 0; r < BLK; r++) {
-                w[r] = tile[(rb * BLK + r) * kPitchW + cp];
-                am_lo = max(am_lo, w[r] & 0x7FFFu);
-                am_hi = max(am_hi, (w[r] >> 16) & 0x7FFFu);
-            }
-            // delayed scaling: this tile's finite amax (zero-filled padding adds nothing)
-            if (FMT == kNVFP4 && nv.amax_acc) nv_acc_group(acc, max(am_lo, am_hi), w, BLK);
+        for (int i = 0; i < 8; i++) {
+            cm[0] = vmax4(cm[0], w[i].x & 0x7FFF7FFFu);
+            cm[1] = vmax4(cm[1], w[i].y & 0x7FFF7FFFu);
+            cm[2] = vmax4(cm[2], w[i].z & 0x7FFF7FFFu);
+            cm[3] = vmax4(cm[3], w[i].w & 0x7FFF7FFFu);
+        }
+        if (FMT == kNVFP4 && nv.amax_acc) {
+            // delayed scaling: this tensor's finite amax (zero padding adds nothing)
+            uint32_t acc = 0;
+            const uint32_t m = vmax4(vmax4(cm[0], cm[1]), vmax4(cm[2], cm[3]));
+            if (((m & 0xFFFFu) >= 0x7F80u) || ((m >> 16) >= 0x7F80u)) {
 #pragma unroll
-            for (int half = 0; half < 2; half++) {
-                const uint32_t am = half ? am_hi : am_lo;
-                float f[BLK];
-#pragma unroll
-                for (int r = 0; r < BLK; r++) f[r] = half ? bf16hi(w[r]) : bf16lo(w[r]);
-                bool sat = false;
-                uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, nt, sat) : mx_scale_byte<FMT>(am);
-                uint32_t out[BLK / 4];
-                if (FMT == kNVFP4) nv_encode<BLK>(f, sb, sat, nt.s_t, out);
-                else mx_encode<FMT, BLK>(f, sb, out);
-                const int cl = 2 * cp + half;
-                sf_col[cl * NB + rb] = (uint8_t)sb;
-                const int64_t gc = c0 + cl, gr = r0 + rb * BLK;
-                if (gc < C && gr < R) {
-                    if (is_fp4(FMT)) {
-                        uint8_t* dst = codes_c + gc * (R / 2) + gr / 2;
-                        if (BLK == 32) *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
-                        else *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
-                    } else {
-                        uint8_t* dst = codes_c + gc * R + gr;
-                        *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
-                        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(out[4], out[5], out[6], out[7]);
-                    }
+                for (int i = 0; i < 8; i++) {
+                    const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+                    nv_acc_group(acc, 0x7F80u, ws, 4);
                 }
+            } else {
+                acc = max(m & 0xFFFFu, m >> 16);
             }
+            nv_acc_flush(nv, acc);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            cm[k] = vmax4(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 1));
+            if (LB == 4) cm[k] = vmax4(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 2));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+            const uint32_t am = (j & 1) ? (cm[j >> 1] >> 16) : (cm[j >> 1] & 0xFFFFu);
+            bool sat = false;
+            const uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, nt, sat) : mx_scale_byte<FMT>(am);
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const uint32_t word = (j >> 1) == 0 ? w[i].x : ((j >> 1) == 1 ? w[i].y : ((j >> 1) == 2 ? w[i].z : w[i].w));
+                f[i] = (j & 1) ? bf16hi(word) : bf16lo(word);
+            }
+            uint32_t out[2];
+            if (FMT == kNVFP4) nv_encode<8>(f, sb, sat, nt.s_t, out);
+            else mx_encode<FMT, 8>(f, sb, out);
+            if (row_in && col_in) {
+                const int64_t gc = gc0 + j;
+                if (is_fp4(FMT)) *reinterpret_cast<uint32_t*>(codes_c + gc * (R / 2) + gr0 / 2) = out[0];
+                else *reinterpret_cast<uint2*>(codes_c + gc * R + gr0) = make_uint2(out[0], out[1]);
+            }
+            if ((q % LB) == 0) sf_col[(tc + j) * NB + tr / BLK] = (uint8_t)sb;
         }
     }
-    if (FMT == kNVFP4 && nv.amax_acc) nv_acc_flush(nv, acc);
     if (ROW) {
-        // task = (row rr, column block cb): BLK contiguous elements
-        constexpr int TASKS = kTile * NB;
-#pragma unroll 1
-        for (int id = tid; id < TASKS; id += kTileThreads) {
-            const int rr = id % kTile, cb = id / kTile;
-            float f[BLK];
-            uint32_t am = 0;
 #pragma unroll
-            for (int q = 0; q < BLK / 8; q++) {
-                uint4 v = *reinterpret_cast<const uint4*>(&tile[rr * kPitchW + cb * (BLK / 2) + q * 4]);
-                am = max(am, absmax8(v));
-                unpack8(v, f + 8 * q);
-            }
+        for (int i = 0; i < 8; i++) {
+            uint32_t am = absmax8(w[i]);
+            am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 4));
+            if (LB == 4) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 8));
             bool sat = false;
-            uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, nt, sat) : mx_scale_byte<FMT>(am);
-            uint32_t out[BLK / 4];
-            if (FMT == kNVFP4) nv_encode<BLK>(f, sb, sat, nt.s_t, out);
-            else mx_encode<FMT, BLK>(f, sb, out);
-            sf_row[rr * NB + cb] = (uint8_t)sb;
-            const int64_t gr = r0 + rr, gc = c0 + cb * BLK;
-            if (gr < R && gc < C) {
-                if (is_fp4(FMT)) {
-                    uint8_t* dst = codes_r + gr * (C / 2) + gc / 2;
-                    if (BLK == 32) *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
-                    else *reinterpret_cast<uint2*>(dst) = make_uint2(out[0], out[1]);
-                } else {
-                    uint8_t* dst = codes_r + gr * C + gc;
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
-                    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(out[4], out[5], out[6], out[7]);
-                }
+            const uint32_t sb = FMT == kNVFP4 ? nv_scale_byte(am, nt, sat) : mx_scale_byte<FMT>(am);
+            float f[8];
+            unpack8(w[i], f);
+            uint32_t out[2];
+            if (FMT == kNVFP4) nv_encode<8>(f, sb, sat, nt.s_t, out);
+            else mx_encode<FMT, 8>(f, sb, out);
+            if (row_in && col_in) {
+                const int64_t gr = gr0 + i;
+                if (is_fp4(FMT)) *reinterpret_cast<uint32_t*>(codes_r + gr * (C / 2) + gc0 / 2) = out[0];
+                else *reinterpret_cast<uint2*>(codes_r + gr * C + gc0) = make_uint2(out[0], out[1]);
             }
+            if ((g % LB) == 0) sf_row[(tr + i) * NB + tc / BLK] = (uint8_t)sb;
         }
     }
     __syncthreads();
     // scale stores: groups of 4 consecutive blocks -> one 32-bit word
+    const int64_t r0 = (int64_t)blockIdx.y * kTile, c0 = (int64_t)blockIdx.x * kTile;
     constexpr int G = NB / 4;
     if (COL) {
         const int64_t S = R / BLK;                       // scale columns of the [C, R] output
         for (int id = tid; id < kTile * G; id += kTileThreads) {
-            const int cl = id / G, g = id % G;
-            const int64_t gc = c0 + cl, sc = r0 / BLK + 4 * g;
+            const int cl = id / G, gg = id % G;
+            const int64_t gc = c0 + cl, sc = r0 / BLK + 4 * gg;
             if (gc < C && sc < S)
                 *reinterpret_cast<uint32_t*>(scales_c + sf_offset(gc, sc, s_tiles_c)) =
-                    *reinterpret_cast<const uint32_t*>(&sf_col[cl * NB + 4 * g]);
+                    *reinterpret_cast<const uint32_t*>(&sf_col[cl * NB + 4 * gg]);
         }
     }
     if (ROW) {
         const int64_t S = C / BLK;
         for (int id = tid; id < kTile * G; id += kTileThreads) {
-            const int rr = id / G, g = id % G;
-            const int64_t gr = r0 + rr, sc = c0 / BLK + 4 * g;
+            const int rr = id / G, gg = id % G;
+            const int64_t gr = r0 + rr, sc = c0 / BLK + 4 * gg;
             if (gr < R && sc < S)
                 *reinterpret_cast<uint32_t*>(scales_r + sf_offset(gr, sc, s_tiles_r)) =
-                    *reinterpret_cast<const uint32_t*>(&sf_row[rr * NB + 4 * g]);
+                    *reinterpret_cast<const uint32_t*>(&sf_row[rr * NB + 4 * gg]);
         }
     }
 }
@@ -611,6 +759,26 @@ __global__ void nv_delayed_finalize_kernel(float* hist, int n, float* ts0, float
 template <int FMT>
 static cudaError_t launch_rows(const void* src, int64_t R, int64_t C, uint8_t* codes, uint8_t* scales,
                                const NvScale& nv, cudaStream_t st, int num_sms) {
+    const bool wide = ((reinterpret_cast<uintptr_t>(src) & 31) == 0) &&
+                      (is_fp4(FMT) || (reinterpret_cast<uintptr_t>(codes) & 31) == 0);
+    if (FMT != kNVFP4 && wide) {
+        // persistent grid: as many CTAs as fit on the SMs at once
+        static int resident = 0;
+        if (resident == 0 &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, quantize_rows_wide_kernel<FMT == kNVFP4 ? kE4M3 : FMT>,
+                                                          kRowThreads, 0) != cudaSuccess)
+            resident = 4;
+        if (resident < 1) resident = 1;
+        const int64_t nblocks = R * C / 32;
+        const int64_t per_cta = (int64_t)kRowThreads * kWideUnroll;
+        int64_t grid = (nblocks + per_cta - 1) / per_cta;
+        if (grid > (int64_t)num_sms * resident) grid = (int64_t)num_sms * resident;
+        if (grid < 1) grid = 1;
+        const int64_t S = C / 32;
+        quantize_rows_wide_kernel<FMT == kNVFP4 ? kE4M3 : FMT><<<(unsigned)grid, kRowThreads, 0, st>>>(
+            reinterpret_cast<const uint8_t*>(src), nblocks, (uint32_t)S, (S + 3) / 4, codes, scales);
+        return cudaGetLastError();
+    }
     const int64_t nchunks = R * C / 8;
     const int64_t per_cta = (int64_t)kRowThreads * kRowUnroll;
     int64_t grid = (nchunks + per_cta - 1) / per_cta;

@@ -413,6 +413,29 @@ def test_gemm_wait_limit_runs_out_then_recovers(bsq, fmt, kernel, limit_ns):
     assert ok.all(), f"{(~ok).sum()} outputs outside the bound after the timed-out GEMM"
 
 
+@pytest.mark.parametrize("fmt", ["mxfp8_e4m3", "mxfp8_e5m2", "mxfp4", "nvfp4"])
+@pytest.mark.parametrize("src_off,codes_off", [(16, 0), (0, 16), (16, 16)])
+def test_row_quantize_16_byte_aligned_buffers(bsq, fmt, src_off, codes_off):
+    # the row kernels read and write 32 bytes per instruction when both
+    # buffers are 32-byte aligned; 16-byte aligned buffers take the other path
+    import torch
+    R, C = 96, 1056
+    x = inputs.outlier_activations_bf16((R, C), 71)
+    buf = torch.empty(R * C + 64, dtype=torch.bfloat16, device="cuda")
+    base = (-buf.data_ptr() // 2) % 16                      # first element on a 32-byte boundary
+    xd = buf[base + src_off // 2:base + src_off // 2 + R * C].view(R, C)
+    xd.copy_(dev_bf16(x))
+    assert xd.data_ptr() % 32 == src_off
+    out = poisoned_qtensor(bsq, fmt, R, C)
+    if codes_off:
+        cb = torch.full((out.codes.numel() + 64,), 0xAB, dtype=torch.uint8, device="cuda")
+        cbase = (-cb.data_ptr()) % 32
+        out.codes = cb[cbase + codes_off:cbase + codes_off + out.codes.numel()]
+        assert out.codes.data_ptr() % 32 == codes_off
+    bsq.quantize_into(xd, fmt, "row", out, None)
+    assert_qtensor_equal(out, expected(x, fmt, "row")["row"], f"{fmt} src+{src_off} codes+{codes_off}")
+
+
 def test_quantize_rejects_unaligned_cols(bsq):
     x = inputs.normal_bf16((96, 130), 1)
     with pytest.raises(bsq.BsqError) as ei:
