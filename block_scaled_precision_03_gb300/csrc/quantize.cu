@@ -15,11 +15,36 @@
 //
 // NVFP4 (FP8 page, section "MXFP8 e NVFP4 do Blackwell"): a tensor amax
 // pass, then per 16-block UE4M3 scales against the FP32 tensor scale
-// amax / (448 * 6), each step an IEEE FP32 operation.
+// amax / (448 * 6), each step an IEEE FP32 operation.  Row-wise with
+// just-in-time scaling both run in one cooperative kernel with a grid-wide
+// barrier between them; column-wise and both run the amax pass, then the
+// tile kernel as its programmatic dependent.
 #include "common.cuh"
 #include "internal.h"
 
 namespace bsq {
+
+// ---------------------------------------------------------------------------
+// Division of 32-bit unsigned integers by an invariant divisor d (1 <= d <
+// 2^31), after Granlund and Montgomery, "Division by invariant integers
+// using multiplication" (PLDI 1994), the round-up method: with l = ceil(log2
+// d) and m = floor(2^32 (2^l - d) / d) + 1, n / d = (t + ((n - t) >> 1)) >>
+// (l - 1) where t = umulhi(m, n), for every 32-bit n; d = 1 is n itself.
+// ---------------------------------------------------------------------------
+struct DivU32 {
+    uint32_t m, l;
+};
+static DivU32 make_div_u32(uint32_t d) {
+    uint32_t l = 0;
+    while (l < 32 && (1ull << l) < d) l++;
+    const uint64_t m = ((((1ull << l) - d) << 32) / d) + 1;
+    return DivU32{(uint32_t)m, l};
+}
+__device__ __forceinline__ uint32_t div_u32(uint32_t n, DivU32 q) {
+    if (q.l == 0) return n;
+    const uint32_t t = __umulhi(q.m, n);
+    return (t + ((n - t) >> 1)) >> (q.l - 1);
+}
 
 // ---------------------------------------------------------------------------
 // Block encoders working on registers.
@@ -149,9 +174,14 @@ __device__ __forceinline__ void nv_encode(const float* x, uint32_t sb, bool sat,
     for (int i = 0; i < N / 8; i++) out[i] = pack8_e2m1(v + 8 * i);
 }
 
-__device__ __forceinline__ float nv_tensor_scale(const unsigned* amax_bits) {
-    float amax = __uint_as_float(*amax_bits);
-    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+// Just in time, the amax pass leaves max over CTAs of RN(amax_cta / 2688)
+// in the tensor-scale slot.  Division by a positive constant is monotone, so
+// that max is RN(amax / 2688) of the tensor amax; a slot still at 0 means
+// the tensor has no nonzero finite value, and s_t = 1.
+__device__ __forceinline__ float nv_tensor_scale(const unsigned* ts_bits) {
+    unsigned b;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(b) : "l"(ts_bits) : "memory");
+    return b == 0u ? 1.0f : __uint_as_float(b);
 }
 
 // Where a kernel takes the NVFP4 tensor scale from: the amax of this tensor
@@ -161,7 +191,8 @@ __device__ __forceinline__ float nv_tensor_scale(const unsigned* amax_bits) {
 // largest positive finite entry of the amax history; then this tensor's
 // amax is accumulated in the same pass for the history update.
 struct NvScale {
-    const unsigned* amax_bits;     // just in time: tensor amax (FP32 bits)
+    unsigned* ts_bits;             // just in time: the tensor-scale slot the amax pass filled
+    float* ts_other;               // just in time: a second tensor-scale output (both axes), or nullptr
     const float* history;          // delayed: amax history (nullptr: just in time)
     int32_t hist_len;
     unsigned* amax_acc;            // delayed: this tensor's amax accumulates here (FP32 bits)
@@ -177,8 +208,24 @@ __device__ __forceinline__ float nv_history_scale(const float* h, int n) {
 }
 
 __device__ __forceinline__ float nv_scale_of(const NvScale& ns) {
-    return ns.history ? nv_history_scale(ns.history, ns.hist_len) : nv_tensor_scale(ns.amax_bits);
+    return ns.history ? nv_history_scale(ns.history, ns.hist_len) : nv_tensor_scale(ns.ts_bits);
 }
+
+// Just in time, one thread of the quantize grid completes the tensor-scale
+// outputs: an all-zero tensor's slot becomes 1.0 (threads still reading it
+// see 0 or 1.0, both meaning s_t = 1), and a second output gets a copy.
+__device__ __forceinline__ void nv_publish_scale(const NvScale& ns, float s_t) {
+    if (ns.history) return;
+    atomicCAS(ns.ts_bits, 0u, __float_as_uint(1.0f));
+    if (ns.ts_other) *ns.ts_other = s_t;
+}
+
+// Programmatic dependent launch: a quantize kernel launched with programmatic
+// stream serialization may start while the amax pass before it still runs;
+// it waits here before its first read of the tensor scale.  Under an
+// ordinary launch both instructions do nothing.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Running max of finite |x| (BF16 bit patterns without sign): `am` is the
 // max over a group of values given as packed words `w`; a group holding a
@@ -212,6 +259,15 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 __device__ __forceinline__ void unpack8(const uint4& w, float* f) {
     f[0] = bf16lo(w.x); f[1] = bf16hi(w.x); f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
     f[4] = bf16lo(w.z); f[5] = bf16hi(w.z); f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+}
+
+// Per half, the BF16 value of larger magnitude (sign the XOR of the signs,
+// NaN if either is NaN): the magnitudes of max.NaN.xorsign.abs are exact,
+// subnormals included, so |result| & 0x7FFF is the larger |x| bit pattern.
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 // largest |x| bit pattern of 8 bf16 values (packed 16-bit max on the
@@ -396,10 +452,13 @@ quantize_rows_wide_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint
 #pragma unroll
         for (int u = 0; u < U; u++) {
             const int64_t b = base + u * 32 + lane;
-            uint32_t m = 0;
+            uint32_t m8[8];
 #pragma unroll
-            for (int k = 0; k < 16; k++) m = __vmaxu2(m, w[u][k] & 0x7FFF7FFFu);
-            const uint32_t sb = mx_scale_byte<FMT>(max(m & 0xFFFFu, m >> 16));
+            for (int k = 0; k < 8; k++) m8[k] = bmax2(w[u][2 * k], w[u][2 * k + 1]);
+            uint32_t m = bmax2(bmax2(bmax2(m8[0], m8[1]), bmax2(m8[2], m8[3])),
+                               bmax2(bmax2(m8[4], m8[5]), bmax2(m8[6], m8[7])));
+            m = bmax2(m, __byte_perm(m, 0, 0x1032)) & 0x7FFFu;
+            const uint32_t sb = mx_scale_byte<FMT>(m);
             uint32_t out[8];
             if (sb == 0xFFu) {
                 // NaN/Inf in the block: NaN scale, NaN codes (E2M1 has no NaN: 0)
@@ -456,11 +515,14 @@ quantize_rows_wide_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint
 }
 
 // ---------------------------------------------------------------------------
-// NVFP4 row-wise kernel: one thread = one 16-element block (two 16-byte
-// loads), so the per-block scale work is done once and needs no shuffle.
+// NVFP4 row-wise kernel: a thread takes two consecutive 16-element blocks
+// per iteration (two 32-byte loads, or four 16-byte loads when the input is
+// only 16-byte aligned) and loads the next two before encoding these.  Each
+// block's scale work is done once, by its thread; d and -RN(1 / d) for the
+// 126 finite scale codes come from a table each CTA builds once, and the
+// element quotients run two at a time on the packed FP32 pipe.
 // ---------------------------------------------------------------------------
-constexpr int kNvUnroll = 1;
-constexpr int kNvMinBlocks = 4;     // CTAs per SM the register budget must allow
+constexpr int kNvMinBlocks = 3;     // CTAs per SM the register budget must allow
 
 __device__ __forceinline__ uint4 ld_cached(const uint4* p) {
     uint4 r;
@@ -468,76 +530,194 @@ __device__ __forceinline__ uint4 ld_cached(const uint4* p) {
     return r;
 }
 
-template <bool DELAYED>
-__global__ void __launch_bounds__(kRowThreads, kNvMinBlocks)
-quantize_rows_nv_kernel(const uint4* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row, int64_t s_tiles,
-                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, const NvScale nv) {
+// blocks b and b + 1 (zeros past the end) into w[0..7] and w[8..15]
+template <bool V8>
+__device__ __forceinline__ void ld_nv_pair(const uint8_t* src, int64_t b, int64_t nblocks, uint32_t* w) {
+#pragma unroll
+    for (int u = 0; u < 2; u++) {
+        uint32_t* o = w + 8 * u;
+        if (b + u < nblocks) {
+            if (V8) {
+                ld_v8(src + (b + u) * 32, o);
+            } else {
+                const uint4 lo = ld_cached(reinterpret_cast<const uint4*>(src + (b + u) * 32));
+                const uint4 hi = ld_cached(reinterpret_cast<const uint4*>(src + (b + u) * 32 + 16));
+                o[0] = lo.x; o[1] = lo.y; o[2] = lo.z; o[3] = lo.w;
+                o[4] = hi.x; o[5] = hi.y; o[6] = hi.z; o[7] = hi.w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; k++) o[k] = 0;
+        }
+    }
+}
+
+// Packed FP32 pairs (Blackwell f32x2 arithmetic, each half IEEE RN).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// -(x / d), correctly rounded, for both halves of x: div_from_rcp run with
+// -r in place of r.  Round to nearest is odd-symmetric, so every step yields
+// the exact negation of the corresponding div_from_rcp step, signed zeros
+// included: q0' = RN(x (-r)) = -q0, e' = RN(q0' d + x) = -e, and RN(e' (-r) +
+// q0') = -q.
+__device__ __forceinline__ uint64_t neg_div2(uint64_t x, uint64_t d2, uint64_t nr2) {
+    const uint64_t q0 = mul2(x, nr2);
+    const uint64_t e = fma2(q0, d2, x);
+    return fma2(e, nr2, q0);
+}
+
+// (d, -RN(1 / d)) of scale code c against s_t, the second 0 where the
+// reciprocal route does not apply (d or 1 / d outside the normal range);
+// codes 0 and 0x7F never reach it.
+__device__ __forceinline__ float2 nv_scale_entry(uint32_t c, float s_t) {
+    if (c == 0 || c >= 0x7F) return make_float2(0.0f, 0.0f);
+    const float d = __fmul_rn(e4m3_to_float(c), s_t);
+    const float r = __frcp_rn(d);
+    return make_float2(d, (d >= 1.17549435e-38f && r < 1.0e38f) ? -r : 0.0f);
+}
+
+// E2M1 codes of one block (8 BF16 pairs) with scale entry t into out[0..1]:
+// code(x / d) = code(-(x / d)) with the sign bit of every nibble flipped
+// (E2M1 is sign-magnitude and its rounding symmetric).
+__device__ __forceinline__ void nv_encode_pairs(const uint32_t* w, float2 t, bool fast, uint32_t* out) {
+    if (fast) {
+        const uint64_t d2 = f2(t.x, t.x), nr2 = f2(t.y, t.y);
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 4; k++)
+                f2split(neg_div2(f2(bf16lo(w[4 * h + k]), bf16hi(w[4 * h + k])), d2, nr2), v[2 * k], v[2 * k + 1]);
+            out[h] = pack8_e2m1(v) ^ 0x88888888u;
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                v[2 * k] = nv_exact_div(bf16lo(w[4 * h + k]), t.x);
+                v[2 * k + 1] = nv_exact_div(bf16hi(w[4 * h + k]), t.x);
+            }
+            out[h] = pack8_e2m1(v);
+        }
+    }
+}
+
+// largest |x| bit pattern of one block (8 BF16 pairs); NaN anywhere gives a
+// NaN pattern (above 0x7F80), like an Inf
+__device__ __forceinline__ uint32_t block_absmax(const uint32_t* w) {
+    const uint32_t m = bmax2(bmax2(bmax2(w[0], w[1]), bmax2(w[2], w[3])), bmax2(bmax2(w[4], w[5]), bmax2(w[6], w[7])));
+    return bmax2(m, __byte_perm(m, 0, 0x1032)) & 0x7FFFu;
+}
+
+// scale byte (returned) and the two code words of one block
+__device__ __forceinline__ uint32_t nv_quantize_block(const uint32_t* w, uint32_t am, const NvT& nt,
+                                                      const float2* tab, uint32_t* out) {
+    bool sat;
+    const uint32_t sb = nv_scale_byte(am, nt, sat);
+    if (sb == 0 || sb == 0x7F) {
+        out[0] = out[1] = 0u;
+    } else {
+        const float2 t = tab[sb];
+        nv_encode_pairs(w, t, !sat && t.y != 0.0f, out);
+    }
+    return sb;
+}
+
+// The row-wise pass over all blocks, two per lane per iteration, starting
+// from the blocks already loaded into w.  Codes of blocks below `nres` are
+// left unwritten (the fused kernel writes them last).
+template <bool DELAYED, bool V8>
+__device__ __forceinline__ void nv_rows_pass(const uint8_t* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row,
+                                             int64_t s_tiles, uint8_t* __restrict__ codes,
+                                             uint8_t* __restrict__ scales, const NvT& nt, const float2* tab,
+                                             int64_t nres, uint32_t (&w)[16], uint32_t& acc) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
     const bool vec_sf = (blocks_per_row & 3u) == 0;
-    const NvT nt = nv_tensor_consts(nv_scale_of(nv));
-    uint32_t acc = 0;                 // delayed scaling: running amax of this tensor
-    const int64_t step = nwarps * 32 * kNvUnroll;
-    uint4 w[kNvUnroll][2];
-    int64_t base = warp * 32 * kNvUnroll;
-    static_assert(kNvUnroll == 1, "the block coordinates below advance one block per iteration");
-    // row r and block column j of this lane's block, advanced by `step`
-    // blocks per iteration without a division
-    uint32_t r = (uint32_t)((base + lane) / blocks_per_row);
-    uint32_t j = (uint32_t)(base + lane - (int64_t)r * blocks_per_row);
+    const int64_t step = nwarps * 64;
+    int64_t base = warp * 64;
+    // row r and block column j of this lane's first block, advanced by
+    // `step` blocks per iteration without a division
+    uint32_t r = (uint32_t)((base + 2 * lane) / blocks_per_row);
+    uint32_t j = (uint32_t)(base + 2 * lane - (int64_t)r * blocks_per_row);
     const uint32_t dq = (uint32_t)(step / blocks_per_row), dr = (uint32_t)(step % blocks_per_row);
-#pragma unroll
-    for (int u = 0; u < kNvUnroll; u++) {
-        const int64_t b = base + u * 32 + lane;
-        w[u][0] = b < nblocks ? ld_cached(src + 2 * b) : make_uint4(0, 0, 0, 0);
-        w[u][1] = b < nblocks ? ld_cached(src + 2 * b + 1) : make_uint4(0, 0, 0, 0);
-    }
     for (; base < nblocks; base += step) {
-        uint4 wn[kNvUnroll][2];
+        uint32_t wn[16];
+        ld_nv_pair<V8>(src, base + step + 2 * lane, nblocks, wn);
+        const int64_t b = base + 2 * lane;
+        uint32_t sb[2], out[4];
 #pragma unroll
-        for (int u = 0; u < kNvUnroll; u++) {
-            const int64_t b = base + step + u * 32 + lane;
-            wn[u][0] = b < nblocks ? ld_cached(src + 2 * b) : make_uint4(0, 0, 0, 0);
-            wn[u][1] = b < nblocks ? ld_cached(src + 2 * b + 1) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < 2; u++) {
+            const uint32_t am = block_absmax(w + 8 * u);
+            if (DELAYED && b + u < nblocks) nv_acc_group(acc, am, w + 8 * u, 8);
+            sb[u] = nv_quantize_block(w + 8 * u, am, nt, tab, out + 2 * u);
         }
-#pragma unroll
-        for (int u = 0; u < kNvUnroll; u++) {
-            const int64_t b = base + u * 32 + lane;
-            const uint32_t am = max(absmax8(w[u][0]), absmax8(w[u][1]));
-            if (DELAYED && b < nblocks) {
-                const uint32_t ws[8] = {w[u][0].x, w[u][0].y, w[u][0].z, w[u][0].w,
-                                        w[u][1].x, w[u][1].y, w[u][1].z, w[u][1].w};
-                nv_acc_group(acc, am, ws, 8);
-            }
-            bool sat;
-            const uint32_t sb = nv_scale_byte(am, nt, sat);
-            float f[16];
-            unpack8(w[u][0], f);
-            unpack8(w[u][1], f + 8);
-            uint32_t out[2];
-            nv_encode<16>(f, sb, sat, nt.s_t, out);
-            if (b < nblocks) reinterpret_cast<uint2*>(codes)[b] = make_uint2(out[0], out[1]);
-            const uint32_t s1 = __shfl_down_sync(0xFFFFFFFFu, sb, 1);
-            const uint32_t s2 = __shfl_down_sync(0xFFFFFFFFu, sb, 2);
-            const uint32_t s3 = __shfl_down_sync(0xFFFFFFFFu, sb, 3);
-            if (b < nblocks) {
-                if (vec_sf) {
-                    if ((lane & 3) == 0)
-                        *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) =
-                            sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
-                } else {
-                    scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb;
-                }
+        if (b >= nres) {
+            if (b + 1 < nblocks)
+                *reinterpret_cast<uint4*>(codes + b * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+            else if (b < nblocks)
+                *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(out[0], out[1]);
+        }
+        const uint32_t pair = sb[0] | (sb[1] << 8);
+        const uint32_t next = __shfl_down_sync(0xFFFFFFFFu, pair, 1);
+        if (vec_sf) {
+            // blocks b .. b + 3 share a row and one scale word
+            if ((lane & 1) == 0 && b < nblocks)
+                *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) = pair | (next << 16);
+        } else {
+            if (b < nblocks) scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb[0];
+            if (b + 1 < nblocks) {
+                const bool wrap = j + 1 == blocks_per_row;
+                scales[sf_offset(wrap ? r + 1 : r, wrap ? 0 : j + 1, s_tiles)] = (uint8_t)sb[1];
             }
         }
 #pragma unroll
-        for (int u = 0; u < kNvUnroll; u++) { w[u][0] = wn[u][0]; w[u][1] = wn[u][1]; }
+        for (int k = 0; k < 16; k++) w[k] = wn[k];
         j += dr;
         r += dq;
         if (j >= blocks_per_row) { j -= blocks_per_row; ++r; }
     }
-    if (DELAYED) nv_acc_flush(nv, acc);
+}
+
+// Row-wise NVFP4 with delayed scaling: the tensor scale from the amax
+// history, this tensor's amax accumulated for the history update.
+template <bool V8>
+__global__ void __launch_bounds__(kRowThreads, kNvMinBlocks)
+quantize_rows_nv_delayed_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row,
+                                int64_t s_tiles, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                const NvScale nv) {
+    __shared__ float2 tab[128];
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
+    uint32_t w[16];
+    ld_nv_pair<V8>(src, warp * 64 + 2 * lane, nblocks, w);
+    const float s_t = nv_scale_of(nv);
+    const NvT nt = nv_tensor_consts(s_t);
+    if (threadIdx.x < 128) tab[threadIdx.x] = nv_scale_entry(threadIdx.x, s_t);
+    __syncthreads();
+    uint32_t acc = 0;
+    nv_rows_pass<true, V8>(src, nblocks, blocks_per_row, s_tiles, codes, scales, nt, tab, 0, w, acc);
+    nv_acc_flush(nv, acc);
 }
 
 // ---------------------------------------------------------------------------
@@ -576,14 +756,19 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
     const int64_t gr0 = (int64_t)blockIdx.y * kTile + tr;
     const int64_t gc0 = (int64_t)blockIdx.x * kTile + tc;
     const bool col_in = gc0 < C, row_in = gr0 < R;  // R % BLK == 0 and C % 8 == 0: chunks are whole
-    NvT nt{1.0f, 1.0f, true};
-    if (FMT == kNVFP4) nt = nv_tensor_consts(nv_scale_of(nv));
-
     uint4 w[8];
 #pragma unroll
     for (int i = 0; i < 8; i++)
         w[i] = (row_in && col_in) ? ld_stream(reinterpret_cast<const uint4*>(src + (gr0 + i) * C + gc0))
                                   : make_uint4(0, 0, 0, 0);
+    NvT nt{1.0f, 1.0f, true};
+    if (FMT == kNVFP4) {
+        // just in time, the tensor scale comes from the amax pass this grid may overlap
+        if (!nv.history) pdl_wait();
+        const float s_t = nv_scale_of(nv);
+        if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) nv_publish_scale(nv, s_t);
+        nt = nv_tensor_consts(s_t);
+    }
 
     if (COL) {
         // column maxima of the 8 rows (packed |bf16| pairs), then across the block's lanes
@@ -685,60 +870,273 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
 }
 
 // ---------------------------------------------------------------------------
-// NVFP4 tensor amax: max over finite |x| as FP32 bits (atomicMax on the
-// non-negative float bit pattern equals the float max).
+// NVFP4 tensor amax, just in time: max over finite |x|.  Each CTA reduces its
+// share and folds RN(amax_cta / 2688) into the tensor-scale slot with one
+// atomicMax on the FP32 bit pattern (for non-negative floats the integer
+// order is the float order).  A persistent grid sweeps the tensor from its
+// end to its start in NW-word chunks (8 words: one 32-byte load), so that
+// the quantize pass, which runs forward, first meets the part read last and
+// still held in L2.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
-amax_kernel(const uint4* __restrict__ src, int64_t nchunks, unsigned* __restrict__ amax_bits) {
+constexpr int kAmaxThreads = 256;
+constexpr int kAmaxUnroll = 4;
+
+template <int NW>
+__device__ __forceinline__ void ld_chunk(const uint32_t* p, uint32_t* w) {
+    if (NW == 8) {
+        ld_v8(p, w);
+    } else {
+        const uint4 v = ld_stream(reinterpret_cast<const uint4*>(p));
+        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    }
+}
+
+// running max of the finite |x| of one chunk (a chunk holding a non-finite
+// value can still hold finite ones)
+template <int NW>
+__device__ __forceinline__ void amax_chunk(uint32_t& am, const uint32_t* w) {
+    uint32_t m;
+    if (NW == 8)
+        m = bmax2(bmax2(bmax2(w[0], w[1]), bmax2(w[2], w[3])), bmax2(bmax2(w[4], w[5]), bmax2(w[6], w[7])));
+    else
+        m = bmax2(bmax2(w[0], w[1]), bmax2(w[2], w[3]));
+    m = bmax2(m, __byte_perm(m, 0, 0x1032)) & 0x7FFFu;
+    if (m < 0x7F80u) {
+        am = max(am, m);
+        return;
+    }
+#pragma unroll
+    for (int k = 0; k < NW; k++) {
+        const uint32_t lo = w[k] & 0x7FFFu, hi = (w[k] >> 16) & 0x7FFFu;
+        if (lo < 0x7F80u) am = max(am, lo);
+        if (hi < 0x7F80u) am = max(am, hi);
+    }
+}
+
+template <int NW>
+__global__ void __launch_bounds__(kAmaxThreads)
+amax_kernel(const uint32_t* __restrict__ src, int64_t nchunks, unsigned* __restrict__ ts_bits) {
+    // the quantize grid may be scheduled now; it waits for this grid's end
+    pdl_launch_dependents();
     uint32_t am = 0;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < nchunks; i += 4 * stride) {
-        uint4 a = ld_stream(src + i), b = ld_stream(src + i + stride);
-        uint4 c = ld_stream(src + i + 2 * stride), d = ld_stream(src + i + 3 * stride);
-        uint32_t m[4] = {absmax8(a), absmax8(b), absmax8(c), absmax8(d)};
+    const int64_t stride = (int64_t)gridDim.x * kAmaxThreads;
+    const uint32_t* last = src + (nchunks - 1) * NW;         // chunk i is read at last - i NW
+    int64_t i = (int64_t)blockIdx.x * kAmaxThreads + threadIdx.x;
+    for (; i + (kAmaxUnroll - 1) * stride < nchunks; i += kAmaxUnroll * stride) {
+        uint32_t w[kAmaxUnroll][NW];
 #pragma unroll
-        for (int k = 0; k < 4; k++) if (m[k] < 0x7F80u) am = max(am, m[k]);
-        // a chunk holding a non-finite value can still hold finite ones
+        for (int u = 0; u < kAmaxUnroll; u++) ld_chunk<NW>(last - (i + u * stride) * NW, w[u]);
 #pragma unroll
-        for (int k = 0; k < 4; k++) if (m[k] >= 0x7F80u) {
-            const uint4 v = k == 0 ? a : (k == 1 ? b : (k == 2 ? c : d));
-            const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                uint32_t lo = ws[q] & 0x7FFFu, hi = (ws[q] >> 16) & 0x7FFFu;
-                if (lo < 0x7F80u) am = max(am, lo);
-                if (hi < 0x7F80u) am = max(am, hi);
-            }
-        }
+        for (int u = 0; u < kAmaxUnroll; u++) amax_chunk<NW>(am, w[u]);
     }
     for (; i < nchunks; i += stride) {
-        uint4 v = ld_stream(src + i);
-        const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            uint32_t lo = ws[q] & 0x7FFFu, hi = (ws[q] >> 16) & 0x7FFFu;
-            if (lo < 0x7F80u) am = max(am, lo);
-            if (hi < 0x7F80u) am = max(am, hi);
-        }
+        uint32_t w[NW];
+        ld_chunk<NW>(last - i * NW, w);
+        amax_chunk<NW>(am, w);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, o));
-    __shared__ uint32_t red[8];
+    __shared__ uint32_t red[kAmaxThreads / 32];
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = am;
     __syncthreads();
     if (threadIdx.x == 0) {
         uint32_t m = 0;
-        for (int k = 0; k < (int)(blockDim.x >> 5); k++) m = max(m, red[k]);
-        if (m) atomicMax(amax_bits, m << 16);
+#pragma unroll
+        for (int k = 0; k < kAmaxThreads / 32; k++) m = max(m, red[k]);
+        if (m) atomicMax(ts_bits, __float_as_uint(__fdiv_rn(__uint_as_float(m << 16), 2688.0f)));
     }
 }
 
-// amax bits -> tensor scale s_t, written to one or two outputs.
-__global__ void nv_finalize_kernel(float* ts0, float* ts1) {
-    float s = nv_tensor_scale(reinterpret_cast<const unsigned*>(ts0));
-    *ts0 = s;
-    if (ts1) *ts1 = s;
+// ---------------------------------------------------------------------------
+// Row-wise NVFP4 just in time in one cooperative launch, one CTA per SM: the
+// amax sweep, a grid-wide barrier, the row pass.  Each CTA owns a contiguous
+// share of the tensor in both phases; inside a CTA the warps take items of
+// that share from a shared-memory counter, so that warps the scheduler
+// favours do more of the work instead of idling the SM at the end.  The
+// sweep runs through each share from its end, the pass from its start, so
+// the pass first meets what the sweep read last (still in L2 wherever the
+// tensor does not fit whole).
+//
+// The barrier needs no memory beyond the outputs.  The tensor-scale slot
+// (zeroed before the launch) counts arrivals: each CTA stores its partial
+// amax in code word blockIdx.x, adds 1 and waits (bounded) until all G CTAs
+// have; then each reads the G partials and adds 1 again.  The CTA whose
+// second add returns 2G - 1 knows every CTA has read the partials: it writes
+// the codes of the first `nres` blocks (the words that held partials, which
+// the pass leaves alone) and finally stores s_t into the slot.  A wait that
+// runs out records a timeout in the status word and ends its CTA.
+// ---------------------------------------------------------------------------
+constexpr int kFusedThreads = 768;
+constexpr int kFusedWarps = kFusedThreads / 32;
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// max over the CTA (every thread gets it); `red` holds one word per warp
+template <int NWARPS>
+__device__ __forceinline__ uint32_t cta_max(uint32_t v, uint32_t* red) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < NWARPS; k++) m = max(m, red[k]);
+    return m;
+}
+
+// the next item of this CTA's share for the calling warp (lane 0 takes it)
+__device__ __forceinline__ unsigned take_item(unsigned* counter) {
+    unsigned v = 0;
+    if ((threadIdx.x & 31) == 0) v = atomicAdd(counter, 1u);
+    return __shfl_sync(0xFFFFFFFFu, v, 0);
+}
+
+template <bool V8, typename IDX>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+quantize_rows_nv_fused_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row,
+                              DivU32 div_bpr, int64_t s_tiles, uint8_t* __restrict__ codes,
+                              uint8_t* __restrict__ scales, unsigned* __restrict__ slot,
+                              unsigned* __restrict__ status, uint64_t limit_ns) {
+    constexpr int NW = V8 ? 8 : 4;                  // words per amax chunk (32 or 16 bytes)
+    constexpr int kSweepItem = 32 * kAmaxUnroll;    // chunks per sweep item
+    __shared__ float2 tab[128];
+    __shared__ uint32_t red[kFusedWarps];
+    __shared__ uint32_t flag;
+    __shared__ unsigned counter;
+    const unsigned G = gridDim.x, cta = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) counter = kFusedWarps;            // warp w starts on item w
+    __syncthreads();
+
+    // ---- sweep: this CTA's share of the tensor amax, from the share's end
+    const int64_t nchunks = nblocks * (8 / NW);
+    const int64_t c0 = nchunks * cta / G, c1 = nchunks * (cta + 1) / G;
+    const int64_t n_sweep = (c1 - c0 + kSweepItem - 1) / kSweepItem;
+    const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
+    uint32_t am = 0;
+    for (int64_t it = warp; it < n_sweep;) {
+        uint32_t w[kAmaxUnroll][NW];
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; u++) {
+            const int64_t k = it * kSweepItem + u * 32 + lane;
+            if (c0 + k < c1) {
+                ld_chunk<NW>(s32 + (c1 - 1 - k) * NW, w[u]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < NW; q++) w[u][q] = 0;
+            }
+        }
+        it = take_item(&counter);
+#pragma unroll
+        for (int u = 0; u < kAmaxUnroll; u++) amax_chunk<NW>(am, w[u]);
+    }
+    am = cta_max<kFusedWarps>(am, red);
+
+    // ---- barrier
+    uint32_t* cw = reinterpret_cast<uint32_t*>(codes);
+    if (tid == 0) {
+        cw[cta] = am;
+        __threadfence();
+        atomicAdd(slot, 1u);
+        uint32_t ok = 1;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_u32(slot) < G) {
+            if (globaltimer_ns() - t0 > limit_ns) {
+                record_status(status, kStatusTimeout);
+                ok = 0;
+                break;
+            }
+            __nanosleep(32);
+        }
+        flag = ok;
+        counter = kFusedWarps;
+    }
+    __syncthreads();
+    if (!flag) return;
+    uint32_t m = 0;
+    for (unsigned k = tid; k < G; k += kFusedThreads) m = max(m, __ldcg(cw + k));
+    m = cta_max<kFusedWarps>(m, red);
+    const float s_t = m ? __fdiv_rn(__uint_as_float(m << 16), 2688.0f) : 1.0f;
+    unsigned second = 0;                             // read at the end: who read the partials last
+    if (tid == 0) {
+        __threadfence();
+        second = atomicAdd(slot, 1u);
+    }
+    if (tid < 128) tab[tid] = nv_scale_entry(tid, s_t);
+    __syncthreads();
+
+    // ---- row pass over this CTA's share, in items of 64 blocks (two per lane);
+    // block indices in IDX (32 bits unless the tensor has 2^32 blocks or more)
+    const NvT nt = nv_tensor_consts(s_t);
+    const IDX nb = (IDX)nblocks;
+    const IDX nres = (IDX)min(nblocks, 2 * (((int64_t)G + 3) / 4));   // 8 nres bytes >= 4 G
+    const bool vec_sf = (blocks_per_row & 3u) == 0;
+    const IDX n_items = (IDX)((nblocks + 63) / 64);
+    const IDX i0 = (IDX)((int64_t)n_items * cta / G), i1 = (IDX)((int64_t)n_items * (cta + 1) / G);
+    IDX it = i0 + warp;
+    uint32_t w[16];
+    if (it < i1) ld_nv_pair<V8>(src, (int64_t)(it * 64 + 2 * lane), nblocks, w);
+    while (it < i1) {
+        const IDX nx = i0 + take_item(&counter);
+        uint32_t wn[16];
+        if (nx < i1) ld_nv_pair<V8>(src, (int64_t)(nx * 64 + 2 * lane), nblocks, wn);
+        const IDX b = it * 64 + 2 * lane;
+        uint32_t sb[2], out[4];
+#pragma unroll
+        for (int u = 0; u < 2; u++) sb[u] = nv_quantize_block(w + 8 * u, block_absmax(w + 8 * u), nt, tab, out + 2 * u);
+        if (b >= nres) {
+            if (b + 1 < nb)
+                *reinterpret_cast<uint4*>(codes + (size_t)b * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+            else if (b < nb)
+                *reinterpret_cast<uint2*>(codes + (size_t)b * 8) = make_uint2(out[0], out[1]);
+        }
+        // row and block column of block b
+        uint32_t r, j;
+        if (sizeof(IDX) == 4) {
+            r = div_u32((uint32_t)b, div_bpr);
+            j = (uint32_t)b - r * blocks_per_row;
+        } else {
+            r = (uint32_t)(b / blocks_per_row);
+            j = (uint32_t)(b - (IDX)r * blocks_per_row);
+        }
+        const uint32_t pair = sb[0] | (sb[1] << 8);
+        const uint32_t next = __shfl_down_sync(0xFFFFFFFFu, pair, 1);
+        if (vec_sf) {
+            // blocks b .. b + 3 share a row and one scale word
+            if ((lane & 1) == 0 && b < nb)
+                *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) = pair | (next << 16);
+        } else {
+            if (b < nb) scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb[0];
+            if (b + 1 < nb) {
+                const bool wrap = j + 1 == blocks_per_row;
+                scales[sf_offset(wrap ? r + 1 : r, wrap ? 0 : j + 1, s_tiles)] = (uint8_t)sb[1];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; k++) w[k] = wn[k];
+        it = nx;
+    }
+
+    // ---- the CTA that read the partials last writes what they covered
+    if (tid == 0) flag = second == 2 * G - 1;
+    __syncthreads();
+    if (flag) {
+        __threadfence();
+        for (int64_t b = 2 * tid; b < (int64_t)nres; b += 2 * kFusedThreads) {
+            uint32_t v[16], out[4];
+            ld_nv_pair<V8>(src, b, (int64_t)nres, v);
+            nv_quantize_block(v, block_absmax(v), nt, tab, out);
+            nv_quantize_block(v + 8, block_absmax(v + 8), nt, tab, out + 2);
+            *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(out[0], out[1]);
+            if (b + 1 < (int64_t)nres) *reinterpret_cast<uint2*>(codes + b * 8 + 8) = make_uint2(out[2], out[3]);
+        }
+        if (tid == 0) *slot = __float_as_uint(s_t);
+    }
 }
 
 // Delayed scaling, after the quantize pass: the outputs get the tensor scale
@@ -756,6 +1154,35 @@ __global__ void nv_delayed_finalize_kernel(float* hist, int n, float* ts0, float
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
+// Launches kernel k; with `after_amax` as a programmatic dependent of the
+// kernel before it on the stream (the amax pass): k may be scheduled while
+// that kernel still runs and waits for its end in pdl_wait.
+template <typename... P, typename... A>
+static cudaError_t launch_k(bool after_amax, void (*k)(P...), dim3 grid, unsigned threads, cudaStream_t st,
+                            A... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = after_amax ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+// CTAs of k (256 threads) resident on one SM, asked once per kernel
+template <typename K>
+static int resident_ctas(K k, int fallback) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kRowThreads, 0) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = fallback;
+    }
+    return n;
+}
 template <int FMT>
 static cudaError_t launch_rows(const void* src, int64_t R, int64_t C, uint8_t* codes, uint8_t* scales,
                                const NvScale& nv, cudaStream_t st, int num_sms) {
@@ -798,11 +1225,12 @@ static cudaError_t launch_tile(const void* src, int64_t R, int64_t C, int axis,
     const int BLK = block_of(FMT);
     const int64_t str = (C / BLK + 3) / 4, stc = (R / BLK + 3) / 4;
     const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
+    const bool after_amax = FMT == kNVFP4 && !nv.history;
     if (axis == 3)
-        quantize_tile_kernel<FMT, true, true><<<grid, kTileThreads, 0, st>>>(s, R, C, cr, sr, str, cc, sc, stc, nv);
-    else
-        quantize_tile_kernel<FMT, false, true><<<grid, kTileThreads, 0, st>>>(s, R, C, cr, sr, str, cc, sc, stc, nv);
-    return cudaGetLastError();
+        return launch_k(after_amax, quantize_tile_kernel<FMT, true, true>, grid, kTileThreads, st,
+                        s, R, C, cr, sr, str, cc, sc, stc, nv);
+    return launch_k(after_amax, quantize_tile_kernel<FMT, false, true>, grid, kTileThreads, st,
+                    s, R, C, cr, sr, str, cc, sc, stc, nv);
 }
 
 cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
@@ -815,25 +1243,35 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
     if (a.col_scales && a.col_scales_pad) {
         if ((e = cudaMemsetAsync(a.col_scales, 0, a.col_scales_bytes, st)) != cudaSuccess) return e;
     }
-    unsigned* amax = nullptr;
+    unsigned* slot = nullptr;
     NvScale nv{};
     if (a.fmt == kNVFP4) {
-        // the tensor-scale output first holds the amax (FP32 bits)
-        amax = reinterpret_cast<unsigned*>(a.axis & 1 ? a.row_ts : a.col_ts);
-        if ((e = cudaMemsetAsync(amax, 0, sizeof(float), st)) != cudaSuccess) return e;
+        // just in time the slot collects the tensor scale, delayed the tensor amax
+        slot = reinterpret_cast<unsigned*>(a.axis & 1 ? a.row_ts : a.col_ts);
+        if ((e = cudaMemsetAsync(slot, 0, sizeof(float), st)) != cudaSuccess) return e;
     }
+    const bool src32 = (reinterpret_cast<uintptr_t>(a.src) & 31) == 0;
     if (a.fmt == kNVFP4 && a.history) {
         // delayed scaling: no amax pass; the quantize pass accumulates the amax
         nv.history = a.history;
         nv.hist_len = a.hist_len;
-        nv.amax_acc = amax;
-    } else if (a.fmt == kNVFP4) {
-        nv.amax_bits = amax;
-        int64_t nchunks = R * C / 8;
-        int64_t grid = (nchunks + 256 * 4 - 1) / (256 * 4);
-        if (grid > (int64_t)a.num_sms * 8) grid = (int64_t)a.num_sms * 8;
+        nv.amax_acc = slot;
+    } else if (a.fmt == kNVFP4 && a.axis != 1) {
+        nv.ts_bits = slot;
+        nv.ts_other = a.axis == 3 ? a.col_ts : nullptr;
+        // persistent grid, as many CTAs as fit on the SMs at once
+        static const int res8 = resident_ctas(amax_kernel<8>, 4), res4 = resident_ctas(amax_kernel<4>, 4);
+        const int NW = src32 ? 8 : 4;
+        const int64_t nchunks = R * C * 2 / (NW * 4);
+        int64_t grid = (nchunks + kAmaxThreads * kAmaxUnroll - 1) / (kAmaxThreads * kAmaxUnroll);
+        const int64_t cap = (int64_t)a.num_sms * (src32 ? res8 : res4);
+        if (grid > cap) grid = cap;
         if (grid < 1) grid = 1;
-        amax_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(a.src), nchunks, amax);
+        const uint32_t* s32 = reinterpret_cast<const uint32_t*>(a.src);
+        if (src32)
+            amax_kernel<8><<<(unsigned)grid, kAmaxThreads, 0, st>>>(s32, nchunks, slot);
+        else
+            amax_kernel<4><<<(unsigned)grid, kAmaxThreads, 0, st>>>(s32, nchunks, slot);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (a.axis == 1) {
@@ -842,26 +1280,45 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
         case kE5M2: e = launch_rows<kE5M2>(a.src, R, C, a.row_codes, a.row_scales, nv, st, a.num_sms); break;
         case kMXFP4: e = launch_rows<kMXFP4>(a.src, R, C, a.row_codes, a.row_scales, nv, st, a.num_sms); break;
         default: {
-            // persistent grid: as many CTAs as fit on the SMs at once
-            static int resident = 0;
-            if (resident == 0 &&
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, quantize_rows_nv_kernel<false>, kRowThreads, 0) !=
-                    cudaSuccess)
-                resident = kNvMinBlocks;
-            if (resident < 1) resident = 1;
             const int64_t nblocks = R * C / 16;
-            const int64_t per_cta = (int64_t)kRowThreads * kNvUnroll;
-            int64_t grid = (nblocks + per_cta - 1) / per_cta;
-            if (grid > (int64_t)a.num_sms * resident) grid = (int64_t)a.num_sms * resident;
-            if (grid < 1) grid = 1;
             const int64_t S = C / 16;
-            if (nv.amax_acc)
-                quantize_rows_nv_kernel<true><<<(unsigned)grid, kRowThreads, 0, st>>>(
-                    reinterpret_cast<const uint4*>(a.src), nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, nv);
-            else
-                quantize_rows_nv_kernel<false><<<(unsigned)grid, kRowThreads, 0, st>>>(
-                    reinterpret_cast<const uint4*>(a.src), nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, nv);
-            e = cudaGetLastError();
+            const uint8_t* s8 = reinterpret_cast<const uint8_t*>(a.src);
+            if (nv.history) {
+                // delayed: persistent grid, as many CTAs as fit on the SMs at once
+                static const int res_d = resident_ctas(quantize_rows_nv_delayed_kernel<true>, 1);
+                int64_t g = (nblocks + 2 * kRowThreads - 1) / (2 * kRowThreads);
+                if (g > (int64_t)a.num_sms * res_d) g = (int64_t)a.num_sms * res_d;
+                if (g < 1) g = 1;
+                if (src32)
+                    quantize_rows_nv_delayed_kernel<true><<<(unsigned)g, kRowThreads, 0, st>>>(
+                        s8, nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, nv);
+                else
+                    quantize_rows_nv_delayed_kernel<false><<<(unsigned)g, kRowThreads, 0, st>>>(
+                        s8, nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, nv);
+                e = cudaGetLastError();
+                break;
+            }
+            // just in time: the fused kernel, one CTA per SM, all resident at once
+            int64_t g = a.num_sms;
+            if (g > 2 * nblocks) g = 2 * nblocks;            // the partials fit in the code words
+            if (g < 1) g = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)g);
+            cfg.blockDim = dim3(kFusedThreads);
+            cfg.stream = st;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeCooperative;
+            at[0].val.cooperative = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            const DivU32 dv = make_div_u32((uint32_t)S);
+            const bool small = nblocks < (1ll << 32) - 64 * (int64_t)g;   // item indices stay in 32 bits
+            auto k = src32 ? (small ? quantize_rows_nv_fused_kernel<true, uint32_t>
+                                    : quantize_rows_nv_fused_kernel<true, int64_t>)
+                           : (small ? quantize_rows_nv_fused_kernel<false, uint32_t>
+                                    : quantize_rows_nv_fused_kernel<false, int64_t>);
+            e = cudaLaunchKernelEx(&cfg, k, s8, nblocks, (uint32_t)S, dv, (S + 3) / 4, a.row_codes, a.row_scales, slot,
+                                   a.status, a.timeout_ns);
             break;
         }
         }
@@ -874,12 +1331,9 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
         }
     }
     if (e != cudaSuccess) return e;
-    if (a.fmt == kNVFP4) {
+    if (a.fmt == kNVFP4 && a.history) {
         float* other = (a.axis == 3) ? a.col_ts : nullptr;
-        if (a.history)
-            nv_delayed_finalize_kernel<<<1, 1, 0, st>>>(a.history, a.hist_len, reinterpret_cast<float*>(amax), other);
-        else
-            nv_finalize_kernel<<<1, 1, 0, st>>>(reinterpret_cast<float*>(amax), other);
+        nv_delayed_finalize_kernel<<<1, 1, 0, st>>>(a.history, a.hist_len, reinterpret_cast<float*>(slot), other);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
