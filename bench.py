@@ -725,20 +725,36 @@ def main():
         dist.destroy_process_group()
 
 
+# sources the FP8 GEMM launch is built from; the profile that gives its DRAM
+# traffic names their hash, taken with comments and blank space removed
+KERNEL_SOURCES = ("gemm2.cu", "tcgen05.cuh", "epilogue.cuh", "common.cuh", "tmap.h")
+
+
+def kernel_source_hash() -> str:
+    """sha256[:16] of the GEMM sources with // and /* */ comments and all
+    white space removed (comment edits leave it unchanged)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        src = open(os.path.join(ROOT, "block_scaled_precision_03_gb300", "csrc", name)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(re.sub(r"\s+", "", src).encode())
+    return h.hexdigest()[:16]
+
+
 def _profile_traffic():
     """DRAM bytes per launch of the FP8 GEMM from the committed ncu summary,
-    only if that summary was taken on the current GEMM source."""
-    import hashlib
+    only if that summary was taken on the current GEMM sources."""
     try:
-        src = open(os.path.join(ROOT, "block_scaled_precision_03_gb300", "csrc", "gemm2.cu"), "rb").read()
-        sha = hashlib.sha256(src).hexdigest()[:16]
         vals = {}
         with open(os.path.join(ROOT, "profiles", "gemm2_fp8_fwd_8192x14336x4096.md")) as f:
             for line in f:
                 if ":" in line and line.startswith("- "):
                     k, v = line[2:].rsplit(":", 1)
                     vals[k.strip()] = v.strip().strip("`")
-        if vals.get("gemm2.cu sha256[:16]") != sha:
+        if vals.get("kernel source sha256[:16]") != kernel_source_hash():
             return None
         return float(vals["dram bytes per full launch"])
     except Exception:

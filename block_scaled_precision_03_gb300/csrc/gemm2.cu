@@ -1,4 +1,5 @@
-// Dense block-scaled GEMM on a CTA pair (tcgen05 cta_group::2), sm_103a.
+// Block-scaled GEMM on a CTA pair (tcgen05 cta_group::2), sm_103a: dense,
+// and grouped over experts; MXFP8 (E4M3 / E5M2), NVFP4 and MXFP4 operands.
 //
 // C[M,N] = A[M,K] * B[N,K]^T with per-block scales and FP32 accumulation
 // ("Practical FP4 Training for Large-Scale MoE Models on Hopper GPUs",
@@ -10,11 +11,13 @@
 // tile with M=256 MMAs issued by the even CTA.  Each CTA stages only its
 // own 128 rows of A and its own 128 rows of B per K step, so a CTA holds
 // 32 KB of operands per stage (a 1-CTA 128 x 256 tile needs 48 KB) and the
-// ring holds 3 stages of 256 K-bytes (5 of 128 for NVFP4).  The tcgen05
-// instruction queue is about one MMA deep, so the issuing thread runs in
-// lockstep with the tensor pipe; every barrier handshake costs pipe time,
-// and larger stages (8 MMAs per handshake) amortize it.  Each CTA also keeps the full 256-row B scale tile so
-// its tensor memory holds the scales its half of the MMA reads.
+// ring holds 3 stages of 256 K-bytes (MXFP4: 5 of 128, NVFP4: 4 of 128).
+// The tcgen05 instruction queue is about one MMA deep, so the issuing
+// thread runs in lockstep with the tensor pipe; every barrier handshake
+// costs pipe time, and larger stages (8 MMAs per handshake) amortize it.
+// Each CTA also keeps the full 256-row B scale tile so its tensor memory
+// holds the scales its half of the MMA reads (a pair's scale copy fills each
+// CTA's tensor memory from that CTA's own shared memory).
 //
 // Roles (both CTAs, 11 warps each):
 //   warp 0      TMA producer: own A / B halves and scale atoms; completion is
@@ -74,13 +77,19 @@ struct Cfg2 {
     // FP4 stages stay at 128 bytes: the scales of a 256-byte MXFP4 stage
     // (6 KB) would not leave room for three stages and the epilogue.
     static constexpr int KSUB = FP4 ? 1 : 2;
-    static constexpr int STAGES = FP4 ? 5 : 3;
+    // NVFP4 (one scale atom per MMA) takes B's scales four times over, laid
+    // out for one 128x256b copy per atom instead of two 32x128b.warpx4: 8
+    // scale copies per stage instead of 12, for 12 KB more scale bytes per
+    // stage and one stage less.  (The same for A's scales, or for MXFP4's B
+    // scales, costs more in loads and stages than it saves in copies.)
+    static constexpr bool SFB_QUARTERS = KIND == kKindNV;
+    static constexpr int STAGES = FP4 ? (SFB_QUARTERS ? 4 : 5) : 3;
     static constexpr int MPS = 4 * KSUB;                  // MMAs per stage
     static constexpr int OP_BYTES = KSUB * HALF;          // one CTA's A (or B) bytes per stage
     // 512-byte scale atoms (4 scale columns x 128 rows) per 128 rows per stage
     static constexpr int SF_ATOMS = KSUB * (KIND == kKindNV ? 4 : (KIND == kKindMX4 ? 2 : 1));
     static constexpr int SFA_BYTES = SF_ATOMS * 512;
-    static constexpr int SFB_BYTES = 2 * SF_ATOMS * 512;
+    static constexpr int SFB_BYTES = SFB_QUARTERS ? SF_ATOMS * 4096 : 2 * SF_ATOMS * 512;
     static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
     static constexpr uint32_t SFA_COLS = 4 * SF_ATOMS;    // TMEM columns: SFA atoms, then SFB atom pairs
     static constexpr uint32_t SF_COLS = 12 * SF_ATOMS;
@@ -200,10 +209,10 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     constexpr int S = CF::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* smA = base;
-    uint8_t* smB = base + S * CF::OP_BYTES;
-    uint8_t* smSF = smB + S * CF::OP_BYTES;
-    uint8_t* smOut = smSF + S * CF::SF_STAGE;             // epilogue staging, 2 KB per warp
+    uint8_t* smSF = base;                                 // scales first: stage sizes are 1 KB multiples
+    uint8_t* smA = base + S * CF::SF_STAGE;
+    uint8_t* smB = smA + S * CF::OP_BYTES;
+    uint8_t* smOut = smB + S * CF::OP_BYTES;              // epilogue staging, 2 KB per warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(smOut + kEpiWarps * 2048);
     GroupTable2* gt = reinterpret_cast<GroupTable2*>(bars + 32);
     // bars: full[S], empty[S], sfready[S], tfull, tempty, drain (MMAs), cdrain (scale copies)
@@ -316,7 +325,12 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                         tc::tma_load_2d_pair(tc::smem_u32(smB + stage * CF::OP_BYTES + j * HALF), &tmB, kx, brow, fb);
                     }
                     tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, ti.a_band, fb);
-                    tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS, ti.sfb_band, fb);
+                    if (CF::SFB_QUARTERS)
+                        tc::tma_load_4d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, 0, ti.sfb_band,
+                                             kb * CF::SF_ATOMS, fb);
+                    else
+                        tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS,
+                                             ti.sfb_band, fb);
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
@@ -440,7 +454,8 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         // Issued apart from the MMAs, the copies overlap with them.
         if (lane == 0 && leader) {
             constexpr int NCP = 3 * CF::SF_ATOMS;
-            const uint64_t sfd_base = tc::desc_sf(tc::smem_u32(smSF));
+            const uint32_t sf_smem = tc::smem_u32(smSF);
+            const uint64_t sfd_base = tc::desc_sf(sf_smem);
             constexpr uint32_t SF_STEP = CF::SF_STAGE >> 4;
             int stage = 0;
             uint32_t phase = 0;
@@ -454,14 +469,26 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     tc::fence_after();
                     const uint64_t sd = sfd_base + (uint64_t)(stage * SF_STEP);
                     const uint32_t sfa_t = sf_t0 + stage * CF::SF_COLS, sfb_t = sfa_t + CF::SFA_COLS;
-                    // copy c: atom c / 3, part c % 3 (A; B rows 0-127; B rows 128-255), each
-                    // one 512-byte 128x4 tile broadcast to the four lane quarters
+                    if (CF::SFB_QUARTERS) {
+                        // per atom: A's 512-byte 128x4 tile broadcast to the four lane
+                        // quarters, B's two tiles as one 128 x 32-byte matrix already
+                        // laid out four times over ([band][quarter][row][16 bytes])
+                        const uint32_t sfb_s = sf_smem + stage * CF::SF_STAGE + CF::SFA_BYTES;
 #pragma unroll
-                    for (int c = 0; c < NCP; c++) {
-                        const int a = c / 3, part = c % 3;
-                        if (part == 0) tc::cp_sf<2>(sfa_t + 4 * a, sd + 32 * a);
-                        else tc::cp_sf<2>(sfb_t + 8 * a + 4 * (part - 1),
-                                          sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + a) * 512) >> 4));
+                        for (int a = 0; a < CF::SF_ATOMS; a++) {
+                            tc::cp_sf<2>(sfa_t + 4 * a, sd + 32 * a);
+                            tc::cp_sf_128x256<2>(sfb_t + 8 * a, tc::desc_sf_ns(sfb_s + a * 4096, 2048, 128));
+                        }
+                    } else {
+                        // copy c: atom c / 3, part c % 3 (A; B rows 0-127; B rows 128-255), each
+                        // one 512-byte 128x4 tile broadcast to the four lane quarters
+#pragma unroll
+                        for (int c = 0; c < NCP; c++) {
+                            const int a = c / 3, part = c % 3;
+                            if (part == 0) tc::cp_sf<2>(sfa_t + 4 * a, sd + 32 * a);
+                            else tc::cp_sf<2>(sfb_t + 8 * a + 4 * (part - 1),
+                                              sd + ((CF::SFA_BYTES + ((part - 1) * CF::SF_ATOMS + a) * 512) >> 4));
+                        }
                     }
                     tc::commit<2>(sfr0 + 8 * stage, 1);
                     any = true;
@@ -583,7 +610,12 @@ cudaError_t run_gemm_pair(const GemmArgs& a, cudaStream_t st) {
     // the per-expert padded scale layout spans up to one extra 128-row tile per expert
     const int64_t a_bands = (a.M + 127) / 128 + (p.gsf ? a.num_groups : 0);
     if (!tmap::scales_3d(&tsa, a.a_scales, a_bands, n_atoms, sf_atoms, 1)) return cudaErrorInvalidValue;
-    if (!tmap::scales_3d(&tsb, b_sf, (b_rows + 127) / 128, n_atoms, sf_atoms, 2)) return cudaErrorInvalidValue;
+    if (kind == kKindNV) {
+        if (!tmap::scales_4d_quarters(&tsb, b_sf, (b_rows + 127) / 128, n_atoms, sf_atoms, 2))
+            return cudaErrorInvalidValue;
+    } else if (!tmap::scales_3d(&tsb, b_sf, (b_rows + 127) / 128, n_atoms, sf_atoms, 2)) {
+        return cudaErrorInvalidValue;
+    }
     // TMA stores of the output when its base and row pitch allow them
     CUtensorMap tcm = ta;
     p.tma_store = p.vec_ok && tmap::out_2d(&tcm, a.C, a.M, a.N, a.N, a.out_bf16 != 0);

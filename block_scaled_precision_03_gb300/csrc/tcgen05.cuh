@@ -130,6 +130,12 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
     asm volatile("cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
                  :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
 }
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                                 int32_t c3, uint32_t bar) {
+    asm volatile("cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
@@ -190,6 +196,15 @@ __device__ __forceinline__ void cp_sf(uint32_t taddr, uint64_t sdesc) {
     else
         asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
 }
+// 128 lanes x 256 bits (8 columns): lane r takes row r of a 128-row x
+// 32-byte matrix in shared memory (descriptor desc_sf_ns).
+template <int G>
+__device__ __forceinline__ void cp_sf_128x256(uint32_t taddr, uint64_t sdesc) {
+    if (G == 1)
+        asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" :: "r"(taddr), "l"(sdesc) : "memory");
+}
 // Block-scaled MMA kinds: FP8/FP6 operands with one UE8M0 scale per 32
 // K-values (mxf8f6f4, scale_vec::1X; the scale byte of the 32-bit TMEM word is
 // chosen by the descriptor's sf ids), NVFP4 with one UE4M3 scale per 16
@@ -249,6 +264,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 // 8-row core matrices 128 bytes apart.
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+// No-swizzle descriptor of a scale matrix whose core matrices (8 rows x 16
+// bytes, 128 contiguous bytes) lie `lbo` bytes apart along the columns (the
+// two 16-byte halves of a 32-byte row) and `sbo` bytes apart along the rows.
+__device__ __forceinline__ uint64_t desc_sf_ns(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
 }
 
 }  // namespace tc

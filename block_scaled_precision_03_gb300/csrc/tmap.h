@@ -53,6 +53,26 @@ inline bool scales_3d(CUtensorMap* m, const void* ptr, int64_t bands, int64_t at
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same tiled scale buffer read for a 128x256b scale copy: per atom
+// (4 scale columns of a 128-row band; one 16-element block each for NVFP4)
+// the box holds box_bands bands x 4 copies of the band's 512-byte tile, i.e.
+// for lane r = 32 q + l of the copy the 16-byte row l of each band's tile
+// (the scales of rows l, 32 + l, 64 + l, 96 + l of the band).  The copy
+// index q has stride 0: the four lane quarters each get the whole tile.
+// Box = 128 words x 4 copies x box_bands x box_atoms, atoms outermost.
+inline bool scales_4d_quarters(CUtensorMap* m, const void* ptr, int64_t bands, int64_t atoms, uint32_t box_atoms,
+                               uint32_t box_bands) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {128, 4, (cuuint64_t)bands, (cuuint64_t)atoms};
+    cuuint64_t strides[3] = {0, (cuuint64_t)(atoms * 512), 512};
+    cuuint32_t box[4] = {128u, 4u, box_bands, box_atoms};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row-major output matrix [rows, cols] of BF16 or FP32 for TMA stores: box =
 // 64 bytes x 32 rows, 64-byte swizzle; elements outside the matrix are not
 // written.  Needs a 16-byte aligned base and a row pitch that is a multiple
