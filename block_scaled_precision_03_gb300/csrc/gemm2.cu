@@ -93,7 +93,8 @@ struct Cfg2 {
     static constexpr int SF_STAGE = SFA_BYTES + SFB_BYTES;
     static constexpr uint32_t SFA_COLS = 4 * SF_ATOMS;    // TMEM columns: SFA atoms, then SFB atom pairs
     static constexpr uint32_t SF_COLS = 12 * SF_ATOMS;
-    static constexpr uint32_t CTA_TX = 2 * OP_BYTES + SF_STAGE;     // bytes one CTA loads per stage
+    static constexpr uint32_t OP_TX = 2 * OP_BYTES;       // operand bytes one CTA loads per stage
+    static constexpr uint32_t SF_TX = SF_STAGE;           // scale bytes one CTA loads per stage
     static constexpr int SMEM = 1024 + STAGES * (2 * OP_BYTES + SF_STAGE) + kEpiWarps * 2048 + 256 + kGroupTableBytes;
     static_assert(kSfCol0 + STAGES * SF_COLS <= kTmemCols, "TMEM columns");
     static_assert(SMEM <= 232448, "shared memory per block");
@@ -215,18 +216,21 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     uint8_t* smOut = smB + S * CF::OP_BYTES;              // epilogue staging, 2 KB per warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(smOut + kEpiWarps * 2048);
     GroupTable2* gt = reinterpret_cast<GroupTable2*>(bars + 32);
-    // bars: full[S], empty[S], sfready[S], tfull, tempty, drain (MMAs), cdrain (scale copies)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 4);
+    // bars: full[S] (operands), empty[S], sfready[S], sfull[S] (scales), sfree[S] (scales
+    // read into tensor memory), tfull, tempty, drain (MMAs), cdrain (scale copies)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 5 * S + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* issued_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);   // stage loads this CTA issued
-    static_assert(8 * (3 * S + 4) + 12 <= 256, "barrier area");
+    volatile int* issued_slot = reinterpret_cast<volatile int*>(tmem_slot + 2);   // operand loads this CTA issued
+    volatile int* sf_issued_slot = reinterpret_cast<volatile int*>(tmem_slot + 3);   // scale loads it issued
+    static_assert(8 * (5 * S + 4) + 16 <= 256, "barrier area");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = tc::cluster_rank();
     const bool leader = rank == 0;
     const uint32_t full0 = tc::smem_u32(bars), empty0 = tc::smem_u32(bars + S), sfr0 = tc::smem_u32(bars + 2 * S);
-    const uint32_t tfull = tc::smem_u32(bars + 3 * S), tempty = tc::smem_u32(bars + 3 * S + 1);
-    const uint32_t drain = tc::smem_u32(bars + 3 * S + 2), cdrain = tc::smem_u32(bars + 3 * S + 3);
+    const uint32_t sfull0 = tc::smem_u32(bars + 3 * S), sfree0 = tc::smem_u32(bars + 4 * S);
+    const uint32_t tfull = tc::smem_u32(bars + 5 * S), tempty = tc::smem_u32(bars + 5 * S + 1);
+    const uint32_t drain = tc::smem_u32(bars + 5 * S + 2), cdrain = tc::smem_u32(bars + 5 * S + 3);
     const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
     if (warp == 0 && lane == 0) {
@@ -234,6 +238,8 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             tc::mbar_init(full0 + 8 * s, 1);
             tc::mbar_init(empty0 + 8 * s, 1);
             tc::mbar_init(sfr0 + 8 * s, 1);
+            tc::mbar_init(sfull0 + 8 * s, 1);
+            tc::mbar_init(sfree0 + 8 * s, 1);
         }
         tc::mbar_init(tfull, 1);
         tc::mbar_init(tempty, 2 * kEpiWarps);
@@ -241,6 +247,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         tc::mbar_init(cdrain, 1);
         *abort_flag = 0;
         *issued_slot = 0;
+        *sf_issued_slot = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tc::prefetch_tmap(&tmA);
         tc::prefetch_tmap(&tmB);
@@ -300,9 +307,15 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     const uint32_t sf_t0 = tmem + kSfCol0;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer (both CTAs)
+        // ------------------------------------------------ TMA producers (both CTAs)
+        // Lane 0 loads the operands of a stage once the MMAs that read its
+        // previous contents completed (empty).  Lane 1 loads the stage's scales
+        // once the scale copies read their previous contents into tensor
+        // memory (sfree), which is up to a whole ring ahead of the operands, so
+        // the copies of a stage are done long before its MMAs are issued.
+        // Completion of both is signalled on the even CTA's barriers.
         if (lane == 0) {
-            const uint32_t full_c0 = tc::mapa(full0, 0);       // even CTA's stage barriers
+            const uint32_t full_c0 = tc::mapa(full0, 0);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -316,26 +329,47 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                         break;
                     }
                     const uint32_t fb = full_c0 + 8 * stage;
-                    if (leader) tc::mbar_expect_tx(full0 + 8 * stage, 2 * CF::CTA_TX);
-                    uint8_t* sf = smSF + stage * CF::SF_STAGE;
+                    if (leader) tc::mbar_expect_tx(full0 + 8 * stage, 2 * CF::OP_TX);
 #pragma unroll
                     for (int j = 0; j < CF::KSUB; j++) {
                         const int kx = (kb * CF::KSUB + j) * BKB;
                         tc::tma_load_2d_pair(tc::smem_u32(smA + stage * CF::OP_BYTES + j * HALF), &tmA, kx, arow, fb);
                         tc::tma_load_2d_pair(tc::smem_u32(smB + stage * CF::OP_BYTES + j * HALF), &tmB, kx, brow, fb);
                     }
-                    tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, ti.a_band, fb);
-                    if (CF::SFB_QUARTERS)
-                        tc::tma_load_4d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, 0, ti.sfb_band,
-                                             kb * CF::SF_ATOMS, fb);
-                    else
-                        tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS,
-                                             ti.sfb_band, fb);
                     ++issued;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
             }
             *issued_slot = issued;
+            if (!ok) *abort_flag = 1;
+        } else if (lane == 1) {
+            const uint32_t sfull_c0 = tc::mapa(sfull0, 0);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int gcur = 0, issued = 0;
+            for (int t = cid; t < total && ok; t += ncl) {
+                const Tile2 ti = tile2(p, t, gt, gcur, rank);
+                for (int kb = 0; kb < p.k_stages; kb++) {
+                    if (!tc::mbar_wait(sfree0 + 8 * stage, phase ^ 1, abort_flag, p.status, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sb = sfull_c0 + 8 * stage;
+                    if (leader) tc::mbar_expect_tx(sfull0 + 8 * stage, 2 * CF::SF_TX);
+                    uint8_t* sf = smSF + stage * CF::SF_STAGE;
+                    tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, ti.a_band, sb);
+                    if (CF::SFB_QUARTERS)
+                        tc::tma_load_4d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, 0, ti.sfb_band,
+                                             kb * CF::SF_ATOMS, sb);
+                    else
+                        tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS,
+                                             ti.sfb_band, sb);
+                    ++issued;
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            *sf_issued_slot = issued;
             if (!ok) *abort_flag = 1;
         }
     } else if (warp == 1) {
@@ -448,10 +482,11 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     } else {
         // ------------------------------------------------ scale copies (even CTA)
         // Copies each stage's scale atoms from shared memory into the stage's
-        // tensor-memory slot as soon as the stage has landed (a slot is free
-        // once its stage was loaded again: the producer reloads a stage only
-        // after the MMAs that read it completed), then commits sfready.
-        // Issued apart from the MMAs, the copies overlap with them.
+        // tensor-memory slot as soon as the stage's scales have landed (they
+        // load on their own barrier, ahead of the operands; a slot is free once
+        // its stage was loaded again: the producer reloads a stage only after
+        // the MMAs that read it completed), then commits sfready.  Issued apart
+        // from the MMAs, the copies overlap with them.
         if (lane == 0 && leader) {
             constexpr int NCP = 3 * CF::SF_ATOMS;
             const uint32_t sf_smem = tc::smem_u32(smSF);
@@ -462,7 +497,10 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             bool ok = true, any = false;
             for (int t = cid; t < total && ok; t += ncl) {
                 for (int kb = 0; kb < p.k_stages; kb++) {
-                    if (!tc::mbar_wait(full0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns)) {
+                    // the stage's scales have landed, and the MMAs that read the stage's
+                    // tensor-memory slot last time have completed
+                    if (!tc::mbar_wait(sfull0 + 8 * stage, phase, abort_flag, p.status, p.timeout_ns) ||
+                        !tc::mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag, p.status, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -491,6 +529,7 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                         }
                     }
                     tc::commit<2>(sfr0 + 8 * stage, 1);
+                    tc::commit<2>(sfree0 + 8 * stage, 3);         // both CTAs' scale slots are free again
                     any = true;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
@@ -517,7 +556,10 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         if (*abort_flag || peer_abort) {
             const int n_own = *issued_slot;
             const int n_peer = tc::ld_cluster_s32(tc::mapa(tc::smem_u32((const void*)issued_slot), 1));
-            drain_pair_loads(full0, S, n_own, n_peer, CF::CTA_TX);
+            const int sf_own = *sf_issued_slot;
+            const int sf_peer = tc::ld_cluster_s32(tc::mapa(tc::smem_u32((const void*)sf_issued_slot), 1));
+            drain_pair_loads(sfull0, S, sf_own, sf_peer, CF::SF_TX);
+            drain_pair_loads(full0, S, n_own, n_peer, CF::OP_TX);
         }
     }
     tc::cluster_sync();
