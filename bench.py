@@ -171,10 +171,10 @@ class Step:
             ("quant X e4m3 col", "a2", "quant", lambda: q(i["X"], "mxfp8_e4m3", "col", None, o["Xc"]), M * K * B_ROW8, 0, 1),
             ("gemm dgrad dX=dY W", "a4", "gemm8", lambda: bsq.gemm_into(o["dYr"], o["Wc"], o["dX"]), 0, 2 * M * K * N, 1),
             ("gemm wgrad dW=dY^T X", "a4", "gemm8", lambda: bsq.gemm_into(o["dYc"], o["Xc"], o["dW"]), 0, 2 * N * K * M, 1),
-            ("quant X nvfp4", "a3", "quant", lambda: q(i["X4"], "nvfp4", "row", o["X4q"], None), n["M"] * n["K"] * B_NV, 0, 1),
-            ("quant W nvfp4", "a3", "quant", lambda: q(i["W4"], "nvfp4", "row", o["W4q"], None), n["N"] * n["K"] * B_NV, 0, 1),
-            ("quant X' nvfp4", "a3", "quant", lambda: q(i["X42"], "nvfp4", "row", o["X42q"], None), n["M"] * n["K2"] * B_NV, 0, 1),
-            ("quant W' nvfp4", "a3", "quant", lambda: q(i["W42"], "nvfp4", "row", o["W42q"], None), n["N"] * n["K2"] * B_NV, 0, 1),
+            ("quant X nvfp4", "a3", "quant", lambda: q(i["X4"], "nvfp4", "row", o["X4q"], None), n["M"] * n["K"] * B_NV, 0, 2),
+            ("quant W nvfp4", "a3", "quant", lambda: q(i["W4"], "nvfp4", "row", o["W4q"], None), n["N"] * n["K"] * B_NV, 0, 2),
+            ("quant X' nvfp4", "a3", "quant", lambda: q(i["X42"], "nvfp4", "row", o["X42q"], None), n["M"] * n["K2"] * B_NV, 0, 2),
+            ("quant W' nvfp4", "a3", "quant", lambda: q(i["W42"], "nvfp4", "row", o["W42q"], None), n["N"] * n["K2"] * B_NV, 0, 2),
             ("gemm nvfp4 Y=XW^T", "a4", "gemm4", lambda: bsq.gemm_into(o["X4q"], o["W4q"], o["Y4"]), 0, 2 * n["M"] * n["N"] * n["K"], 1),
             ("gemm nvfp4 Y'=X'W'^T", "a4", "gemm4", lambda: bsq.gemm_into(o["X42q"], o["W42q"], o["Y42"]), 0, 2 * n["M"] * n["N"] * n["K2"], 1),
             ("quant A_moe mxfp4 row", "a1", "quant", lambda: q(i["A_moe"], "mxfp4", "row", o["A4"], None), mn * B_ROW4, 0, 1),

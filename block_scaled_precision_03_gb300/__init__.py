@@ -73,7 +73,6 @@ def lib():
         "bsq_mxfp4_to_fp8_1x128": (i32, [PT, vp, vp, vp]),
         "bsq_sync_status": (i32, [vp]),
         "bsq_debug_timeout_probe": (i32, [ctypes.c_uint64, vp]),
-        "bsq_debug_quantize_timeout": (i32, [vp, i64, i64, i32, i32, PT, PT, ctypes.c_uint64, vp]),
         "bsq_debug_gemm_timeout": (i32, [PT, PT, vp, i32, ctypes.c_uint64, i32, vp]),
         "bsq_status_string": (ctypes.c_char_p, [i32]),
         "bsq_version": (ctypes.c_char_p, []),
@@ -336,21 +335,6 @@ def sync_status(stream=None):
 
 def debug_timeout_probe(limit_ns: int, stream=None):
     _check(lib().bsq_debug_timeout_probe(limit_ns, _stream(stream)), "bsq_debug_timeout_probe")
-
-
-def debug_quantize_timeout_into(x, fmt, axis, out_row: QTensor | None, out_col: QTensor | None, timeout_ns: int,
-                                stream=None):
-    """quantize_into with the grid-wide wait of the NVFP4 row-wise kernel
-    limited to timeout_ns (test hook for the failure path; see
-    bsq_debug_quantize_timeout)."""
-    f, a = _fmt(fmt), AXES[axis] if isinstance(axis, str) else int(axis)
-    R, C = x.shape
-    cr = out_row.c() if out_row is not None else None
-    cc = out_col.c() if out_col is not None else None
-    st = lib().bsq_debug_quantize_timeout(ctypes.c_void_p(x.data_ptr()), R, C, f, a,
-                                          ctypes.byref(cr) if cr is not None else None,
-                                          ctypes.byref(cc) if cc is not None else None, timeout_ns, _stream(stream))
-    _check(st, "bsq_debug_quantize_timeout")
 
 
 def debug_gemm_timeout_into(A: QTensor, B: QTensor, C, timeout_ns: int, kernel: int = 0, stream=None):

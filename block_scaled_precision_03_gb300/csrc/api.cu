@@ -84,7 +84,7 @@ const uint64_t kDefaultTimeoutNs = 4000000000ull;   // 4 s per wait
 // `history` (NVFP4 only) selects delayed scaling.
 bsq_status quantize_common(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
                            bsq_tensor* out_row, bsq_tensor* out_col, float* history, int32_t hist_len,
-                           uint64_t timeout_ns, void* stream) {
+                           void* stream) {
     if (!src_bf16 || !valid_fmt(fmt) || axis < BSQ_ROWWISE || axis > BSQ_BOTH) return BSQ_ERR_INVALID_ARG;
     if (rows < 1 || cols < 1) return BSQ_ERR_INVALID_ARG;
     if (!al16(src_bf16) || (cols % 8) != 0) return BSQ_ERR_ALIGNMENT;
@@ -128,9 +128,6 @@ bsq_status quantize_common(const void* src_bf16, int64_t rows, int64_t cols, int
     a.num_sms = num_sms();
     a.history = history;
     a.hist_len = hist_len;
-    a.status = status_ptr();
-    a.timeout_ns = timeout_ns;
-    if (!a.status) return BSQ_ERR_CUDA;
     return from_cuda(bsq::run_quantize(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -152,7 +149,7 @@ size_t bsq_scales_bytes(int32_t fmt, int64_t rows, int64_t cols) {
 
 bsq_status bsq_quantize(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
                         bsq_tensor* out_row, bsq_tensor* out_col, void* stream) {
-    return quantize_common(src_bf16, rows, cols, fmt, axis, out_row, out_col, nullptr, 0, kDefaultTimeoutNs, stream);
+    return quantize_common(src_bf16, rows, cols, fmt, axis, out_row, out_col, nullptr, 0, stream);
 }
 
 bsq_status bsq_quantize_nvfp4_delayed(const void* src_bf16, int64_t rows, int64_t cols, int32_t axis,
@@ -162,7 +159,7 @@ bsq_status bsq_quantize_nvfp4_delayed(const void* src_bf16, int64_t rows, int64_
     if (reinterpret_cast<uintptr_t>(amax_history) & 3) return BSQ_ERR_ALIGNMENT;
     // same argument rules as bsq_quantize with NVFP4; the scale then comes from the history
     return quantize_common(src_bf16, rows, cols, BSQ_NVFP4_E2M1, axis, out_row, out_col, amax_history, history_len,
-                           kDefaultTimeoutNs, stream);
+                           stream);
 }
 
 bsq_status bsq_dequantize(const bsq_tensor* in, void* dst, int32_t dst_type, void* stream) {
@@ -234,12 +231,6 @@ static bsq_status gemm_common(const bsq_tensor* A, const bsq_tensor* B, void* C,
 
 bsq_status bsq_gemm(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type, void* stream) {
     return gemm_common(A, B, C, out_type, kDefaultTimeoutNs, false, stream);
-}
-
-bsq_status bsq_debug_quantize_timeout(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
-                                      bsq_tensor* out_row, bsq_tensor* out_col, uint64_t timeout_ns, void* stream) {
-    if (timeout_ns == 0 || timeout_ns > kDefaultTimeoutNs) return BSQ_ERR_INVALID_ARG;
-    return quantize_common(src_bf16, rows, cols, fmt, axis, out_row, out_col, nullptr, 0, timeout_ns, stream);
 }
 
 bsq_status bsq_debug_gemm_timeout(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type,

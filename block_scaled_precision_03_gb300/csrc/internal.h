@@ -16,8 +16,6 @@ struct QuantizeArgs {
     int num_sms;
     float* history;                // NVFP4 delayed scaling: amax history (nullptr: just in time)
     int hist_len;
-    unsigned* status;              // device status word (timeouts)
-    uint64_t timeout_ns;           // limit of any grid-wide wait
 };
 cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st);
 

@@ -15,10 +15,9 @@
 //
 // NVFP4 (FP8 page, section "MXFP8 e NVFP4 do Blackwell"): a tensor amax
 // pass, then per 16-block UE4M3 scales against the FP32 tensor scale
-// amax / (448 * 6), each step an IEEE FP32 operation.  Row-wise with
-// just-in-time scaling both run in one cooperative kernel with a grid-wide
-// barrier between them; column-wise and both run the amax pass, then the
-// tile kernel as its programmatic dependent.
+// amax / (448 * 6), each step an IEEE FP32 operation.  Just in time, the
+// amax pass runs first and the quantize kernel (row pass or tile kernel)
+// follows as its programmatic dependent.
 #include "common.cuh"
 #include "internal.h"
 
@@ -515,14 +514,13 @@ quantize_rows_wide_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint
 }
 
 // ---------------------------------------------------------------------------
-// NVFP4 row-wise kernel: a thread takes two consecutive 16-element blocks
-// per iteration (two 32-byte loads, or four 16-byte loads when the input is
-// only 16-byte aligned) and loads the next two before encoding these.  Each
-// block's scale work is done once, by its thread; d and -RN(1 / d) for the
+// NVFP4 row-wise encode: a lane takes two consecutive 16-element blocks per
+// item (two 32-byte loads, or four 16-byte loads when the input is only
+// 16-byte aligned) and loads the next two before encoding these.  Each
+// block's scale work is done once, by its lane; d and -RN(1 / d) for the
 // 126 finite scale codes come from a table each CTA builds once, and the
 // element quotients run two at a time on the packed FP32 pipe.
 // ---------------------------------------------------------------------------
-constexpr int kNvMinBlocks = 3;     // CTAs per SM the register budget must allow
 
 __device__ __forceinline__ uint4 ld_cached(const uint4* p) {
     uint4 r;
@@ -640,84 +638,6 @@ __device__ __forceinline__ uint32_t nv_quantize_block(const uint32_t* w, uint32_
         nv_encode_pairs(w, t, !sat && t.y != 0.0f, out);
     }
     return sb;
-}
-
-// The row-wise pass over all blocks, two per lane per iteration, starting
-// from the blocks already loaded into w.  Codes of blocks below `nres` are
-// left unwritten (the fused kernel writes them last).
-template <bool DELAYED, bool V8>
-__device__ __forceinline__ void nv_rows_pass(const uint8_t* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row,
-                                             int64_t s_tiles, uint8_t* __restrict__ codes,
-                                             uint8_t* __restrict__ scales, const NvT& nt, const float2* tab,
-                                             int64_t nres, uint32_t (&w)[16], uint32_t& acc) {
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kRowThreads) >> 5;
-    const bool vec_sf = (blocks_per_row & 3u) == 0;
-    const int64_t step = nwarps * 64;
-    int64_t base = warp * 64;
-    // row r and block column j of this lane's first block, advanced by
-    // `step` blocks per iteration without a division
-    uint32_t r = (uint32_t)((base + 2 * lane) / blocks_per_row);
-    uint32_t j = (uint32_t)(base + 2 * lane - (int64_t)r * blocks_per_row);
-    const uint32_t dq = (uint32_t)(step / blocks_per_row), dr = (uint32_t)(step % blocks_per_row);
-    for (; base < nblocks; base += step) {
-        uint32_t wn[16];
-        ld_nv_pair<V8>(src, base + step + 2 * lane, nblocks, wn);
-        const int64_t b = base + 2 * lane;
-        uint32_t sb[2], out[4];
-#pragma unroll
-        for (int u = 0; u < 2; u++) {
-            const uint32_t am = block_absmax(w + 8 * u);
-            if (DELAYED && b + u < nblocks) nv_acc_group(acc, am, w + 8 * u, 8);
-            sb[u] = nv_quantize_block(w + 8 * u, am, nt, tab, out + 2 * u);
-        }
-        if (b >= nres) {
-            if (b + 1 < nblocks)
-                *reinterpret_cast<uint4*>(codes + b * 8) = make_uint4(out[0], out[1], out[2], out[3]);
-            else if (b < nblocks)
-                *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(out[0], out[1]);
-        }
-        const uint32_t pair = sb[0] | (sb[1] << 8);
-        const uint32_t next = __shfl_down_sync(0xFFFFFFFFu, pair, 1);
-        if (vec_sf) {
-            // blocks b .. b + 3 share a row and one scale word
-            if ((lane & 1) == 0 && b < nblocks)
-                *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) = pair | (next << 16);
-        } else {
-            if (b < nblocks) scales[sf_offset(r, j, s_tiles)] = (uint8_t)sb[0];
-            if (b + 1 < nblocks) {
-                const bool wrap = j + 1 == blocks_per_row;
-                scales[sf_offset(wrap ? r + 1 : r, wrap ? 0 : j + 1, s_tiles)] = (uint8_t)sb[1];
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 16; k++) w[k] = wn[k];
-        j += dr;
-        r += dq;
-        if (j >= blocks_per_row) { j -= blocks_per_row; ++r; }
-    }
-}
-
-// Row-wise NVFP4 with delayed scaling: the tensor scale from the amax
-// history, this tensor's amax accumulated for the history update.
-template <bool V8>
-__global__ void __launch_bounds__(kRowThreads, kNvMinBlocks)
-quantize_rows_nv_delayed_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row,
-                                int64_t s_tiles, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                const NvScale nv) {
-    __shared__ float2 tab[128];
-    const int lane = threadIdx.x & 31;
-    const int64_t warp = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 5;
-    uint32_t w[16];
-    ld_nv_pair<V8>(src, warp * 64 + 2 * lane, nblocks, w);
-    const float s_t = nv_scale_of(nv);
-    const NvT nt = nv_tensor_consts(s_t);
-    if (threadIdx.x < 128) tab[threadIdx.x] = nv_scale_entry(threadIdx.x, s_t);
-    __syncthreads();
-    uint32_t acc = 0;
-    nv_rows_pass<true, V8>(src, nblocks, blocks_per_row, s_tiles, codes, scales, nt, tab, 0, w, acc);
-    nv_acc_flush(nv, acc);
 }
 
 // ---------------------------------------------------------------------------
@@ -948,46 +868,16 @@ amax_kernel(const uint32_t* __restrict__ src, int64_t nchunks, unsigned* __restr
 }
 
 // ---------------------------------------------------------------------------
-// Row-wise NVFP4 just in time in one cooperative launch, one CTA per SM: the
-// amax sweep, a grid-wide barrier, the row pass.  Each CTA owns a contiguous
-// share of the tensor in both phases; inside a CTA the warps take items of
-// that share from a shared-memory counter, so that warps the scheduler
-// favours do more of the work instead of idling the SM at the end.  The
-// sweep runs through each share from its end, the pass from its start, so
-// the pass first meets what the sweep read last (still in L2 wherever the
-// tensor does not fit whole).
-//
-// The barrier needs no memory beyond the outputs.  The tensor-scale slot
-// (zeroed before the launch) counts arrivals: each CTA stores its partial
-// amax in code word blockIdx.x, adds 1 and waits (bounded) until all G CTAs
-// have; then each reads the G partials and adds 1 again.  The CTA whose
-// second add returns 2G - 1 knows every CTA has read the partials: it writes
-// the codes of the first `nres` blocks (the words that held partials, which
-// the pass leaves alone) and finally stores s_t into the slot.  A wait that
-// runs out records a timeout in the status word and ends its CTA.
+// Row-wise NVFP4 pass: just in time as the programmatic dependent of the
+// amax pass (it waits before it reads the tensor scale), or with delayed
+// scaling.  One 768-thread CTA per SM owns a contiguous share of the blocks;
+// its warps take 64-block items (two blocks per lane) from a shared-memory
+// counter, so that warps the scheduler favours do more of the work instead
+// of idling the SM at the end (clock traces of a static split showed CTAs
+// on one SM finishing up to 10 us apart).
 // ---------------------------------------------------------------------------
-constexpr int kFusedThreads = 768;
-constexpr int kFusedWarps = kFusedThreads / 32;
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// max over the CTA (every thread gets it); `red` holds one word per warp
-template <int NWARPS>
-__device__ __forceinline__ uint32_t cta_max(uint32_t v, uint32_t* red) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    uint32_t m = 0;
-#pragma unroll
-    for (int k = 0; k < NWARPS; k++) m = max(m, red[k]);
-    return m;
-}
+constexpr int kNvPassThreads = 768;
+constexpr int kNvPassWarps = kNvPassThreads / 32;
 
 // the next item of this CTA's share for the calling warp (lane 0 takes it)
 __device__ __forceinline__ unsigned take_item(unsigned* counter) {
@@ -996,91 +886,31 @@ __device__ __forceinline__ unsigned take_item(unsigned* counter) {
     return __shfl_sync(0xFFFFFFFFu, v, 0);
 }
 
-template <bool V8, typename IDX>
-__global__ void __launch_bounds__(kFusedThreads, 1)
-quantize_rows_nv_fused_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row,
-                              DivU32 div_bpr, int64_t s_tiles, uint8_t* __restrict__ codes,
-                              uint8_t* __restrict__ scales, unsigned* __restrict__ slot,
-                              unsigned* __restrict__ status, uint64_t limit_ns) {
-    constexpr int NW = V8 ? 8 : 4;                  // words per amax chunk (32 or 16 bytes)
-    constexpr int kSweepItem = 32 * kAmaxUnroll;    // chunks per sweep item
+template <bool DELAYED, bool V8, typename IDX>
+__global__ void __launch_bounds__(kNvPassThreads, 1)
+quantize_rows_nv_pass_kernel(const uint8_t* __restrict__ src, int64_t nblocks, uint32_t blocks_per_row,
+                             DivU32 div_bpr, int64_t s_tiles, uint8_t* __restrict__ codes,
+                             uint8_t* __restrict__ scales, const NvScale nv) {
     __shared__ float2 tab[128];
-    __shared__ uint32_t red[kFusedWarps];
-    __shared__ uint32_t flag;
     __shared__ unsigned counter;
     const unsigned G = gridDim.x, cta = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) counter = kFusedWarps;            // warp w starts on item w
-    __syncthreads();
-
-    // ---- sweep: this CTA's share of the tensor amax, from the share's end
-    const int64_t nchunks = nblocks * (8 / NW);
-    const int64_t c0 = nchunks * cta / G, c1 = nchunks * (cta + 1) / G;
-    const int64_t n_sweep = (c1 - c0 + kSweepItem - 1) / kSweepItem;
-    const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
-    uint32_t am = 0;
-    for (int64_t it = warp; it < n_sweep;) {
-        uint32_t w[kAmaxUnroll][NW];
-#pragma unroll
-        for (int u = 0; u < kAmaxUnroll; u++) {
-            const int64_t k = it * kSweepItem + u * 32 + lane;
-            if (c0 + k < c1) {
-                ld_chunk<NW>(s32 + (c1 - 1 - k) * NW, w[u]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < NW; q++) w[u][q] = 0;
-            }
-        }
-        it = take_item(&counter);
-#pragma unroll
-        for (int u = 0; u < kAmaxUnroll; u++) amax_chunk<NW>(am, w[u]);
-    }
-    am = cta_max<kFusedWarps>(am, red);
-
-    // ---- barrier
-    uint32_t* cw = reinterpret_cast<uint32_t*>(codes);
-    if (tid == 0) {
-        cw[cta] = am;
-        __threadfence();
-        atomicAdd(slot, 1u);
-        uint32_t ok = 1;
-        const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_u32(slot) < G) {
-            if (globaltimer_ns() - t0 > limit_ns) {
-                record_status(status, kStatusTimeout);
-                ok = 0;
-                break;
-            }
-            __nanosleep(32);
-        }
-        flag = ok;
-        counter = kFusedWarps;
-    }
-    __syncthreads();
-    if (!flag) return;
-    uint32_t m = 0;
-    for (unsigned k = tid; k < G; k += kFusedThreads) m = max(m, __ldcg(cw + k));
-    m = cta_max<kFusedWarps>(m, red);
-    const float s_t = m ? __fdiv_rn(__uint_as_float(m << 16), 2688.0f) : 1.0f;
-    unsigned second = 0;                             // read at the end: who read the partials last
-    if (tid == 0) {
-        __threadfence();
-        second = atomicAdd(slot, 1u);
-    }
-    if (tid < 128) tab[tid] = nv_scale_entry(tid, s_t);
-    __syncthreads();
-
-    // ---- row pass over this CTA's share, in items of 64 blocks (two per lane);
-    // block indices in IDX (32 bits unless the tensor has 2^32 blocks or more)
-    const NvT nt = nv_tensor_consts(s_t);
+    if (tid == 0) counter = kNvPassWarps;           // warp w starts on item w
     const IDX nb = (IDX)nblocks;
-    const IDX nres = (IDX)min(nblocks, 2 * (((int64_t)G + 3) / 4));   // 8 nres bytes >= 4 G
-    const bool vec_sf = (blocks_per_row & 3u) == 0;
     const IDX n_items = (IDX)((nblocks + 63) / 64);
     const IDX i0 = (IDX)((int64_t)n_items * cta / G), i1 = (IDX)((int64_t)n_items * (cta + 1) / G);
     IDX it = i0 + warp;
     uint32_t w[16];
+    // the input is not written by the amax pass: its first load may precede the wait
     if (it < i1) ld_nv_pair<V8>(src, (int64_t)(it * 64 + 2 * lane), nblocks, w);
+    if (!DELAYED) pdl_wait();
+    const float s_t = nv_scale_of(nv);
+    if (!DELAYED && cta == 0 && tid == 0) nv_publish_scale(nv, s_t);
+    const NvT nt = nv_tensor_consts(s_t);
+    if (tid < 128) tab[tid] = nv_scale_entry(tid, s_t);
+    __syncthreads();
+    const bool vec_sf = (blocks_per_row & 3u) == 0;
+    uint32_t acc = 0;                 // delayed scaling: running amax of this tensor
     while (it < i1) {
         const IDX nx = i0 + take_item(&counter);
         uint32_t wn[16];
@@ -1088,14 +918,15 @@ quantize_rows_nv_fused_kernel(const uint8_t* __restrict__ src, int64_t nblocks, 
         const IDX b = it * 64 + 2 * lane;
         uint32_t sb[2], out[4];
 #pragma unroll
-        for (int u = 0; u < 2; u++) sb[u] = nv_quantize_block(w + 8 * u, block_absmax(w + 8 * u), nt, tab, out + 2 * u);
-        if (b >= nres) {
-            if (b + 1 < nb)
-                *reinterpret_cast<uint4*>(codes + (size_t)b * 8) = make_uint4(out[0], out[1], out[2], out[3]);
-            else if (b < nb)
-                *reinterpret_cast<uint2*>(codes + (size_t)b * 8) = make_uint2(out[0], out[1]);
+        for (int u = 0; u < 2; u++) {
+            const uint32_t am = block_absmax(w + 8 * u);
+            if (DELAYED && b + u < nb) nv_acc_group(acc, am, w + 8 * u, 8);
+            sb[u] = nv_quantize_block(w + 8 * u, am, nt, tab, out + 2 * u);
         }
-        // row and block column of block b
+        if (b + 1 < nb)
+            *reinterpret_cast<uint4*>(codes + (size_t)b * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+        else if (b < nb)
+            *reinterpret_cast<uint2*>(codes + (size_t)b * 8) = make_uint2(out[0], out[1]);
         uint32_t r, j;
         if (sizeof(IDX) == 4) {
             r = div_u32((uint32_t)b, div_bpr);
@@ -1107,7 +938,6 @@ quantize_rows_nv_fused_kernel(const uint8_t* __restrict__ src, int64_t nblocks, 
         const uint32_t pair = sb[0] | (sb[1] << 8);
         const uint32_t next = __shfl_down_sync(0xFFFFFFFFu, pair, 1);
         if (vec_sf) {
-            // blocks b .. b + 3 share a row and one scale word
             if ((lane & 1) == 0 && b < nb)
                 *reinterpret_cast<uint32_t*>(scales + sf_offset(r, j, s_tiles)) = pair | (next << 16);
         } else {
@@ -1121,22 +951,7 @@ quantize_rows_nv_fused_kernel(const uint8_t* __restrict__ src, int64_t nblocks, 
         for (int k = 0; k < 16; k++) w[k] = wn[k];
         it = nx;
     }
-
-    // ---- the CTA that read the partials last writes what they covered
-    if (tid == 0) flag = second == 2 * G - 1;
-    __syncthreads();
-    if (flag) {
-        __threadfence();
-        for (int64_t b = 2 * tid; b < (int64_t)nres; b += 2 * kFusedThreads) {
-            uint32_t v[16], out[4];
-            ld_nv_pair<V8>(src, b, (int64_t)nres, v);
-            nv_quantize_block(v, block_absmax(v), nt, tab, out);
-            nv_quantize_block(v + 8, block_absmax(v + 8), nt, tab, out + 2);
-            *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(out[0], out[1]);
-            if (b + 1 < (int64_t)nres) *reinterpret_cast<uint2*>(codes + b * 8 + 8) = make_uint2(out[2], out[3]);
-        }
-        if (tid == 0) *slot = __float_as_uint(s_t);
-    }
+    if (DELAYED) nv_acc_flush(nv, acc);
 }
 
 // Delayed scaling, after the quantize pass: the outputs get the tensor scale
@@ -1256,7 +1071,7 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
         nv.history = a.history;
         nv.hist_len = a.hist_len;
         nv.amax_acc = slot;
-    } else if (a.fmt == kNVFP4 && a.axis != 1) {
+    } else if (a.fmt == kNVFP4) {
         nv.ts_bits = slot;
         nv.ts_other = a.axis == 3 ? a.col_ts : nullptr;
         // persistent grid, as many CTAs as fit on the SMs at once
@@ -1283,42 +1098,24 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
             const int64_t nblocks = R * C / 16;
             const int64_t S = C / 16;
             const uint8_t* s8 = reinterpret_cast<const uint8_t*>(a.src);
-            if (nv.history) {
-                // delayed: persistent grid, as many CTAs as fit on the SMs at once
-                static const int res_d = resident_ctas(quantize_rows_nv_delayed_kernel<true>, 1);
-                int64_t g = (nblocks + 2 * kRowThreads - 1) / (2 * kRowThreads);
-                if (g > (int64_t)a.num_sms * res_d) g = (int64_t)a.num_sms * res_d;
-                if (g < 1) g = 1;
-                if (src32)
-                    quantize_rows_nv_delayed_kernel<true><<<(unsigned)g, kRowThreads, 0, st>>>(
-                        s8, nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, nv);
-                else
-                    quantize_rows_nv_delayed_kernel<false><<<(unsigned)g, kRowThreads, 0, st>>>(
-                        s8, nblocks, (uint32_t)S, (S + 3) / 4, a.row_codes, a.row_scales, nv);
-                e = cudaGetLastError();
-                break;
-            }
-            // just in time: the fused kernel, one CTA per SM, all resident at once
-            int64_t g = a.num_sms;
-            if (g > 2 * nblocks) g = 2 * nblocks;            // the partials fit in the code words
-            if (g < 1) g = 1;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)g);
-            cfg.blockDim = dim3(kFusedThreads);
-            cfg.stream = st;
-            cudaLaunchAttribute at[1];
-            at[0].id = cudaLaunchAttributeCooperative;
-            at[0].val.cooperative = 1;
-            cfg.attrs = at;
-            cfg.numAttrs = 1;
             const DivU32 dv = make_div_u32((uint32_t)S);
-            const bool small = nblocks < (1ll << 32) - 64 * (int64_t)g;   // item indices stay in 32 bits
-            auto k = src32 ? (small ? quantize_rows_nv_fused_kernel<true, uint32_t>
-                                    : quantize_rows_nv_fused_kernel<true, int64_t>)
-                           : (small ? quantize_rows_nv_fused_kernel<false, uint32_t>
-                                    : quantize_rows_nv_fused_kernel<false, int64_t>);
-            e = cudaLaunchKernelEx(&cfg, k, s8, nblocks, (uint32_t)S, dv, (S + 3) / 4, a.row_codes, a.row_scales, slot,
-                                   a.status, a.timeout_ns);
+            const bool small = nblocks < (1ll << 32) - 64 * (int64_t)a.num_sms;   // item indices stay in 32 bits
+            // one CTA per SM; just in time as the programmatic dependent of the amax pass
+            int64_t g = a.num_sms;
+            const int64_t items = (nblocks + 63) / 64;
+            if (g > items) g = items;
+            if (g < 1) g = 1;
+            const bool jit = !nv.history;
+            auto k = jit ? (src32 ? (small ? quantize_rows_nv_pass_kernel<false, true, uint32_t>
+                                           : quantize_rows_nv_pass_kernel<false, true, int64_t>)
+                                  : (small ? quantize_rows_nv_pass_kernel<false, false, uint32_t>
+                                           : quantize_rows_nv_pass_kernel<false, false, int64_t>))
+                         : (src32 ? (small ? quantize_rows_nv_pass_kernel<true, true, uint32_t>
+                                           : quantize_rows_nv_pass_kernel<true, true, int64_t>)
+                                  : (small ? quantize_rows_nv_pass_kernel<true, false, uint32_t>
+                                           : quantize_rows_nv_pass_kernel<true, false, int64_t>));
+            e = launch_k(jit, k, dim3((unsigned)g), kNvPassThreads, st, s8, nblocks, (uint32_t)S, dv, (S + 3) / 4,
+                         a.row_codes, a.row_scales, nv);
             break;
         }
         }

@@ -281,17 +281,6 @@ bsq_status bsq_debug_timeout_probe(uint64_t limit_ns, void* stream);
 bsq_status bsq_debug_gemm_timeout(const bsq_tensor* A, const bsq_tensor* B, void* C, int32_t out_type,
                                   uint64_t timeout_ns, int32_t kernel, void* stream);
 
-/* Test hook for the failure path of the grid-wide wait in the NVFP4
- * row-wise quantize (just-in-time scaling runs the tensor-amax sweep and the
- * quantize pass in one cooperative launch with one barrier between them):
- * bsq_quantize with that wait limited to `timeout_ns` nanoseconds (1 ..
- * 4e9; bsq_quantize uses 4e9).  A CTA whose wait runs out records
- * BSQ_ERR_TIMEOUT in the status word and ends; the outputs are then partly
- * written.  Other formats and axes have no grid-wide wait and ignore the
- * limit.  Argument rules and errors as for bsq_quantize. */
-bsq_status bsq_debug_quantize_timeout(const void* src_bf16, int64_t rows, int64_t cols, int32_t fmt, int32_t axis,
-                                      bsq_tensor* out_row, bsq_tensor* out_col, uint64_t timeout_ns, void* stream);
-
 /* Static description of a status code. */
 const char* bsq_status_string(int32_t status);
 

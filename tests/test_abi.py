@@ -154,13 +154,6 @@ def test_host_argument_checks_launch_nothing(lib):
     assert lib.bsq_debug_gemm_timeout(ctypes.byref(a), ctypes.byref(b2), C, 0, 1000, 0, null) == 1
     m4 = T(2, 0, 128, 256, 256, 256, None)
     assert lib.bsq_debug_gemm_timeout(ctypes.byref(m4), ctypes.byref(m4), C, 0, 1000, 1, null) == 2
-    # quantize wait-limit hook: the limit first, then the rules of bsq_quantize
-    n4 = T(3, 0, 128, 256, 256, 256, 512)
-    src = ctypes.c_void_p(1 << 16)
-    assert lib.bsq_debug_quantize_timeout(src, 128, 256, 3, 1, ctypes.byref(n4), None, 0, null) == 1
-    assert lib.bsq_debug_quantize_timeout(src, 128, 256, 3, 1, ctypes.byref(n4), None, 4_000_000_001, null) == 1
-    assert lib.bsq_debug_quantize_timeout(src, 128, 255, 3, 1, ctypes.byref(n4), None, 1000, null) == 3
-    assert lib.bsq_debug_quantize_timeout(src, 128, 256, 3, 1, None, None, 1000, null) == 1
 
 
 def test_binding_rejects_bad_group_offsets():

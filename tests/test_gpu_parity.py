@@ -413,28 +413,6 @@ def test_gemm_wait_limit_runs_out_then_recovers(bsq, fmt, kernel, limit_ns):
     assert ok.all(), f"{(~ok).sum()} outputs outside the bound after the timed-out GEMM"
 
 
-def test_nvfp4_quantize_wait_limit_runs_out_then_recovers(bsq):
-    """The NVFP4 row-wise quantize waits once, grid-wide, between its amax
-    sweep and its quantize pass.  With that wait limited to 1 ns the CTAs
-    that arrive before the last one give up: BSQ_ERR_TIMEOUT is reported,
-    and the next quantize of the same tensor into the same outputs is
-    exact.  The wait runs out; nothing faults."""
-    # a large tensor: the first CTAs reach the barrier microseconds before the last
-    R, C = 8192, 14336
-    x = inputs.normal_bf16((R, C), 41)
-    xd = dev_bf16(x)
-    row = poisoned_qtensor(bsq, "nvfp4", R, C)
-    bsq.sync_status()
-    bsq.debug_quantize_timeout_into(xd, "nvfp4", "row", row, None, 1)
-    with pytest.raises(bsq.BsqError) as ei:
-        bsq.sync_status()
-    assert ei.value.status == 5
-    bsq.sync_status()                            # taken and cleared
-    bsq.debug_quantize_timeout_into(xd, "nvfp4", "row", row, None, 4_000_000_000)
-    bsq.sync_status()
-    assert_qtensor_equal(row, expected(x, "nvfp4", "row")["row"], "after the timed-out quantize")
-
-
 @pytest.mark.parametrize("fmt", ["mxfp8_e4m3", "mxfp8_e5m2", "mxfp4", "nvfp4"])
 @pytest.mark.parametrize("src_off,codes_off", [(16, 0), (0, 16), (16, 16)])
 def test_row_quantize_16_byte_aligned_buffers(bsq, fmt, src_off, codes_off):
