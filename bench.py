@@ -283,11 +283,13 @@ class Step:
     # e2e op order: the host link bounds the pass (3.2 GB up), so the inputs
     # go up largest-consumer first and the step ends soon after the last one
     # lands: the MoE part (2.35 GB of inputs) first, the 33.5 MB NVFP4 weight
-    # and its GEMM last.  Each op still waits only for its own inputs.
+    # and its GEMM last, the other NVFP4 GEMM just before, so that its output
+    # goes down while the last two inputs come up.  Each op still waits only
+    # for its own inputs.
     E2E_ORDER = ("quant A_moe mxfp4 row", "repack mxfp4->mxfp8", "quant W_moe e4m3 row", "grouped gemm moe",
                  "quant X e4m3 row", "quant W e4m3 row", "gemm fwd Y=XW^T", "quant dY e5m2 both",
                  "quant W e4m3 col", "quant X e4m3 col", "gemm dgrad dX=dY W", "gemm wgrad dW=dY^T X",
-                 "quant X nvfp4", "quant X' nvfp4", "quant W' nvfp4", "gemm nvfp4 Y'=X'W'^T",
+                 "quant X' nvfp4", "quant W' nvfp4", "gemm nvfp4 Y'=X'W'^T", "quant X nvfp4",
                  "quant W nvfp4", "gemm nvfp4 Y=XW^T")
 
     def setup_e2e(self):
