@@ -5,9 +5,11 @@ One step is one pass of the whole hot path over one synthetic batch, with
 every input resident in HBM when the timed region starts:
 
   forward  (Llama-3-8B MLP up-projection, MXFP8 E4M3)
-      quantize X[8192,4096] row, W[14336,4096] row; Y = X W^T (BF16 out)
+      quantize X[8192,4096] and W[14336,4096] both ways in one read each
+      (rows for the forward, columns kept for the backward); Y = X W^T
+      (BF16 out)
   backward (MXFP8, gradients E5M2)
-      quantize dY[8192,14336] both (row + column), W column, X column;
+      quantize dY[8192,14336] both (row + column);
       dX = dY W (8192x4096, K=14336); dW = dY^T X (14336x4096, K=8192)
   NVFP4 forward
       quantize X[8192,4096], W[4096,4096], X'[8192,14336], W'[4096,14336]
@@ -132,12 +134,12 @@ class Step:
         if "fwd" in want or "bwd" in want:
             o["Xq"] = E("mxfp8_e4m3", M, K)
             o["Wq"] = E("mxfp8_e4m3", N, K)
+            o["Wc"] = E("mxfp8_e4m3", K, N)
+            o["Xc"] = E("mxfp8_e4m3", K, M)
             o["Y"] = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         if "bwd" in want:
             o["dYr"] = E("mxfp8_e5m2", M, N)
             o["dYc"] = E("mxfp8_e5m2", N, M)
-            o["Wc"] = E("mxfp8_e4m3", K, N)
-            o["Xc"] = E("mxfp8_e4m3", K, M)
             o["dX"] = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
             o["dW"] = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
         if "nv" in want:
@@ -162,13 +164,13 @@ class Step:
         B_ROW8, B_ROW4, B_BOTH, B_NV, B_REPACK = 2 + 1 + 1 / 32, 2 + 0.5 + 1 / 32, 2 + 2 * (1 + 1 / 32), \
             2 + 2 + 0.5 + 1 / 16, 0.5 + 1 / 32 + 1 + 1 / 32
         mn = m["rows"] * m["K"]
+        # X and W are quantized once, both ways: the rows feed the forward GEMM,
+        # the columns (the transposed operands) the dgrad and wgrad GEMMs
         ops = [
-            ("quant X e4m3 row", "a1", "quant", lambda: q(i["X"], "mxfp8_e4m3", "row", o["Xq"], None), M * K * B_ROW8, 0, 1),
-            ("quant W e4m3 row", "a1", "quant", lambda: q(i["W"], "mxfp8_e4m3", "row", o["Wq"], None), N * K * B_ROW8, 0, 1),
+            ("quant X e4m3 both", "a2", "quant", lambda: q(i["X"], "mxfp8_e4m3", "both", o["Xq"], o["Xc"]), M * K * B_BOTH, 0, 1),
+            ("quant W e4m3 both", "a2", "quant", lambda: q(i["W"], "mxfp8_e4m3", "both", o["Wq"], o["Wc"]), N * K * B_BOTH, 0, 1),
             ("gemm fwd Y=XW^T", "a4", "gemm8", lambda: bsq.gemm_into(o["Xq"], o["Wq"], o["Y"]), 0, 2 * M * N * K, 1),
             ("quant dY e5m2 both", "a2", "quant", lambda: q(i["dY"], "mxfp8_e5m2", "both", o["dYr"], o["dYc"]), M * N * B_BOTH, 0, 1),
-            ("quant W e4m3 col", "a2", "quant", lambda: q(i["W"], "mxfp8_e4m3", "col", None, o["Wc"]), N * K * B_ROW8, 0, 1),
-            ("quant X e4m3 col", "a2", "quant", lambda: q(i["X"], "mxfp8_e4m3", "col", None, o["Xc"]), M * K * B_ROW8, 0, 1),
             ("gemm dgrad dX=dY W", "a4", "gemm8", lambda: bsq.gemm_into(o["dYr"], o["Wc"], o["dX"]), 0, 2 * M * K * N, 1),
             ("gemm wgrad dW=dY^T X", "a4", "gemm8", lambda: bsq.gemm_into(o["dYc"], o["Xc"], o["dW"]), 0, 2 * N * K * M, 1),
             ("quant X nvfp4", "a3", "quant", lambda: q(i["X4"], "nvfp4", "row", o["X4q"], None), n["M"] * n["K"] * B_NV, 0, 2),
@@ -186,7 +188,7 @@ class Step:
                                                                                padded_scales=True),
              0, 2 * m["rows"] * m["N"] * m["K"], 1),
         ]
-        part_of = ["fwd"] * 3 + ["bwd"] * 5 + ["nv"] * 6 + ["moe"] * 4
+        part_of = ["fwd"] * 3 + ["bwd"] * 3 + ["nv"] * 6 + ["moe"] * 4
         if part == "bwd":
             want = ("fwd", "bwd")      # the backward quantizes from the forward inputs
         ops = [op for op, pt in zip(ops, part_of) if pt in want]
@@ -197,6 +199,14 @@ class Step:
         # the tensor's own amax as in steady state.
         self.extra_ops = []
         if "fwd" in want:
+            # the same quantizes one layout at a time (rows a1 and a2 on X and W;
+            # the outputs are the step's own, rewritten with the same bytes)
+            self.extra_ops += [
+                ("quant X e4m3 row", "a1", "quant", lambda: q(i["X"], "mxfp8_e4m3", "row", o["Xq"], None), M * K * B_ROW8, 0, 1),
+                ("quant W e4m3 row", "a1", "quant", lambda: q(i["W"], "mxfp8_e4m3", "row", o["Wq"], None), N * K * B_ROW8, 0, 1),
+                ("quant X e4m3 col", "a2", "quant", lambda: q(i["X"], "mxfp8_e4m3", "col", None, o["Xc"]), M * K * B_ROW8, 0, 1),
+                ("quant W e4m3 col", "a2", "quant", lambda: q(i["W"], "mxfp8_e4m3", "col", None, o["Wc"]), N * K * B_ROW8, 0, 1),
+            ]
             # NEXT-4, dense: the forward GEMM on MXFP4 x MXFP4 operands
             # (quantized once here; the timed op is the GEMM alone)
             o["Xq4"] = E("mxfp4", M, K)
@@ -272,8 +282,8 @@ class Step:
     # the copies are pipelined: inputs go up on one copy stream in the order
     # the ops need them, each op waits only for its own inputs, and each
     # output goes down on a second copy stream as soon as its GEMM finished.
-    NEEDS = {"quant X e4m3 row": ("X",), "quant W e4m3 row": ("W",), "quant dY e5m2 both": ("dY",),
-             "quant W e4m3 col": ("W",), "quant X e4m3 col": ("X",), "quant X nvfp4": ("X4",),
+    NEEDS = {"quant X e4m3 both": ("X",), "quant W e4m3 both": ("W",), "quant dY e5m2 both": ("dY",),
+             "quant X nvfp4": ("X4",),
              "quant W nvfp4": ("W4",), "quant X' nvfp4": ("X42",), "quant W' nvfp4": ("W42",),
              "quant A_moe mxfp4 row": ("A_moe",), "quant W_moe e4m3 row": ("W_moe",),
              "repack mxfp4->mxfp8": ("offsets",), "grouped gemm moe": ("offsets",)}
@@ -287,8 +297,8 @@ class Step:
     # goes down while the last two inputs come up.  Each op still waits only
     # for its own inputs.
     E2E_ORDER = ("quant A_moe mxfp4 row", "repack mxfp4->mxfp8", "quant W_moe e4m3 row", "grouped gemm moe",
-                 "quant X e4m3 row", "quant W e4m3 row", "gemm fwd Y=XW^T", "quant dY e5m2 both",
-                 "quant W e4m3 col", "quant X e4m3 col", "gemm dgrad dX=dY W", "gemm wgrad dW=dY^T X",
+                 "quant X e4m3 both", "quant W e4m3 both", "gemm fwd Y=XW^T", "quant dY e5m2 both",
+                 "gemm dgrad dX=dY W", "gemm wgrad dW=dY^T X",
                  "quant X' nvfp4", "quant W' nvfp4", "gemm nvfp4 Y'=X'W'^T", "quant X nvfp4",
                  "quant W nvfp4", "gemm nvfp4 Y=XW^T")
 
