@@ -49,6 +49,26 @@ __device__ __forceinline__ uint32_t div_u32(uint32_t n, DivU32 q) {
 // Block encoders working on registers.
 // ---------------------------------------------------------------------------
 
+// Packed FP32 pairs (Blackwell f32x2 arithmetic, each half IEEE RN).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // MX: encode n values (n multiple of 8) given the block's scale byte.
 // FP8 output: n bytes; FP4 output: n/2 bytes.  Writes to `out` words.
 template <int FMT, int N>
@@ -59,10 +79,12 @@ __device__ __forceinline__ void mx_encode(const float* x, uint32_t sbyte, uint32
         for (int i = 0; i < (is_fp4(FMT) ? N / 8 : N / 4); i++) out[i] = is_fp4(FMT) ? 0u : 0x7F7F7F7Fu;
         return;
     }
+    // times 2^-e, two values per packed multiply (exact: a power of two)
     const float inv = mx_inv_scale(sbyte);
+    const uint64_t inv2 = f2(inv, inv);
     float v[N];
 #pragma unroll
-    for (int i = 0; i < N; i++) v[i] = x[i] * inv;
+    for (int i = 0; i < N; i += 2) f2split(mul2(f2(x[i], x[i + 1]), inv2), v[i], v[i + 1]);
     if (is_fp4(FMT)) {
 #pragma unroll
         for (int i = 0; i < N / 8; i++) out[i] = pack8_fp4(v + 8 * i);
@@ -550,26 +572,6 @@ __device__ __forceinline__ void ld_nv_pair(const uint8_t* src, int64_t b, int64_
     }
 }
 
-// Packed FP32 pairs (Blackwell f32x2 arithmetic, each half IEEE RN).
-__device__ __forceinline__ uint64_t f2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2split(uint64_t v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
 // -(x / d), correctly rounded, for both halves of x: div_from_rcp run with
 // -r in place of r.  Round to nearest is odd-symmetric, so every step yields
 // the exact negation of the corresponding div_from_rcp step, signed zeros
@@ -656,6 +658,7 @@ constexpr int kTile = 128;
 constexpr int kTileThreads = 256;
 
 __device__ __forceinline__ uint32_t vmax4(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+
 
 template <int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kTileThreads)
