@@ -294,10 +294,12 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
 // largest |x| bit pattern of 8 bf16 values (packed 16-bit max on the
 // sign-cleared halves; for non-negative finite values and NaN/Inf the
 // integer order is the order the block scale needs)
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b);
+// largest |x| bit pattern of 8 BF16 values; NaN anywhere gives a NaN
+// pattern (above 0x7F80), like an Inf
 __device__ __forceinline__ uint32_t absmax8(const uint4& w) {
-    const uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
-                                __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-    return max(m & 0xFFFFu, m >> 16);
+    const uint32_t m = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+    return bmax2(m, __byte_perm(m, 0, 0x1032)) & 0x7FFFu;
 }
 
 // ---------------------------------------------------------------------------
@@ -657,8 +659,6 @@ __device__ __forceinline__ uint32_t nv_quantize_block(const uint32_t* w, uint32_
 constexpr int kTile = 128;
 constexpr int kTileThreads = 256;
 
-__device__ __forceinline__ uint32_t vmax4(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
-
 
 template <int FMT, bool ROW, bool COL>
 __global__ void __launch_bounds__(kTileThreads)
@@ -694,19 +694,20 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
     }
 
     if (COL) {
-        // column maxima of the 8 rows (packed |bf16| pairs), then across the block's lanes
-        uint32_t cm[4] = {0, 0, 0, 0};
+        // column maxima of the 8 rows (packed |bf16| pairs, NaN-propagating,
+        // the sign bits masked off at the end), then across the block's lanes
+        uint32_t cm[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            cm[0] = vmax4(cm[0], w[i].x & 0x7FFF7FFFu);
-            cm[1] = vmax4(cm[1], w[i].y & 0x7FFF7FFFu);
-            cm[2] = vmax4(cm[2], w[i].z & 0x7FFF7FFFu);
-            cm[3] = vmax4(cm[3], w[i].w & 0x7FFF7FFFu);
+        for (int i = 1; i < 8; i++) {
+            cm[0] = bmax2(cm[0], w[i].x);
+            cm[1] = bmax2(cm[1], w[i].y);
+            cm[2] = bmax2(cm[2], w[i].z);
+            cm[3] = bmax2(cm[3], w[i].w);
         }
         if (FMT == kNVFP4 && nv.amax_acc) {
             // delayed scaling: this tensor's finite amax (zero padding adds nothing)
             uint32_t acc = 0;
-            const uint32_t m = vmax4(vmax4(cm[0], cm[1]), vmax4(cm[2], cm[3]));
+            const uint32_t m = bmax2(bmax2(cm[0], cm[1]), bmax2(cm[2], cm[3])) & 0x7FFF7FFFu;
             if (((m & 0xFFFFu) >= 0x7F80u) || ((m >> 16) >= 0x7F80u)) {
 #pragma unroll
                 for (int i = 0; i < 8; i++) {
@@ -720,8 +721,9 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
         }
 #pragma unroll
         for (int k = 0; k < 4; k++) {
-            cm[k] = vmax4(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 1));
-            if (LB == 4) cm[k] = vmax4(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 2));
+            cm[k] = bmax2(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 1));
+            if (LB == 4) cm[k] = bmax2(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 2));
+            cm[k] &= 0x7FFF7FFFu;
         }
 #pragma unroll
         for (int j = 0; j < 8; j++) {
