@@ -686,8 +686,10 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
                                   : make_uint4(0, 0, 0, 0);
     NvT nt{1.0f, 1.0f, true};
     if (FMT == kNVFP4) {
-        // just in time, the tensor scale comes from the amax pass this grid may overlap
+        // just in time, the tensor scale comes from the amax pass this grid may
+        // overlap; delayed, the history update after this grid may be scheduled now
         if (!nv.history) pdl_wait();
+        else pdl_launch_dependents();
         const float s_t = nv_scale_of(nv);
         if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) nv_publish_scale(nv, s_t);
         nt = nv_tensor_consts(s_t);
@@ -900,6 +902,7 @@ quantize_rows_nv_pass_kernel(const uint8_t* __restrict__ src, int64_t nblocks, u
     __shared__ unsigned counter;
     const unsigned G = gridDim.x, cta = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (DELAYED) pdl_launch_dependents();       // the history update may be scheduled now
     if (tid == 0) counter = kNvPassWarps;           // warp w starts on item w
     const IDX nb = (IDX)nblocks;
     const IDX n_items = (IDX)((nblocks + 63) / 64);
@@ -961,8 +964,11 @@ quantize_rows_nv_pass_kernel(const uint8_t* __restrict__ src, int64_t nblocks, u
 
 // Delayed scaling, after the quantize pass: the outputs get the tensor scale
 // the pass used (from the history as it stood), and the history takes this
-// tensor's amax at the front, dropping its oldest entry.
+// tensor's amax at the front, dropping its oldest entry.  Launched as the
+// pass's programmatic dependent: it may be resident while the pass runs and
+// waits here for the pass's end.
 __global__ void nv_delayed_finalize_kernel(float* hist, int n, float* ts0, float* ts1) {
+    pdl_wait();
     const float s = nv_history_scale(hist, n);
     const float amax = __uint_as_float(*reinterpret_cast<const unsigned*>(ts0));
     for (int i = n - 1; i > 0; i--) hist[i] = hist[i - 1];
@@ -974,11 +980,12 @@ __global__ void nv_delayed_finalize_kernel(float* hist, int n, float* ts0, float
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
-// Launches kernel k; with `after_amax` as a programmatic dependent of the
-// kernel before it on the stream (the amax pass): k may be scheduled while
-// that kernel still runs and waits for its end in pdl_wait.
+// Launches kernel k; with `dependent` as a programmatic dependent of the
+// kernel before it on the stream (the amax pass before a quantize kernel, the
+// quantize pass before the history update): k may be scheduled while that
+// kernel still runs and waits for its end in pdl_wait.
 template <typename... P, typename... A>
-static cudaError_t launch_k(bool after_amax, void (*k)(P...), dim3 grid, unsigned threads, cudaStream_t st,
+static cudaError_t launch_k(bool dependent, void (*k)(P...), dim3 grid, unsigned threads, cudaStream_t st,
                             A... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -989,7 +996,7 @@ static cudaError_t launch_k(bool after_amax, void (*k)(P...), dim3 grid, unsigne
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
-    cfg.numAttrs = after_amax ? 1 : 0;
+    cfg.numAttrs = dependent ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
@@ -1135,8 +1142,9 @@ cudaError_t run_quantize(const QuantizeArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (a.fmt == kNVFP4 && a.history) {
         float* other = (a.axis == 3) ? a.col_ts : nullptr;
-        nv_delayed_finalize_kernel<<<1, 1, 0, st>>>(a.history, a.hist_len, reinterpret_cast<float*>(slot), other);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_k(true, nv_delayed_finalize_kernel, dim3(1), 1, st, a.history, (int)a.hist_len,
+                          reinterpret_cast<float*>(slot), other)) != cudaSuccess)
+            return e;
     }
     return cudaSuccess;
 }
