@@ -19,10 +19,11 @@ every input resident in HBM when the timed region starts:
       expert weights to E4M3, grouped GEMM (BF16 out)
 
 value = block-scaled GEMM FLOPs of the step / device time of the whole step
-(quantize + re-encode + GEMMs), TFLOP/s.  Per-kernel times come from CUDA
-events on the launching stream inside the timed region; the roofline of the
-dominant kernel (the FP8 GEMM) and of every step are reported against the
-measured peaks.  e2e repeats the step through the same C ABI with the BF16
+(quantize + re-encode + GEMMs), TFLOP/s; the timed steps replay CUDA graphs
+of the step.  The dominant kernel (the forward FP8 GEMM) is timed with CUDA
+events inside the timed region for the roofline; the per-op table comes from
+a separate op-by-op pass with an event pair per op; both are reported
+against the measured peaks.  e2e repeats the step through the same C ABI with the BF16
 inputs copied from pinned host memory and the outputs read back, every step.
 
 Run: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
@@ -53,6 +54,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="1/8-size shapes (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps op by op on the stream instead of replaying CUDA graphs")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-reps", type=int, default=12)
     ap.add_argument("--part", default="all", choices=["all", "fwd", "bwd", "nv", "moe"],
@@ -588,21 +591,78 @@ def main():
         if world > 1:
             dist.barrier()
 
-    for _ in range(max(args.warmup, 0)):
-        step.run()
+    # The roofline kernel: the forward FP8 GEMM (2*M*N*K FLOPs per launch over
+    # its average event time), else the first GEMM of the step.
+    fwd = next((j for j, op in enumerate(step.ops) if op[0].startswith("gemm fwd")), None)
+    jr = fwd if fwd is not None else next((j for j, op in enumerate(step.ops) if op[2] == "gemm8"),
+                                          next((j for j, op in enumerate(step.ops) if op[5]), 0))
+
+    # The timed steps replay CUDA graphs of the step (one launch per graph
+    # instead of one per kernel): one graph of G = min(10, K) steps, replayed
+    # K // G times, and one of a single step for the K % G left over and the
+    # warm-up.  Inside the timed region only the roofline kernel carries an
+    # event pair (external event nodes, so that they can be read after the
+    # replay; the G-step graph's pairs hold the last G timed launches): an
+    # event pair per op costs ~70 us of a 2.4 ms step, so the per-op table
+    # comes from a separate pass after the timed region.  --no-graph (or a
+    # PyTorch without external events) launches the timed steps op by op,
+    # with the same single event pair per step.
+    def run_timed(pair):
+        for j, op in enumerate(step.ops):
+            if j == jr:
+                pair[0].record()
+            op[3]()
+            if j == jr:
+                pair[1].record()
+
+    launch_mode = "stream, op by op"
+    graphs = None
+    step.run()                 # first calls outside any capture (lazy set-up in the library)
+    torch.cuda.synchronize()
+    if not args.no_graph and args.steps > 0:
+        try:
+            G = min(10, args.steps)
+            evG = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(G)]
+            ev1 = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+            gG, g1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gG):
+                for s_ in range(G):
+                    run_timed(evG[s_])
+            with torch.cuda.graph(g1):
+                run_timed(ev1)
+            torch.cuda.synchronize()
+            graphs = (G, gG, g1, evG)
+            launch_mode = f"CUDA graph replay ({G} steps per graph)"
+        except (TypeError, RuntimeError) as exc:
+            print(f"[bench] CUDA graph capture unavailable ({exc}); launching op by op", file=sys.stderr)
+            graphs = None
+            torch.cuda.synchronize()
+    for _ in range(max(args.warmup, 0) - 1):
+        if graphs is not None:
+            graphs[2].replay()
+        else:
+            step.run()
     torch.cuda.synchronize()
 
-    # ---- timed region: K steps, per-op events on the launching stream
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nops)]
-          for _ in range(args.steps)]
+    # ---- timed region: K steps
+    evK = None
+    if graphs is None:
+        evK = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = Clocks(local)
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
     start.record()
-    for s in range(args.steps):
-        step.run(ev[s])
+    if graphs is not None:
+        G, gG, g1, evG = graphs
+        for _ in range(args.steps // G):
+            gG.replay()
+        for _ in range(args.steps % G):
+            g1.replay()
+    else:
+        for s_ in range(args.steps):
+            run_timed(evK[s_])
     stop.record()
     torch.cuda.synchronize()
     barrier()
@@ -610,9 +670,19 @@ def main():
     elapsed_ms = reduce_max(start.elapsed_time(stop), "cuda")
     ms_step = elapsed_ms / args.steps
     value = world * step.flops / (ms_step * 1e-3) / 1e12
+    timed_pairs = graphs[3] if graphs is not None else evK
+    roof_ms = statistics.mean(a.elapsed_time(b) for a, b in timed_pairs)
 
-    # per-op averages
-    op_ms = [statistics.mean(ev[s][j][0].elapsed_time(ev[s][j][1]) for s in range(args.steps)) for j in range(nops)]
+    # ---- per-op table: a separate pass after the timed region, op by op
+    # with an event pair per op
+    nrows = max(1, min(args.steps, 100))
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(nops)]
+          for _ in range(nrows)]
+    torch.cuda.synchronize()
+    for s_ in range(nrows):
+        step.run(ev[s_])
+    torch.cuda.synchronize()
+    op_ms = [statistics.mean(ev[s_][j][0].elapsed_time(ev[s_][j][1]) for s_ in range(nrows)) for j in range(nops)]
     rows, agg = {}, {}
     for (name, row, kind, _, nbytes, flops, nk), ms in zip(step.ops, op_ms):
         if flops:
@@ -678,19 +748,16 @@ def main():
     g8_ms, g8_fl = agg["gemm8"][0], agg["gemm8"][2]
     g4_ms, g4_fl = agg["gemm4"][0], agg["gemm4"][2]
     g8 = g8_fl / (g8_ms * 1e-3) / 1e12
-    # roofline of the dominant kernel (FP8 GEMM), taken on its largest launch:
-    # the forward GEMM (2*M*N*K FLOPs per launch / its average event time)
-    fwd = next((j for j, op in enumerate(step.ops) if op[0].startswith("gemm fwd")), None)
-    jr = fwd if fwd is not None else next((j for j, op in enumerate(step.ops) if op[2] == "gemm8"),
-                                          next((j for j, op in enumerate(step.ops) if op[5]), 0))
-    ach = step.ops[jr][5] / (op_ms[jr] * 1e-3) / 1e12
+    # roofline of the dominant kernel (FP8 GEMM), taken on its largest launch
+    # inside the timed region
+    ach = step.ops[jr][5] / (roof_ms * 1e-3) / 1e12
     fp4_gemm = step.ops[jr][2] == "gemm4"
     rpeak = pk["fp4_tflops"] if fp4_gemm else pk["fp8_tflops"]
     roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": rpeak, "unit": "TFLOP/s",
                 "frac": round(ach / rpeak, 4), "traffic": None,
                 "kernel": ("gemm2_kernel<nvfp4> (CTA pair, tcgen05 mxf4nvf4 block_scale)" if fp4_gemm else
                            "gemm2_kernel<fp8> (CTA pair, tcgen05 mxf8f6f4 block_scale)") + ", launch: " + step.ops[jr][0],
-                "flops_per_launch": step.ops[jr][5], "ms_per_launch": round(op_ms[jr], 4),
+                "flops_per_launch": step.ops[jr][5], "ms_per_launch": round(roof_ms, 4),
                 "peak_note": f"{'6' if fp4_gemm else '2'}x {pk['source']} bf16 burst {pk['bf16_tflops']} TFLOP/s "
                              f"(nominal dense FP8 = 2x, FP4 = 6x the BF16 rate)",
                 "frac_vs_sustained": round(ach / ((6 if fp4_gemm else 2) * pk["bf16_tflops_sustained"]), 4),
@@ -736,7 +803,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3/e5m2/e2m1 codes, f32 accumulate", "data": "synthetic",
-            "config": workload_config(args, world),
+            "config": dict(workload_config(args, world), launch=launch_mode),
             "quantize_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
             "quantize_frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "gemm_fp8_tflops": round(g8, 1), "gemm_nvfp4_tflops": round(g4_fl / (g4_ms * 1e-3) / 1e12, 1),
