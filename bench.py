@@ -625,10 +625,12 @@ def main():
             evG = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(G)]
             ev1 = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
             gG, g1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gG):
+            # thread-local capture: other threads of the process (NCCL's watchdog
+            # under torchrun) may keep making CUDA calls meanwhile
+            with torch.cuda.graph(gG, capture_error_mode="thread_local"):
                 for s_ in range(G):
                     run_timed(evG[s_])
-            with torch.cuda.graph(g1):
+            with torch.cuda.graph(g1, capture_error_mode="thread_local"):
                 run_timed(ev1)
             torch.cuda.synchronize()
             graphs = (G, gG, g1, evG)
