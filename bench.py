@@ -639,13 +639,13 @@ def main():
                                           next((j for j, op in enumerate(step.ops) if op[5]), 0))
 
     # The timed steps replay CUDA graphs of the step (one launch per graph
-    # instead of one per kernel): one graph of G = min(10, K) steps, replayed
+    # instead of one per kernel): graphs of G = min(10, K) steps, replayed
     # K // G times, and one of a single step for the K % G left over and the
-    # warm-up.  Inside the timed region only the roofline kernel carries an
-    # event pair (external event nodes, so that they can be read after the
-    # replay; the G-step graph's pairs hold the last G timed launches): an
-    # event pair per op costs ~70 us of a 2.4 ms step, so the per-op table
-    # comes from a separate pass after the timed region.  --no-graph (or a
+    # warm-up.  Only the last G timed steps carry event pairs, on the roofline
+    # kernel (external event nodes, which can be read after the replay, but
+    # cost ~8 us each inside a graph); an event pair per op costs ~70 us of a
+    # 2.4 ms step, so the per-op table comes from a separate pass after the
+    # timed region.  --no-graph (or a
     # PyTorch without external events) launches the timed steps op by op,
     # with the same single event pair per step.
     def run_timed(pair):
@@ -659,17 +659,19 @@ def main():
         try:
             G = min(10, args.steps)
             evG = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)] for _ in range(G)]
-            ev1 = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
-            gG, g1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            gG, gP, g1 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
             # thread-local capture: other threads of the process (NCCL's watchdog
             # under torchrun) may keep making CUDA calls meanwhile
             with torch.cuda.graph(gG, capture_error_mode="thread_local"):
                 for s_ in range(G):
                     run_timed(evG[s_])
+            with torch.cuda.graph(gP, capture_error_mode="thread_local"):
+                for s_ in range(G):
+                    step.run_overlapped()
             with torch.cuda.graph(g1, capture_error_mode="thread_local"):
-                run_timed(ev1)
+                step.run_overlapped()
             torch.cuda.synchronize()
-            graphs = (G, gG, g1, evG)
+            graphs = (G, gG, gP, g1, evG)
             launch_mode = f"CUDA graph replay ({G} steps per graph)"
         except (TypeError, RuntimeError) as exc:
             print(f"[bench] CUDA graph capture unavailable ({exc}); launching op by op", file=sys.stderr)
@@ -677,7 +679,7 @@ def main():
             torch.cuda.synchronize()
     for _ in range(max(args.warmup, 0) - 1):
         if graphs is not None:
-            graphs[2].replay()
+            graphs[3].replay()
         else:
             step.run()
     torch.cuda.synchronize()
@@ -693,11 +695,13 @@ def main():
     torch.cuda.synchronize()
     start.record()
     if graphs is not None:
-        G, gG, g1, evG = graphs
-        for _ in range(args.steps // G):
-            gG.replay()
+        # the last G timed steps carry the roofline kernel's event nodes
+        G, gG, gP, g1, evG = graphs
         for _ in range(args.steps % G):
             g1.replay()
+        for _ in range(args.steps // G - 1):
+            gP.replay()
+        gG.replay()
     else:
         for s_ in range(args.steps):
             run_timed(evK[s_])
@@ -708,7 +712,7 @@ def main():
     elapsed_ms = reduce_max(start.elapsed_time(stop), "cuda")
     ms_step = elapsed_ms / args.steps
     value = world * step.flops / (ms_step * 1e-3) / 1e12
-    timed_pairs = graphs[3] if graphs is not None else evK
+    timed_pairs = graphs[4] if graphs is not None else evK
     roof_ms = statistics.mean(a.elapsed_time(b) for a, b in timed_pairs)
 
     # ---- per-op table: a separate pass after the timed region, op by op
