@@ -278,46 +278,52 @@ class Step:
             if events is not None:
                 events[j][1].record()
 
-    # Independent quantizes that run side by side: op -> (the op it starts
-    # beside, the op that waits for it).  Each side op goes to a second stream
-    # when the main stream reaches its partner, and the GEMM that reads its
-    # output waits for that stream; the GEMMs themselves run alone.
-    SIDE = {"quant W e4m3 both": ("quant X e4m3 both", "gemm fwd Y=XW^T"),
-            "quant W nvfp4": ("quant X nvfp4", "gemm nvfp4 Y=XW^T"),
-            "quant W' nvfp4": ("quant X' nvfp4", "gemm nvfp4 Y'=X'W'^T"),
-            "quant W_moe e4m3 row": ("quant A_moe mxfp4 row", "grouped gemm moe")}
+    # Independent quantizes that run side by side: op -> (side stream, the op
+    # it starts beside, the op that waits for it).  Each side op goes to its
+    # side stream when the main stream reaches its partner, and the op that
+    # reads its output waits for that stream; the GEMMs themselves run alone.
+    # The four NVFP4 quantizes run at once: X on the main stream, W then W' on
+    # side stream 0, X' on side stream 1.
+    SIDE = {"quant W e4m3 both": (0, "quant X e4m3 both", "gemm fwd Y=XW^T"),
+            "quant W nvfp4": (0, "quant X nvfp4", "gemm nvfp4 Y=XW^T"),
+            "quant X' nvfp4": (1, "quant X nvfp4", "gemm nvfp4 Y'=X'W'^T"),
+            "quant W' nvfp4": (0, "quant X nvfp4", "gemm nvfp4 Y'=X'W'^T"),
+            "quant W_moe e4m3 row": (0, "quant A_moe mxfp4 row", "grouped gemm moe")}
 
     def run_overlapped(self, timed=None, jr=None):
-        """The step with the SIDE quantizes on a second stream (the timed
-        steps); `timed`: an event pair recorded around op `jr`."""
+        """The step with the SIDE quantizes on side streams (the timed steps);
+        `timed`: an event pair recorded around op `jr`."""
         torch = self.torch
-        if not hasattr(self, "side_stream"):
-            self.side_stream = torch.cuda.Stream()
+        if not hasattr(self, "side_streams"):
+            self.side_streams = [torch.cuda.Stream() for _ in range(2)]
         cur = torch.cuda.current_stream()
         by_name = {op[0]: j for j, op in enumerate(self.ops)}
-        starts = {}
-        joins = {}
-        for side, (partner, reader) in self.SIDE.items():
+        starts, joins = {}, {}
+        for side, (lane, partner, reader) in self.SIDE.items():
             if side in by_name and partner in by_name and reader in by_name:
-                starts.setdefault(partner, []).append(side)
-                joins.setdefault(reader, []).append(side)
-        moved = {side for sides in starts.values() for side in sides}
+                starts.setdefault(partner, []).append((lane, side))
+                joins.setdefault(reader, set()).add(lane)
+        moved = {side for sides in starts.values() for _, side in sides}
+        used = set()
         for j, op in enumerate(self.ops):
             name = op[0]
             if name in moved:
                 continue
-            if name in joins:
-                cur.wait_stream(self.side_stream)
-            for side in starts.get(name, ()):
-                self.side_stream.wait_stream(cur)
-                with torch.cuda.stream(self.side_stream):
+            for lane in sorted(joins.get(name, ())):
+                cur.wait_stream(self.side_streams[lane])
+            for lane, side in starts.get(name, ()):
+                used.add(lane)
+                self.side_streams[lane].wait_stream(cur)
+                with torch.cuda.stream(self.side_streams[lane]):
                     self.ops[by_name[side]][3]()
             if j == jr and timed is not None:
                 timed[0].record()
             op[3]()
             if j == jr and timed is not None:
                 timed[1].record()
-        cur.wait_stream(self.side_stream)
+        # (a stream that took no work here must not be joined inside a capture)
+        for lane in sorted(used):
+            cur.wait_stream(self.side_streams[lane])
 
     # e2e: host (pinned) -> device copies of every BF16 input, the step, and a
     # device -> host read of every output, all inside the timed region.  The
