@@ -104,6 +104,45 @@ def test_quantize_every_bf16_pattern_scaled_blocks(bsq, fmt):
     assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} anchored")
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("axis", ["col", "both"])
+@pytest.mark.parametrize("order", [None, 1])
+def test_quantize_every_bf16_pattern_columns(bsq, fmt, axis, order):
+    """All 65536 BF16 bit patterns through the column-wise and both-ways
+    kernel: the 32-row (NVFP4: 16-row) column blocks hold every NaN, Inf,
+    subnormal and signed zero, and the row blocks of `both` every pattern
+    again in another grouping."""
+    x = _all_bf16_patterns(order)
+    row, col = qz(bsq, dev_bf16(x), fmt, axis)
+    exp = expected(x, fmt, axis)
+    assert_qtensor_equal(col, exp["col"], f"{fmt} {axis} col all-bf16 order={order}")
+    if axis == "both":
+        assert_qtensor_equal(row, exp["row"], f"{fmt} both/row all-bf16 order={order}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_quantize_every_bf16_pattern_scaled_columns(bsq, fmt):
+    """The anchored blocks of the row test, transposed: each column block
+    holds 31 (NVFP4: 15) patterns and an anchor 2^k above them."""
+    rng = np.random.default_rng(4)
+    fin = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    fin = fin[(fin & 0x7F80) != 0x7F80]
+    blk = 16 if fmt == "nvfp4" else 32
+    blocks = []
+    for shift in (0, 1, 3, 7):
+        v = rng.permutation(fin)
+        n = len(v) // (blk - 1) * (blk - 1)
+        body = v[:n].reshape(-1, blk - 1)
+        mags = (body & 0x7FFF).max(axis=1)
+        anchor = np.minimum(mags.astype(np.int64) + (shift << 7), 0x7F7F).astype(np.uint16)
+        blocks.append(np.concatenate([body, anchor[:, None]], axis=1))
+    b = np.concatenate(blocks)
+    b = b[: len(b) // 8 * 8]                       # whole 8-column chunks
+    x = np.ascontiguousarray(b.T)                  # [blk, n]: one block per column
+    _, col = qz(bsq, dev_bf16(x), fmt, "col")
+    assert_qtensor_equal(col, expected(x, fmt, "col")["col"], f"{fmt} anchored columns")
+
+
 def test_quantize_zero_and_nonfinite_blocks(bsq):
     x = np.zeros((4, 64), dtype=np.uint16)
     x[1, 3] = 0x7FC0          # NaN
@@ -113,6 +152,13 @@ def test_quantize_zero_and_nonfinite_blocks(bsq):
     for fmt in FMTS:
         row, col = qz(bsq, dev_bf16(x), fmt, "row")
         assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} special")
+    # the same blocks down the columns (32 rows: one block per column)
+    xt = np.ascontiguousarray(np.tile(x.T, (1, 8)))          # [64, 32]
+    for fmt in FMTS:
+        row, col = qz(bsq, dev_bf16(xt), fmt, "both")
+        exp = expected(xt, fmt, "both")
+        assert_qtensor_equal(col, exp["col"], f"{fmt} special columns")
+        assert_qtensor_equal(row, exp["row"], f"{fmt} special both/row")
 
 
 def test_nvfp4_tensor_scale_shared(bsq):
