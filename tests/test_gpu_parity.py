@@ -282,6 +282,39 @@ def test_gemm_bf16_output(bsq, fmt):
     _check_gemm(bsq, xa, fmt, xb, fmt, "bf16")
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dtype_name", ["f32", "bf16"])
+def test_gemm_nonfinite_blocks_propagate(bsq, fmt, dtype_name):
+    """A block holding NaN or Inf quantizes to the NaN scale (E8M0 0xFF, or
+    UE4M3 0x7F for NVFP4), whose value is NaN; every output of that row of A
+    (or column of C for a row of B) must then be NaN, as in the oracle's FP64
+    product, and no other output may be NaN or leave the bound.  Rows on
+    both M tiles and a ragged N tail."""
+    import torch
+    M, N, K = 200, 300, 512
+    xa = inputs.normal_bf16((M, K), 7)
+    xb = inputs.normal_bf16((N, K), 8, std=0.02)
+    xa[5, 40] = 0x7FC0      # NaN
+    xa[9, 100] = 0x7F80     # +Inf
+    xa[130, 511] = 0xFF80   # -Inf, last block of the row
+    xb[17, 0] = 0xFFC1      # a NaN with a payload and the sign set
+    xb[299, 256] = 0x7F80
+    ca, sa, ta = _q_oracle(xa, fmt)
+    cb, sb, tb = _q_oracle(xb, fmt)
+    A = upload_q(bsq, fmt, ca, sa, ta)
+    B = upload_q(bsq, fmt, cb, sb, tb)
+    dt = torch.float32 if dtype_name == "f32" else torch.bfloat16
+    C = gemm_g(bsq, A, B, dt).float().cpu().numpy()
+    ref, mag = oracle.gemm_full(oracle.dequant_rows(ca, sa, fmt, ta), oracle.dequant_rows(cb, sb, fmt, tb))
+    nan_ref = np.isnan(ref)
+    rows, cols = np.array([5, 9, 130]), np.array([17, 299])
+    assert nan_ref[rows].all() and nan_ref[:, cols].all()
+    assert nan_ref.sum() == len(rows) * N + len(cols) * M - len(rows) * len(cols)
+    np.testing.assert_array_equal(np.isnan(C), nan_ref)
+    ok, _, _ = gemm_tol_ok(C[~nan_ref], ref[~nan_ref], mag[~nan_ref], dtype_name == "bf16")
+    assert ok.all(), f"{(~ok).sum()} finite outputs outside the bound"
+
+
 def test_gemm_single_scale_probe(bsq):
     """One non-unit scale per 128x4 tile position: checks that every scale
     byte reaches the MMA for the row / block it belongs to."""
