@@ -546,6 +546,26 @@ def test_gemm_single_cta_tile_path(bsq, M, N, K, fmt, monkeypatch):
     _check_gemm(bsq, xa, fmt, xb, fb, "f32")
 
 
+@pytest.mark.parametrize("kernel", ["pair", "1cta"])
+@pytest.mark.parametrize("dtype_name", ["f32", "bf16"])
+def test_gemm_nvfp4_tiny_tensor_scales(bsq, kernel, dtype_name, monkeypatch):
+    """NVFP4 operands whose tensor amax is about 2^-58: each tensor scale
+    amax / 2688 is a normal FP32 number, but their product is an FP32
+    subnormal with about eleven significant bits, so an epilogue that formed it
+    would leave the bound; applied one after the other they keep the
+    outputs (about 2^-115, normal) within it."""
+    if kernel == "1cta":
+        monkeypatch.setenv("BSQ_GEMM_1CTA", "1")
+    M, N, K = 300, 260, 512
+    xa = inputs.normal_bf16((M, K), 11, std=2.0 ** -60)
+    xb = inputs.normal_bf16((N, K), 12, std=2.0 ** -60)
+    ta = oracle.quantize_rows(xa, "nvfp4")[2]
+    tb = oracle.quantize_rows(xb, "nvfp4")[2]
+    assert ta >= 2.0 ** -126 and tb >= 2.0 ** -126 and float(ta) * float(tb) < 2.0 ** -126
+    C, ref = _check_gemm(bsq, xa, "nvfp4", xb, "nvfp4", dtype_name)
+    assert np.abs(ref).max() > 2.0 ** -120 and np.isfinite(C).all()
+
+
 def test_gemm_pair_tile_tails(bsq):
     """Tails of the 256 x 256 pair tile: the odd CTA's rows fully past M,
     the second B half past N, and a K tail inside the last stage."""
