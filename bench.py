@@ -575,6 +575,23 @@ def dist_setup(args):
     return rank, world, local
 
 
+def attainable(step, ms, pk, fp4):
+    """Attainable time of the grouped MoE GEMM: per expert the larger of its
+    compute time at the tensor peak (FP8, or FP4 for MXFP4 operands) and the
+    time to stream its weights, activations (codes and E8M0 scales per 32)
+    and BF16 output at the HBM rate; small experts are bound by their
+    weights."""
+    K_, N_ = step.moe_kn
+    code = 0.5 if fp4 else 1.0
+    peak = pk["fp4_tflops"] if fp4 else pk["fp8_tflops"]
+    t_bound = 0.0
+    for cnt in step.moe_counts:
+        fl = 2.0 * cnt * N_ * K_
+        by = N_ * K_ * (code + 1 / 32) + cnt * K_ * (code + 1 / 32) + cnt * N_ * 2
+        t_bound += max(fl / (peak * 1e12), by / (pk["hbm_gbs"] * 1e9))
+    return {"attainable_ms": round(t_bound * 1e3, 4), "frac_attainable": round(t_bound * 1e3 / ms, 4)}
+
+
 def reduce_max(x: float, device="cpu") -> float:
     """Max of x over all ranks (identity without a process group)."""
     import torch
@@ -746,17 +763,7 @@ def main():
             one = nbytes * (2 + 0.5 + 1 / 16) / (2 + 2 + 0.5 + 1 / 16)
             rec["frac_one_read"] = round(one / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)
         if name == "grouped gemm moe" and step.moe_counts is not None:
-            # attainable time: per expert the larger of its compute time at the
-            # FP8 peak and the time to stream its weights, activations and
-            # output at the HBM rate (small experts are bound by their weights)
-            K_, N_ = step.moe_kn
-            t_bound = 0.0
-            for cnt in step.moe_counts:
-                fl = 2.0 * cnt * N_ * K_
-                by = N_ * K_ * (1 + 1 / 32) + cnt * K_ * (1 + 1 / 32) + cnt * N_ * 2
-                t_bound += max(fl / (pk["fp8_tflops"] * 1e12), by / (pk["hbm_gbs"] * 1e9))
-            rec["attainable_ms"] = round(t_bound * 1e3, 4)
-            rec["frac_attainable"] = round(t_bound * 1e3 / ms, 4)
+            rec.update(attainable(step, ms, pk, fp4=False))
         rows[name] = dict(row=row, **rec)
         a = agg.setdefault(kind, [0.0, 0.0, 0.0])
         a[0] += ms
@@ -788,6 +795,8 @@ def main():
                 ach = flops / (ms * 1e-3) / 1e12
                 peak = pk["fp4_tflops"] if kind == "gemm4" else pk["fp8_tflops"]
                 rows_next[name] = {"row": row, "ms": round(ms, 4), "tflops": round(ach, 1), "frac": round(ach / peak, 4)}
+                if name == "grouped gemm moe mxfp4" and step.moe_counts is not None:
+                    rows_next[name].update(attainable(step, ms, pk, fp4=True))
             else:
                 ach = nbytes / (ms * 1e-3) / 1e9
                 rows_next[name] = {"row": row, "ms": round(ms, 4), "gbs": round(ach, 1),
