@@ -399,16 +399,16 @@ cudaError_t run_repack_1x128(const RepackArgs& a, cudaStream_t st) {
 // byte s its value is a * 2^(b + s - 127), whose floor(log2) is
 // b + [a == 3] + s - 127.  A 32-row block of one column takes the E8M0
 // exponent e = clamp(max floor(log2) - 8, -127, 127) (the MX rule with
-// E4M3's largest exponent 8; -127 for an all-zero block), each element
-// a * 2^(b + s - 127 - e) is built as an exact FP32 value and rounded once
-// by the hardware E4M3 conversion; a NaN row scale (0xFF) in the block
-// makes the block NaN.  Tiles of 128 input rows x 128 input columns: the
-// codes (8 KB) and the one 512-byte scale tile that covers them are staged
-// in shared memory; a thread encodes two (column, 32-row block) pairs.
+// E4M3's largest exponent 8; -127 for an all-zero block), and each element
+// a * 2^(b + s - 127 - e) is formed exactly and rounded once by the
+// hardware E4M3 conversion; a NaN row scale (0xFF) in the block makes the
+// block NaN.  Tiles of 256 input rows x 128 input columns: the codes
+// (16 KB) and the two 512-byte scale tiles that cover them are staged in
+// shared memory.
 // ---------------------------------------------------------------------------
 constexpr int kColRows = 256;       // tile: 256 input rows x 128 input columns
 constexpr int kColCols = 128;
-constexpr int kColThreads = 256;    // one thread = 4 columns x one 32-row block
+constexpr int kColThreads = 256;    // one thread = 8 columns x 16 rows
 
 // b + 1 of the E2M1 magnitudes, 4 bits each (index m), for the exact path
 constexpr uint32_t kBexp = 0x23120100u;     // m 1..7 -> 0,1,0,2,1,3,2 (m = 0 unused)
@@ -445,16 +445,6 @@ __device__ __forceinline__ uint32_t fp8_of_nibble(uint32_t n, uint32_t sr, uint3
     return fp8_of_nibble_exact(n, (int)sr - (int)sb);
 }
 
-// Fast path helpers.  Two E2M1 pairs (bytes 0 and 1 of w, low nibble
-// first) -> two f16x2 with the low nibble in the low half; the conversion is
-// exact (every E2M1 value is a half).
-__device__ __forceinline__ void h2_of_e2m1x4(uint32_t w, uint32_t& h01, uint32_t& h23) {
-    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\tmov.b32 {t0, t1, t2, t3}, %2;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, t0;\n\tcvt.rn.f16x2.e2m1x2 %1, t1;\n\t}"
-        : "=r"(h01), "=r"(h23)
-        : "r"(w));
-}
-
 // Per-nibble tables for the column maximum, indexed by the magnitude m
 // through a byte permute: lev1 = (m >> 1) + 1 (0 for m = 0), and a high byte
 // 0xFC for m = 0 so that a zero code becomes the 16-bit lane -1024, which
@@ -464,157 +454,194 @@ constexpr uint32_t kLev1Hi = 0x04040303u;   // m 4..7 -> 3, 3, 4, 4
 constexpr uint32_t kZeroLo = 0x000000FCu;   // m 0 -> 0xFC, 1..3 -> 0
 constexpr uint32_t kZeroHi = 0x00000000u;
 
-__global__ void __launch_bounds__(kColThreads)
+// max(|a|, |b|) per half (the sign bit of the result is sign(a) ^ sign(b))
+__device__ __forceinline__ uint32_t habsmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Layout: a thread owns one code word (8 columns) of 16 rows, half of a
+// 32-row block; the two threads of a block are neighbouring lanes and
+// combine their column maxima with shuffles.  The 16 code words stay in
+// registers, and the row scales are staged by column block ([column
+// block][row]), so a thread's 16 row scales are one 16-byte load.
+//
+// Blocks without a NaN row scale whose row scales lie within 14 binades
+// (nearly all) take the half path: each element is formed exactly as
+// code * 2^(sr - smax) in FP16 (E2M1 -> f16x2 is exact, and the factor's
+// exponent field sr - smax + 15 lies in [1, 15], so the product is an exact
+// half, a subnormal at worst); the column's largest |product| gives its
+// largest exponent directly (floor(log2 amax) = exponent(max) + smax - 127),
+// and the encode multiplies the same product by 2^(smax - sb), which makes
+// the exact value code * 2^(sr - sb) whenever that factor's exponent field
+// smax - sb + 15 lies in [1, 30], then rounds once (f16x2 -> E4M3).  Other
+// blocks take the column maximum in the integer domain and the scalar
+// encode.
+__global__ void __launch_bounds__(kColThreads, 4)
 repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ sin, int64_t R, int64_t C,
-                  int64_t s_tiles_in, uint8_t* __restrict__ out, uint8_t* __restrict__ sout, int64_t s_tiles_out,
-                  bool wide) {
-    __shared__ __align__(16) uint32_t codes[kColRows * 16];    // 256 rows x 64 bytes
-    __shared__ __align__(16) uint8_t sf[2 * 512];              // row scales: two 128x4 tiles
+                  int64_t s_tiles_in, uint8_t* __restrict__ out, uint8_t* __restrict__ sout, int64_t s_tiles_out) {
+    // codes: 256 rows x 64 bytes; row r sits at r ^ 1 where bit 4 of r is set,
+    // so that a block's two threads (rows 16 apart) read opposite bank halves
+    __shared__ __align__(16) uint32_t codes[kColRows * 16];
+    __shared__ __align__(16) uint8_t sfr[4 * kColRows];       // row scales: [column block][row]
     const int tid = threadIdx.x;
     const int64_t r0 = (int64_t)blockIdx.y * kColRows, c0 = (int64_t)blockIdx.x * kColCols;
-    // codes: 256 rows x 4 chunks of 16 bytes (32 columns each)
 #pragma unroll
     for (int k = 0; k < 4; k++) {
         const int idx = tid + k * kColThreads, rr = idx >> 2, ch = idx & 3;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (r0 + rr < R && c0 + 32 * ch < C)
             v = *reinterpret_cast<const uint4*>(in + (r0 + rr) * (C / 2) + c0 / 2 + 16 * ch);
-        *reinterpret_cast<uint4*>(&codes[rr * 16 + ch * 4]) = v;
+        *reinterpret_cast<uint4*>(&codes[(rr ^ ((rr >> 4) & 1)) * 16 + ch * 4]) = v;
     }
-    if (tid < 64) {
-        const int band = tid >> 5;          // 128-row band of the tile
-        uint4 v = make_uint4(0, 0, 0, 0);
+    {
+        // row tid's four scale bytes (the tile's column blocks 0-3) from its 128x4 scale tile
+        const int band = tid >> 7;
+        uint32_t v = 0;
         if (r0 + 128 * band < R)
-            v = *reinterpret_cast<const uint4*>(sin + ((r0 / 128 + band) * s_tiles_in + c0 / 128) * 512 + (tid & 31) * 16);
-        *reinterpret_cast<uint4*>(&sf[band * 512 + (tid & 31) * 16]) = v;
+            v = *reinterpret_cast<const uint32_t*>(sin + ((r0 / 128 + band) * s_tiles_in + c0 / 128) * 512 +
+                                                   (tid & 31) * 16 + ((tid >> 5) & 3) * 4);
+#pragma unroll
+        for (int cb = 0; cb < 4; cb++) sfr[cb * kColRows + tid] = (uint8_t)(v >> (8 * cb));
     }
     __syncthreads();
-    const int quad = tid & 31, rb = tid >> 5;           // columns 4 quad .. 4 quad + 3, rows 32 rb .. 32 rb + 31
-    const int c = 4 * quad, cb = c >> 5;
+    const int lane = tid & 31, rb = tid >> 5, w = lane >> 1, h = lane & 1;
+    const int c = 8 * w, cb = w >> 2;                  // columns c .. c + 7, rows 32 rb + 16 h .. + 15
     if (c0 + c >= C || r0 + 32 * rb >= R) return;
-    const int wi = c >> 3, sh = (c & 7) * 4;            // the word and bit offset of the 4 nibbles
-    const uint8_t* srow = sf + (rb >> 2) * 512 + (rb & 3) * 4 + cb;   // + i * 16 for row i of the block
-    // pass 1: per column the largest key + 1 = (m >> 1) + 1 + sr over nonzero
-    // codes (0 if none), in 16-bit lanes for two columns at a time; the
-    // smallest and largest row scale (a NaN scale is the largest byte)
-    uint32_t acc01 = 0, acc23 = 0, smax = 0, smin = 0xFFu;
-#pragma unroll 8
-    for (int i = 0; i < 32; i++) {
-        const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
-        const uint32_t sr = srow[i * 16];
-        smax = max(smax, sr);
-        smin = min(smin, sr);
-        const uint32_t sel = nb & 0x7777u;
-        const uint32_t lev = prmt(kLev1Lo, kLev1Hi, sel), zero = prmt(kZeroLo, kZeroHi, sel);
-        const uint32_t sr2 = sr * 0x00010001u;
-        acc01 = __viaddmax_s16x2(prmt(lev, zero, 0x5140u), sr2, acc01);
-        acc23 = __viaddmax_s16x2(prmt(lev, zero, 0x7362u), sr2, acc23);
+    const unsigned pair = 3u << (lane & 30);
+    uint32_t nb[16];
+#pragma unroll
+    for (int i = 0; i < 16; i++) nb[i] = codes[((32 * rb + 16 * h + i) ^ h) * 16 + w];
+    const uint4 s4 = *reinterpret_cast<const uint4*>(&sfr[cb * kColRows + 32 * rb + 16 * h]);
+    const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};   // row i's scale: byte i & 3 of word i >> 2
+    // the block's largest and smallest row scale (a NaN scale is the largest byte),
+    // in 16-bit lanes as (sr, 255 - sr)
+    uint32_t mm = 0;
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+        const uint32_t j = (uint32_t)(i & 3);
+        mm = __viaddmax_u16x2(prmt(sw[i >> 2], 0u, 0x4040u | j | (j << 8)) ^ 0x00FF0000u, 0u, mm);
     }
+    mm = __viaddmax_u16x2(__shfl_xor_sync(pair, mm, 1), 0u, mm);
+    const uint32_t smax = mm & 0xFFFFu, smin = 255u - (mm >> 16);
     const bool nan = smax == 0xFFu;
-    const uint32_t kp[4] = {acc01 & 0xFFFFu, acc01 >> 16, acc23 & 0xFFFFu, acc23 >> 16};
-    // scale bytes: floor(log2 amax) = key - 128, e = that - 8 clamped to [-127, 127]
-    uint32_t sb[4];
-#pragma unroll
-    for (int k = 0; k < 4; k++) sb[k] = nan ? 0xFFu : (uint32_t)min(max((int)kp[k] - 10, 0), 254);
-    uint8_t* dst0 = out + (c0 + c) * R + r0 + 32 * rb;
-    // Fast path: each element is code * 2^(sr - sb) exactly, formed as a
-    // half product (E2M1 -> f16x2, times the power of two built from its
-    // exponent field sr - sb + 15) and rounded once by the f16x2 -> E4M3
-    // conversion.  It needs that exponent field in [1, 30] for every row and
-    // column of the block; an all-zero column may take any power, so it
-    // takes the one at the largest row scale.  Other blocks (row scales
-    // spread over more than about 15 binades, or a NaN) take the scalar path.
-    int g[4];
-    bool fast = !nan;
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-        const int sbp = kp[k] == 0 ? (int)smax - 15 : (int)sb[k];
-        g[k] = 15 - sbp;
-        fast = fast && (int)smax + g[k] <= 30 && (int)smin + g[k] >= 1;
-    }
+    uint32_t sb[8];
+    int g[8];
+    bool fast = !nan && smax - smin <= 14u;
+    const uint32_t kr = (15u - smax) * 0x04000400u;    // row factor 2^(sr - smax): sr * 0x04000400 + kr
     if (fast) {
-        // exponent fields of two columns in 16-bit lanes: sr * 0x00010001 + G,
-        // the low lane's borrow (G < 0) taken back from the high lane, then
-        // shifted into place (all mod 2^32, so one multiply-add per pair)
-        uint32_t G01 = ((uint32_t)g[0] & 0xFFFFu) | ((uint32_t)g[1] << 16);
-        uint32_t G23 = ((uint32_t)g[2] & 0xFFFFu) | ((uint32_t)g[3] << 16);
-        if (g[0] < 0) G01 -= 0x10000u;
-        if (g[2] < 0) G23 -= 0x10000u;
-        G01 <<= 10;
-        G23 <<= 10;
-        uint32_t ow[4][8];            // column k, rows 4 v .. 4 v + 3 in word v
+        uint32_t M[4] = {0u, 0u, 0u, 0u};               // columns (0,1) (2,3) (4,5) (6,7)
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            uint32_t W[8];            // row 8 q + h: the E4M3 bytes of the 4 columns
-#pragma unroll
-            for (int h = 0; h < 8; h++) {
-                const int i = 8 * q + h;
-                const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
-                const uint32_t sr = srow[i * 16];
-                uint32_t h01, h23;
-                h2_of_e2m1x4(nb, h01, h23);
-                const uint32_t b01 = e4m3x2_of_h2(hmul2_rn(h01, sr * 0x04000400u + G01));
-                const uint32_t b23 = e4m3x2_of_h2(hmul2_rn(h23, sr * 0x04000400u + G23));
-                W[h] = prmt(b01, b23, 0x5410u);
-            }
-            // 4 x 4 byte transposes: rows -> columns
-            uint32_t lo[4], hi[4];
-#pragma unroll
-            for (int half = 0; half < 2; half++) {
-                const uint32_t* w4 = W + 4 * half;
-                const uint32_t t0 = prmt(w4[0], w4[1], 0x5140u), t1 = prmt(w4[0], w4[1], 0x7362u);
-                const uint32_t t2 = prmt(w4[2], w4[3], 0x5140u), t3 = prmt(w4[2], w4[3], 0x7362u);
-                uint32_t* d = half ? hi : lo;
-                d[0] = prmt(t0, t2, 0x5410u);
-                d[1] = prmt(t0, t2, 0x7632u);
-                d[2] = prmt(t1, t3, 0x5410u);
-                d[3] = prmt(t1, t3, 0x7632u);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                ow[k][2 * q] = lo[k];
-                ow[k][2 * q + 1] = hi[k];
-            }
+        for (int i = 0; i < 16; i++) {
+            const uint32_t Fr = prmt(sw[i >> 2], 0u, 0x4440u | (uint32_t)(i & 3)) * 0x04000400u + kr;
+            uint32_t h0, h1, h2, h3;
+            h2_of_e2m1x8(nb[i], h0, h1, h2, h3);
+            M[0] = habsmax2(M[0], hmul2_rn(h0, Fr));
+            M[1] = habsmax2(M[1], hmul2_rn(h1, Fr));
+            M[2] = habsmax2(M[2], hmul2_rn(h2, Fr));
+            M[3] = habsmax2(M[3], hmul2_rn(h3, Fr));
         }
-        // each column's 32 rows leave as whole 32-byte sectors
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-            uint8_t* d = dst0 + (int64_t)k * R;
-            if (wide) {
-                asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(d), "r"(ow[k][0]),
-                             "r"(ow[k][1]), "r"(ow[k][2]), "r"(ow[k][3]), "r"(ow[k][4]), "r"(ow[k][5]), "r"(ow[k][6]),
-                             "r"(ow[k][7])
-                             : "memory");
-            } else {
-                reinterpret_cast<uint4*>(d)[0] = make_uint4(ow[k][0], ow[k][1], ow[k][2], ow[k][3]);
-                reinterpret_cast<uint4*>(d)[1] = make_uint4(ow[k][4], ow[k][5], ow[k][6], ow[k][7]);
-            }
+        for (int k = 0; k < 4; k++) M[k] = habsmax2(M[k], __shfl_xor_sync(pair, M[k], 1)) & 0x7FFF7FFFu;
+        // scale byte = floor(log2 amax) - 8 + 127 = exponent field - 23 + smax, clamped to
+        // [0, 254]; 0 for an all-zero column, which takes the factor 2^15 / 2^(smax - 15)
+        // (any finite factor keeps its zeros)
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const uint32_t mk = (M[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+            const int e = (int)(mk >> 10) - 23 + (int)smax;
+            sb[k] = mk == 0 ? 0u : (uint32_t)min(max(e, 0), 254);
+            const int sbp = mk == 0 ? (int)smax - 15 : (int)sb[k];
+            g[k] = 15 - sbp;
+            fast = fast && (int)smax + g[k] <= 30;
         }
     } else {
-        // scalar path: the E4M3 byte of each code in the integer domain
-#pragma unroll 1
-        for (int q = 0; q < 4; q++) {
-            uint32_t lo[4] = {0, 0, 0, 0}, hi[4] = {0, 0, 0, 0};
+        // column maximum in the integer domain: per column the largest
+        // key + 1 = (m >> 1) + 1 + sr over nonzero codes (0 if none), in
+        // 16-bit lanes for two columns at a time
+        uint32_t acc[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int h = 0; h < 8; h++) {
-                const int i = 8 * q + h;
-                const uint32_t nb = codes[(32 * rb + i) * 16 + wi] >> sh;
-                const uint32_t sr = srow[i * 16];
+        for (int i = 0; i < 16; i++) {
+            const uint32_t j = (uint32_t)(i & 3);
+            const uint32_t sr2 = prmt(sw[i >> 2], 0u, 0x4040u | j | (j << 8));
+            // the byte permutes read only the low 16 bits of their selector
+            const uint32_t sel_lo = nb[i] & 0x77777777u, sel_hi = sel_lo >> 16;
+            const uint32_t lev_lo = prmt(kLev1Lo, kLev1Hi, sel_lo), z_lo = prmt(kZeroLo, kZeroHi, sel_lo);
+            const uint32_t lev_hi = prmt(kLev1Lo, kLev1Hi, sel_hi), z_hi = prmt(kZeroLo, kZeroHi, sel_hi);
+            acc[0] = __viaddmax_s16x2(prmt(lev_lo, z_lo, 0x5140u), sr2, acc[0]);
+            acc[1] = __viaddmax_s16x2(prmt(lev_lo, z_lo, 0x7362u), sr2, acc[1]);
+            acc[2] = __viaddmax_s16x2(prmt(lev_hi, z_hi, 0x5140u), sr2, acc[2]);
+            acc[3] = __viaddmax_s16x2(prmt(lev_hi, z_hi, 0x7362u), sr2, acc[3]);
+        }
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const uint32_t b = fp8_of_nibble((nb >> (4 * k)) & 0xFu, sr, sb[k]) << (8 * (h & 3));
-                    if (h < 4) lo[k] |= b;
-                    else hi[k] |= b;
-                }
-            }
+        for (int k = 0; k < 4; k++) acc[k] = __viaddmax_s16x2(__shfl_xor_sync(pair, acc[k], 1), 0u, acc[k]);
+        // scale bytes: floor(log2 amax) = key - 128, e = that - 8 clamped to [-127, 127]
 #pragma unroll
-            for (int k = 0; k < 4; k++)
-                *reinterpret_cast<uint2*>(dst0 + (int64_t)k * R + 8 * q) =
-                    nan ? make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu) : make_uint2(lo[k], hi[k]);
+        for (int k = 0; k < 8; k++) {
+            const int kp = (int)((acc[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);
+            sb[k] = nan ? 0xFFu : (uint32_t)min(max(kp - 10, 0), 254);
+            g[k] = 0;
         }
     }
+    uint8_t* dst0 = out + (c0 + c) * R + r0 + 32 * rb + 16 * h;
+    if (fast) {
+        // column factors 2^(smax - sb) (exponent fields smax + g in [1, 30])
+        uint32_t Fc[4];
 #pragma unroll
-    for (int k = 0; k < 4; k++) sout[sf_offset(c0 + c + k, r0 / 32 + rb, s_tiles_out)] = (uint8_t)sb[k];
+        for (int p2 = 0; p2 < 4; p2++)
+            Fc[p2] = ((uint32_t)((int)smax + g[2 * p2]) << 10) | ((uint32_t)((int)smax + g[2 * p2 + 1]) << 26);
+        uint32_t ow[8][4];            // column k, rows 4 q .. 4 q + 3 in word q
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            uint32_t e[4][4];         // row 4 q + j, columns (2 p, 2 p + 1): two E4M3 bytes
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const uint32_t Fr = prmt(sw[q], 0u, 0x4440u | (uint32_t)j) * 0x04000400u + kr;
+                uint32_t hh[4];
+                h2_of_e2m1x8(nb[4 * q + j], hh[0], hh[1], hh[2], hh[3]);
+#pragma unroll
+                for (int p2 = 0; p2 < 4; p2++) e[j][p2] = e4m3x2_of_h2(hmul2_rn(hmul2_rn(hh[p2], Fr), Fc[p2]));
+            }
+            // 4 x 4 byte transposes straight from the byte pairs: rows -> columns
+#pragma unroll
+            for (int p2 = 0; p2 < 4; p2 += 2) {
+                const uint32_t t0 = prmt(e[0][p2], e[1][p2], 0x5140u), t1 = prmt(e[0][p2 + 1], e[1][p2 + 1], 0x5140u);
+                const uint32_t t2 = prmt(e[2][p2], e[3][p2], 0x5140u), t3 = prmt(e[2][p2 + 1], e[3][p2 + 1], 0x5140u);
+                ow[2 * p2 + 0][q] = prmt(t0, t2, 0x5410u);
+                ow[2 * p2 + 1][q] = prmt(t0, t2, 0x7632u);
+                ow[2 * p2 + 2][q] = prmt(t1, t3, 0x5410u);
+                ow[2 * p2 + 3][q] = prmt(t1, t3, 0x7632u);
+            }
+        }
+        // a column's 16 rows leave as one 16-byte store; with the neighbouring
+        // lane's 16 they fill a whole 32-byte sector
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            *reinterpret_cast<uint4*>(dst0 + (int64_t)k * R) = make_uint4(ow[k][0], ow[k][1], ow[k][2], ow[k][3]);
+    } else {
+        // scalar path: the E4M3 byte of each code in the integer domain, four
+        // rows at a time (codes and row scales read again from shared memory)
+#pragma unroll 1
+        for (int q = 0; q < 4; q++) {
+            uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int i = 4 * q + j;
+                const uint32_t n8 = codes[((32 * rb + 16 * h + i) ^ h) * 16 + w];
+                const uint32_t sr = sfr[cb * kColRows + 32 * rb + 16 * h + i];
+#pragma unroll
+                for (int k = 0; k < 8; k++) o[k] |= fp8_of_nibble((n8 >> (4 * k)) & 0xFu, sr, sb[k]) << (8 * j);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                *reinterpret_cast<uint32_t*>(dst0 + (int64_t)k * R + 4 * q) = nan ? 0x7F7F7F7Fu : o[k];
+        }
+    }
+    // the four output rows c0 + c + 4 h + k (k = 0..3) sit 16 bytes apart in their 128x4 tile
+    uint8_t* s_dst = sout + sf_offset(c0 + c + 4 * h, r0 / 32 + rb, s_tiles_out);
+#pragma unroll
+    for (int k = 0; k < 4; k++) s_dst[16 * k] = (uint8_t)(h ? sb[4 + k] : sb[k]);
 }
 
 cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st) {
@@ -622,10 +649,8 @@ cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st) {
     if (a.scales_pad && (e = cudaMemsetAsync(a.out_scales, 0, a.scales_bytes, st)) != cudaSuccess) return e;
     const int64_t R = a.rows, C = a.cols;
     dim3 grid((unsigned)((C + kColCols - 1) / kColCols), (unsigned)((R + kColRows - 1) / kColRows));
-    // a column chunk (32 rows) starts at a multiple of 32 bytes from the base
-    const bool wide = (reinterpret_cast<uintptr_t>(a.out_codes) & 31) == 0;
     repack_col_kernel<<<grid, kColThreads, 0, st>>>(a.in_codes, a.in_scales, R, C, (C / 32 + 3) / 4, a.out_codes,
-                                                   a.out_scales, (R / 32 + 3) / 4, wide);
+                                                   a.out_scales, (R / 32 + 3) / 4);
     return cudaGetLastError();
 }
 
