@@ -495,8 +495,12 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
             v = *reinterpret_cast<const uint4*>(in + (r0 + rr) * (C / 2) + c0 / 2 + 16 * ch);
         *reinterpret_cast<uint4*>(&codes[(rr ^ ((rr >> 4) & 1)) * 16 + ch * 4]) = v;
     }
+    // row tid's four scale bytes (the tile's column blocks 0-3) from its 128x4
+    // scale tile; warp k stages rows 32 k .. 32 k + 31, the 32-row block it
+    // encodes, so it also takes each column block's largest and smallest
+    // row scale (a NaN scale is the largest byte), byte cb of smax4 / smin4
+    uint32_t smax4, smin4;
     {
-        // row tid's four scale bytes (the tile's column blocks 0-3) from its 128x4 scale tile
         const int band = tid >> 7;
         uint32_t v = 0;
         if (r0 + 128 * band < R)
@@ -504,6 +508,13 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
                                                    (tid & 31) * 16 + ((tid >> 5) & 3) * 4);
 #pragma unroll
         for (int cb = 0; cb < 4; cb++) sfr[cb * kColRows + tid] = (uint8_t)(v >> (8 * cb));
+        smax4 = smin4 = 0;
+#pragma unroll
+        for (int cb = 0; cb < 4; cb++) {
+            const uint32_t b = (v >> (8 * cb)) & 0xFFu;
+            smax4 |= __reduce_max_sync(0xFFFFFFFFu, b) << (8 * cb);
+            smin4 |= __reduce_min_sync(0xFFFFFFFFu, b) << (8 * cb);
+        }
     }
     __syncthreads();
     const int lane = tid & 31, rb = tid >> 5, w = lane >> 1, h = lane & 1;
@@ -515,16 +526,7 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
     for (int i = 0; i < 16; i++) nb[i] = codes[((32 * rb + 16 * h + i) ^ h) * 16 + w];
     const uint4 s4 = *reinterpret_cast<const uint4*>(&sfr[cb * kColRows + 32 * rb + 16 * h]);
     const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};   // row i's scale: byte i & 3 of word i >> 2
-    // the block's largest and smallest row scale (a NaN scale is the largest byte),
-    // in 16-bit lanes as (sr, 255 - sr)
-    uint32_t mm = 0;
-#pragma unroll
-    for (int i = 0; i < 16; i++) {
-        const uint32_t j = (uint32_t)(i & 3);
-        mm = __viaddmax_u16x2(prmt(sw[i >> 2], 0u, 0x4040u | j | (j << 8)) ^ 0x00FF0000u, 0u, mm);
-    }
-    mm = __viaddmax_u16x2(__shfl_xor_sync(pair, mm, 1), 0u, mm);
-    const uint32_t smax = mm & 0xFFFFu, smin = 255u - (mm >> 16);
+    const uint32_t smax = (smax4 >> (8 * cb)) & 0xFFu, smin = (smin4 >> (8 * cb)) & 0xFFu;
     const bool nan = smax == 0xFFu;
     uint32_t sb[8];
     int g[8];
