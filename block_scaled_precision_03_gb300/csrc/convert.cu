@@ -528,36 +528,45 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
     const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w};   // row i's scale: byte i & 3 of word i >> 2
     const uint32_t smax = (smax4 >> (8 * cb)) & 0xFFu, smin = (smin4 >> (8 * cb)) & 0xFFu;
     const bool nan = smax == 0xFFu;
-    uint32_t sb[8];
-    int g[8];
-    bool fast = !nan && smax - smin <= 14u;
     const uint32_t kr = (15u - smax) * 0x04000400u;    // row factor 2^(sr - smax): sr * 0x04000400 + kr
+    uint32_t SB[4];                                      // scale bytes, columns (0,1) (2,3) (4,5) (6,7)
+    uint32_t Fc[4];                                      // half path: column factors 2^(smax - sb)
+    bool fast = !nan && smax - smin <= 14u;
     if (fast) {
-        uint32_t M[4] = {0u, 0u, 0u, 0u};               // columns (0,1) (2,3) (4,5) (6,7)
+        uint32_t M[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            const uint32_t Fr = prmt(sw[i >> 2], 0u, 0x4440u | (uint32_t)(i & 3)) * 0x04000400u + kr;
-            uint32_t h0, h1, h2, h3;
-            h2_of_e2m1x8(nb[i], h0, h1, h2, h3);
-            M[0] = habsmax2(M[0], hmul2_rn(h0, Fr));
-            M[1] = habsmax2(M[1], hmul2_rn(h1, Fr));
-            M[2] = habsmax2(M[2], hmul2_rn(h2, Fr));
-            M[3] = habsmax2(M[3], hmul2_rn(h3, Fr));
+        for (int q = 0; q < 4; q++) {
+            uint32_t fr[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) fr[j] = prmt(sw[q], 0u, 0x4440u | (uint32_t)j) * 0x04000400u + kr;
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                uint32_t h0, h1, h2, h3;
+                h2_of_e2m1x8(nb[4 * q + j], h0, h1, h2, h3);
+                M[0] = habsmax2(M[0], hmul2_rn(h0, fr[j]));
+                M[1] = habsmax2(M[1], hmul2_rn(h1, fr[j]));
+                M[2] = habsmax2(M[2], hmul2_rn(h2, fr[j]));
+                M[3] = habsmax2(M[3], hmul2_rn(h3, fr[j]));
+            }
         }
-#pragma unroll
-        for (int k = 0; k < 4; k++) M[k] = habsmax2(M[k], __shfl_xor_sync(pair, M[k], 1)) & 0x7FFF7FFFu;
-        // scale byte = floor(log2 amax) - 8 + 127 = exponent field - 23 + smax, clamped to
-        // [0, 254]; 0 for an all-zero column, which takes the factor 2^15 / 2^(smax - 15)
+        // per two columns in 16-bit lanes: scale byte = floor(log2 amax) - 8 + 127
+        // = exponent field - 23 + smax (at least 0; it cannot pass 254 here); the
+        // column factor's exponent field smax + 15 - sb, which must not pass 30
+        // (it is at least 21); an all-zero column gets scale byte 0 and the field 30
         // (any finite factor keeps its zeros)
+        const uint32_t k23 = ((smax - 23u) & 0xFFFFu) * 0x00010001u, k15 = (smax + 15u) * 0x00010001u;
+        uint32_t fmax = 0;
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-            const uint32_t mk = (M[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
-            const int e = (int)(mk >> 10) - 23 + (int)smax;
-            sb[k] = mk == 0 ? 0u : (uint32_t)min(max(e, 0), 254);
-            const int sbp = mk == 0 ? (int)smax - 15 : (int)sb[k];
-            g[k] = 15 - sbp;
-            fast = fast && (int)smax + g[k] <= 30;
+        for (int p2 = 0; p2 < 4; p2++) {
+            const uint32_t Mp = habsmax2(M[p2], __shfl_xor_sync(pair, M[p2], 1)) & 0x7FFF7FFFu;
+            const uint32_t sbv = __viaddmax_s16x2((Mp >> 10) & 0x001F001Fu, k23, 0u);
+            const uint32_t nz = prmt(Mp + 0x7FFF7FFFu, 0u, 0xBB99u);     // 0xFFFF per nonzero column
+            SB[p2] = sbv & nz;
+            const uint32_t F = ((k15 - sbv) & nz) | (0x001E001Eu & ~nz);
+            fmax = __viaddmax_u16x2(F, 0u, fmax);
+            Fc[p2] = F << 10;
         }
+        fast = (fmax & 0xFFFFu) <= 30u && (fmax >> 16) <= 30u;
     } else {
         // column maximum in the integer domain: per column the largest
         // key + 1 = (m >> 1) + 1 + sr over nonzero codes (0 if none), in
@@ -580,30 +589,28 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
         for (int k = 0; k < 4; k++) acc[k] = __viaddmax_s16x2(__shfl_xor_sync(pair, acc[k], 1), 0u, acc[k]);
         // scale bytes: floor(log2 amax) = key - 128, e = that - 8 clamped to [-127, 127]
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-            const int kp = (int)((acc[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);
-            sb[k] = nan ? 0xFFu : (uint32_t)min(max(kp - 10, 0), 254);
-            g[k] = 0;
+        for (int p2 = 0; p2 < 4; p2++) {
+            const int k0 = (int)(acc[p2] & 0xFFFFu), k1 = (int)(acc[p2] >> 16);
+            SB[p2] = nan ? 0x00FF00FFu
+                         : (uint32_t)min(max(k0 - 10, 0), 254) | ((uint32_t)min(max(k1 - 10, 0), 254) << 16);
+            Fc[p2] = 0;
         }
     }
     uint8_t* dst0 = out + (c0 + c) * R + r0 + 32 * rb + 16 * h;
     if (fast) {
-        // column factors 2^(smax - sb) (exponent fields smax + g in [1, 30])
-        uint32_t Fc[4];
-#pragma unroll
-        for (int p2 = 0; p2 < 4; p2++)
-            Fc[p2] = ((uint32_t)((int)smax + g[2 * p2]) << 10) | ((uint32_t)((int)smax + g[2 * p2 + 1]) << 26);
         uint32_t ow[8][4];            // column k, rows 4 q .. 4 q + 3 in word q
 #pragma unroll
         for (int q = 0; q < 4; q++) {
+            uint32_t fr[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) fr[j] = prmt(sw[q], 0u, 0x4440u | (uint32_t)j) * 0x04000400u + kr;
             uint32_t e[4][4];         // row 4 q + j, columns (2 p, 2 p + 1): two E4M3 bytes
 #pragma unroll
             for (int j = 0; j < 4; j++) {
-                const uint32_t Fr = prmt(sw[q], 0u, 0x4440u | (uint32_t)j) * 0x04000400u + kr;
                 uint32_t hh[4];
                 h2_of_e2m1x8(nb[4 * q + j], hh[0], hh[1], hh[2], hh[3]);
 #pragma unroll
-                for (int p2 = 0; p2 < 4; p2++) e[j][p2] = e4m3x2_of_h2(hmul2_rn(hmul2_rn(hh[p2], Fr), Fc[p2]));
+                for (int p2 = 0; p2 < 4; p2++) e[j][p2] = e4m3x2_of_h2(hmul2_rn(hmul2_rn(hh[p2], fr[j]), Fc[p2]));
             }
             // 4 x 4 byte transposes straight from the byte pairs: rows -> columns
 #pragma unroll
@@ -633,7 +640,8 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
                 const uint32_t n8 = codes[((32 * rb + 16 * h + i) ^ h) * 16 + w];
                 const uint32_t sr = sfr[cb * kColRows + 32 * rb + 16 * h + i];
 #pragma unroll
-                for (int k = 0; k < 8; k++) o[k] |= fp8_of_nibble((n8 >> (4 * k)) & 0xFu, sr, sb[k]) << (8 * j);
+                for (int k = 0; k < 8; k++)
+                    o[k] |= fp8_of_nibble((n8 >> (4 * k)) & 0xFu, sr, (SB[k >> 1] >> (16 * (k & 1))) & 0xFFu) << (8 * j);
             }
 #pragma unroll
             for (int k = 0; k < 8; k++)
@@ -642,8 +650,11 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
     }
     // the four output rows c0 + c + 4 h + k (k = 0..3) sit 16 bytes apart in their 128x4 tile
     uint8_t* s_dst = sout + sf_offset(c0 + c + 4 * h, r0 / 32 + rb, s_tiles_out);
-#pragma unroll
-    for (int k = 0; k < 4; k++) s_dst[16 * k] = (uint8_t)(h ? sb[4 + k] : sb[k]);
+    const uint32_t sa = h ? SB[2] : SB[0], sbb = h ? SB[3] : SB[1];
+    s_dst[0] = (uint8_t)sa;
+    s_dst[16] = (uint8_t)(sa >> 16);
+    s_dst[32] = (uint8_t)sbb;
+    s_dst[48] = (uint8_t)(sbb >> 16);
 }
 
 cudaError_t run_repack_col(const RepackArgs& a, cudaStream_t st) {
