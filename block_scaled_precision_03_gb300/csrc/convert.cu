@@ -552,8 +552,9 @@ repack_col_kernel(const uint8_t* __restrict__ in, const uint8_t* __restrict__ si
         // per two columns in 16-bit lanes: scale byte = floor(log2 amax) - 8 + 127
         // = exponent field - 23 + smax (at least 0; it cannot pass 254 here); the
         // column factor's exponent field smax + 15 - sb, which must not pass 30
-        // (it is at least 21); an all-zero column gets scale byte 0 and the field 30
-        // (any finite factor keeps its zeros)
+        // (it is at least 15: 21 unless the scale byte was raised to 0, where every
+        // product stays below 2^8); an all-zero column gets scale byte 0 and the
+        // field 30 (any finite factor keeps its zeros)
         const uint32_t k23 = ((smax - 23u) & 0xFFFFu) * 0x00010001u, k15 = (smax + 15u) * 0x00010001u;
         uint32_t fmax = 0;
 #pragma unroll

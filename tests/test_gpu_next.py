@@ -163,6 +163,55 @@ def test_fp4_row_to_fp8_col_scale_structures(bsq, kind, align):
     bsq.sync_status()
 
 
+@pytest.mark.parametrize("align", [32, 16])
+def test_fp4_row_to_fp8_col_fast_path_edges(bsq, align):
+    """Blocks at the edges of the kernel's half-precision path: row scales
+    spread over exactly 0, 1, 13, 14 (the path's limit), 15 and 40 binades;
+    code 0.5 in a row 14 binades below the block's largest scale (a
+    subnormal half product); columns whose only nonzero codes sit in the
+    lowest-scale rows (a column factor at and beyond its exponent limit),
+    all-zero columns and columns of negative zeros beside full ones; scale
+    bytes near 0 and 254."""
+    from _util import upload_q
+    R, C = 32 * 96, 128
+    rng = np.random.default_rng(733)
+    c4 = rng.integers(0, 16, (R, C)).astype(np.uint8)
+    s_row = np.zeros(R, dtype=np.int64)
+    spreads = [0, 1, 13, 14, 15, 40]
+    for b in range(R // 32):
+        d = spreads[b % len(spreads)]
+        top = int(rng.integers(d + 2, 255)) if b % 7 else (d + 1 if b % 2 else 254)
+        rows = slice(32 * b, 32 * b + 32)
+        sr = top - rng.integers(0, d + 1, 32)
+        sr[0], sr[31] = top, top - d
+        s_row[rows] = sr
+        low = np.flatnonzero(sr == top - d)                 # the block's lowest-scale rows
+        blk = c4[rows]                                      # a view: edits land in c4
+        mode = b % 5
+        cols = rng.choice(C, 24, replace=False)
+        if mode == 1:                                       # code 0.5 (magnitude 1) in the lowest rows only
+            blk[:, cols] = 0
+            blk[np.ix_(low, cols)] = rng.choice([1, 9], (len(low), len(cols)))
+        elif mode == 2:                                     # small codes in the lowest rows only
+            blk[:, cols] = 0
+            blk[np.ix_(low, cols)] = rng.integers(1, 8, (len(low), len(cols)))
+        elif mode == 3:                                     # all-zero and negative-zero columns
+            blk[:, cols[:12]] = 0
+            blk[:, cols[12:]] = 8
+        elif mode == 4:                                     # only rows a few binades below the top
+            mid = np.flatnonzero(sr <= top - min(d, 7))
+            blk[:, cols] = 0
+            if len(mid):
+                blk[np.ix_(mid, cols)] = rng.integers(1, 16, (len(mid), len(cols)))
+    s4 = np.repeat(np.clip(s_row, 0, 254)[:, None], C // 32, axis=1).astype(np.uint8)
+    q4 = upload_q(bsq, "mxfp4", c4, s4)
+    out = codes_at(bsq.empty("mxfp8_e4m3", C, R), align)
+    bsq.mxfp4_to_mxfp8_col_into(q4, out)
+    c8, s8 = oracle.mxfp4_row_to_mxfp8_col(c4, s4)
+    _check_fp8col(out, c8, s8, f"fast-path edges, align {align}")
+    bsq.sync_status()
+
+
 def test_fp4_row_to_fp8_col_from_bf16(bsq):
     # the MoE path: BF16 activations -> MXFP4 rows (GPU) -> FP8 columns (GPU)
     x = inputs.normal_bf16((1024, 7168), 50)
