@@ -359,9 +359,13 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
                     if (leader) tc::mbar_expect_tx(sfull0 + 8 * stage, 2 * CF::SF_TX);
                     uint8_t* sf = smSF + stage * CF::SF_STAGE;
                     tc::tma_load_3d_pair(tc::smem_u32(sf), &tmSFA, 0, kb * CF::SF_ATOMS, ti.a_band, sb);
-                    if (CF::SFB_QUARTERS)
-                        tc::tma_load_4d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, 0, ti.sfb_band,
-                                             kb * CF::SF_ATOMS, sb);
+                    if (CF::SFB_QUARTERS) {
+                        // both CTAs need the same B scale tile: the even CTA loads it once
+                        // into both (multicast); the barrier still counts both copies
+                        if (leader)
+                            tc::tma_load_4d_pair_mc(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, 0, ti.sfb_band,
+                                                    kb * CF::SF_ATOMS, sb, (uint16_t)0x3);
+                    }
                     else
                         tc::tma_load_3d_pair(tc::smem_u32(sf + CF::SFA_BYTES), &tmSFB, 0, kb * CF::SF_ATOMS,
                                              ti.sfb_band, sb);
@@ -558,7 +562,9 @@ gemm2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
             const int n_peer = tc::ld_cluster_s32(tc::mapa(tc::smem_u32((const void*)issued_slot), 1));
             const int sf_own = *sf_issued_slot;
             const int sf_peer = tc::ld_cluster_s32(tc::mapa(tc::smem_u32((const void*)sf_issued_slot), 1));
-            drain_pair_loads(sfull0, S, sf_own, sf_peer, CF::SF_TX);
+            // per scale load the odd CTA's bytes: its own scale tiles (NVFP4: A's only,
+            // the even CTA's multicast carries B's into both)
+            drain_pair_loads(sfull0, S, sf_own, sf_peer, CF::SFB_QUARTERS ? CF::SFA_BYTES : CF::SF_TX);
             drain_pair_loads(full0, S, n_own, n_peer, CF::OP_TX);
         }
     }

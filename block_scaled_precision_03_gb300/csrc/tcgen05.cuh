@@ -136,6 +136,16 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const void* tmap,
                  :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
                  : "memory");
 }
+// The same box into the shared memory of every CTA in `mask` (same offset),
+// one read of global memory; each copy signals the pair's even-CTA barrier.
+__device__ __forceinline__ void tma_load_4d_pair_mc(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                                    int32_t c3, uint32_t bar, uint16_t mask) {
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+                    "h"(mask)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
