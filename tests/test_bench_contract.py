@@ -28,3 +28,26 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_grouped_attainable_bound_limits():
+    """The grouped GEMM's attainable time is, per expert, the larger of its
+    compute time at the tensor peak and the time to stream its weights,
+    activations and BF16 output: one expert holding every row is the plain
+    compute time; experts of one row each are bound by their weight stream."""
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    K, N = 7168, 2048
+    pk = {"hbm_gbs": 1000.0, "fp8_tflops": 1000.0, "fp4_tflops": 3000.0}
+    for fp4, code, peak in ((False, 1.0, 1000.0), (True, 0.5, 3000.0)):
+        step = types.SimpleNamespace(moe_counts=[32768], moe_kn=(K, N))
+        r = bench.attainable(step, 1.0, pk, fp4)
+        t_fl = 2.0 * 32768 * N * K / (peak * 1e12)
+        t_by = (N * K * (code + 1 / 32) + 32768 * K * (code + 1 / 32) + 32768 * N * 2) / 1e12
+        assert abs(r["attainable_ms"] - round(max(t_fl, t_by) * 1e3, 4)) < 1e-9
+        step = types.SimpleNamespace(moe_counts=[1] * 64, moe_kn=(K, N))
+        r = bench.attainable(step, 2.0, pk, fp4)
+        t_w = 64 * (N * K * (code + 1 / 32) + K * (code + 1 / 32) + N * 2) / 1e12
+        assert abs(r["attainable_ms"] - round(t_w * 1e3, 4)) < 1e-9
+        assert abs(r["frac_attainable"] - r["attainable_ms"] / 2.0) <= 1e-4
