@@ -795,7 +795,7 @@ quantize_tile_kernel(const uint16_t* __restrict__ src, int64_t R, int64_t C,
     }
     if (ROW) {
         const int64_t S = C / BLK;
-        if (NBC >= 4) {
+        if constexpr (NBC >= 4) {
             constexpr int GR = NBC / 4;
             for (int id = tid; id < kTile * GR; id += NT) {
                 const int rr = id / GR, gg = id % GR;
