@@ -44,7 +44,7 @@ def test_quantize_rows(bsq, fmt, shape, kind):
     assert_qtensor_equal(row, expected(x, fmt, "row")["row"], f"{fmt} row {shape}")
 
 
-COL_SHAPES = [(256, 256), (96, 200), (32, 8), (4096, 16), (1056, 384), (160, 136)]
+COL_SHAPES = [(256, 256), (96, 200), (32, 8), (4096, 16), (1056, 384), (160, 136), (128, 96), (96, 1056)]
 
 
 @pytest.mark.parametrize("fmt", FMTS)
