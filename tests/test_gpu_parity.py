@@ -363,6 +363,11 @@ GROUPED_CASES = {
     "aligned": (np.array([256, 128, 512, 0, 384], dtype=np.int64), 512, 256),
     # one expert holding every row
     "single": (np.array([1111], dtype=np.int64), 256, 96),
+    # the most experts a call takes: tiny and empty experts (the first three
+    # and the last two empty) and one large one; the device builds its expert
+    # table in passes of 32 boundaries, carried from pass to pass
+    "many": (np.concatenate([[0, 0, 0], np.random.default_rng(256).integers(0, 40, 250), [300], [0, 0]]).astype(np.int64),
+             128, 96),
 }
 
 
