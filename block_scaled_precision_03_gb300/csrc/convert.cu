@@ -94,12 +94,13 @@ __device__ __forceinline__ void st_global_32B(uint4* p, const uint4 a, const uin
 }
 
 constexpr int kRepackThreads = 256;
-constexpr int kRepackUnroll = 4;     // 32-blocks in flight per thread
+constexpr int kRepackUnroll = 2;     // 32-blocks in flight per thread
 
 // Each CTA converts one contiguous range of 32-blocks (row-major order), a
-// thread taking every 256th block, four per iteration so that four 16-byte
+// thread taking every 256th block, two per iteration so that two 16-byte
 // loads are in flight (the kernel is bound by memory latency times the loads
-// in flight per SM).  Rows grow along a thread's walk, so in the grouped
+// in flight per SM; one, four or eight per thread, with their register
+// counts and resident CTAs, measured slower).  Rows grow along a thread's walk, so in the grouped
 // form its expert only moves forward (o_s / p_s: expert row starts and
 // padded scale row starts, built per CTA from the clamped offsets).  The
 // grouped form also writes every other byte of the scale buffer (cap_bytes)
