@@ -663,8 +663,9 @@ __device__ __forceinline__ uint32_t nv_quantize_block(const uint32_t* w, uint32_
 constexpr int kTile = 128;          // tile rows
 constexpr int kTileCols = 64;       // tile columns
 // Resident CTAs per SM the register budget must allow: 9 (56 registers) for
-// the MX formats, 8 for NVFP4 column-wise, 4 (128 registers) for NVFP4 both
-// ways, whose two encodes of each element keep more values live.
+// the MX formats (10, at 48 registers with a few spills, measured slower),
+// 8 for NVFP4 column-wise, 4 (128 registers) for NVFP4 both ways, whose two
+// encodes of each element keep more values live.
 
 
 template <int FMT, bool ROW, bool COL, int TC>
